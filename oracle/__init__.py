@@ -1,0 +1,19 @@
+"""CPU oracle for the multi-head attention sublayer forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check of ``__graft_entry__``
+and the CPU-baseline leg of ``bench.py`` may import this package.  The product
+path (the CUDA library and its Python binding) never calls it and shares no code
+with it.
+
+Every function computes in float64 with NumPy, following the definitions on the
+pages one step at a time.  See ``oracle.mha_ref`` for the citations.
+"""
+from .mha_ref import (  # noqa: F401
+    allowed_keys,
+    attention_weights_ref,
+    sdpa_ref,
+    linear_ref,
+    layernorm_ref,
+    mha_layer_ref,
+    mha_layer_rows_ref,
+)
