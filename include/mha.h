@@ -1,0 +1,157 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head attention sublayer library (libmha.so).
+ *
+ * The operations are those of "Attention Is All You Need" as restated by the Chinese pages
+ * this library follows:
+ *   [LT] lettle.cn translation: 3.1 Encoder and Decoder Stacks (post-norm sublayer),
+ *        3.2.1 缩放点积注意力 (Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V),
+ *        3.2.2 多头注意力 (per-head projections, concat, output projection).
+ *   [JY] "Transformer：抛弃循环与卷积的序列建模" (jiashun-ye.github.io): Multi-Head Attention,
+ *        Transformer 中的三种 Attention (self / masked self / cross attention),
+ *        Residual Connection 与 LayerNorm, 训练样本 (the causal mask), 反向传播 (padding mask).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no
+ *     device memory and keeps no state besides cached per-device properties.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream).  Outputs are
+ *     valid once the caller has synchronised that stream.
+ *   - Row-major layouts; "stride" always counts ELEMENTS, not bytes.
+ *   - dtype MHA_BF16: bf16 storage, fp32 accumulation, bf16 (round-to-nearest-even) outputs,
+ *     tensor-core (tcgen05) kernels.  dtype MHA_F32: fp32 storage and arithmetic (SIMT
+ *     kernels, no TF32).
+ *   - Return value: MHA_OK or a negative mha_status.  Argument errors are found on the host
+ *     before anything is launched.  MHA_ERR_CUDA means a CUDA launch or API call failed.
+ *     Device-side problems (a bounded wait that ran out) are recorded in a device status
+ *     word that mha_debug_last_device_status() reads; no kernel traps.
+ *   - The library needs an sm_103 device (GB300); other devices get MHA_ERR_UNSUPPORTED.
+ */
+#ifndef MHA_GB300_H
+#define MHA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MHA_OK = 0,
+  MHA_ERR_INVALID = -1,        /* bad shape, null pointer, unknown enum, causal with Nq != Nk */
+  MHA_ERR_UNSUPPORTED = -2,    /* valid request this build does not implement (e.g. bf16 d_k != 64) */
+  MHA_ERR_ALIGN = -3,          /* pointer or stride not aligned as the kernel requires */
+  MHA_ERR_WORKSPACE = -4,      /* workspace missing or smaller than mha_layer_workspace_size() */
+  MHA_ERR_CUDA = -5,           /* a CUDA runtime/driver call or a launch failed */
+  MHA_ERR_DEVICE_TIMEOUT = -6  /* a device-side bounded wait ran out (see mha_debug_*) */
+} mha_status;
+
+typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;
+
+/* Mask kinds ([JY] Transformer 中的三种 Attention; 训练样本; 反向传播):
+ *   NONE        every query attends every key;
+ *   CAUSAL      query i attends keys j <= i (Nq must equal Nk);
+ *   KEY_PADDING query rows of batch element b attend keys j < key_len[b]; a row with
+ *               key_len[b] == 0 is written as zeros. */
+typedef enum { MHA_MASK_NONE = 0, MHA_MASK_CAUSAL = 1, MHA_MASK_KEY_PADDING = 2 } mha_mask;
+
+/*
+ * mha_sdpa_fwd -- scaled dot-product attention per (batch, head):
+ *     O[b,h] = softmax(Q[b,h] K[b,h]^T * scale, masked) V[b,h]          ([LT] 3.2.1)
+ *
+ *   Q [B,H,Nq,d_k], K [B,H,Nk,d_k], V [B,H,Nk,d_v], O [B,H,Nq,d_v] (written).
+ *   strides: NULL for contiguous [B,H,N,d] tensors, or 16 int64 element strides laid out as
+ *            {Q: b,h,n,d,  K: b,h,n,d,  V: b,h,n,d,  O: b,h,n,d}.  This lets Q/K/V be read
+ *            straight out of a packed projection buffer and O be written in the head-concat
+ *            layout [B,Nq,H*d_v] (O strides {Nq*H*d_v, d_v, H*d_v, 1}).
+ *   key_len: device int32[B]; required iff mask == MHA_MASK_KEY_PADDING, ignored otherwise.
+ *            Values are clamped to [0, Nk] on the device.
+ *   scale:  > 0 uses the given factor; <= 0 means 1/sqrt(d_k).
+ *   dtype MHA_BF16: d_k == d_v == 64; d strides 1; all other strides multiples of 8 and > 0;
+ *            Q/K/V/O 16-byte aligned (else MHA_ERR_ALIGN).
+ *   dtype MHA_F32:  1 <= d_k, d_v <= 128; pointers 4-byte aligned.
+ * The n x n score matrix is never written to memory.
+ */
+int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                 const int32_t* key_len, float scale,
+                 const void* Q, const void* K, const void* V, void* O,
+                 const int64_t* strides, cudaStream_t stream);
+
+/*
+ * mha_layer_workspace_size -- bytes of device workspace mha_layer_fwd needs for these sizes.
+ * The workspace holds the projected Q/K/V, the head-concat buffer and the W^O output.
+ */
+int mha_layer_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                             size_t* bytes);
+
+/*
+ * mha_layer_fwd -- one post-norm multi-head attention sublayer ([LT] 3.1, 3.2.2; [JY]
+ * Multi-Head Attention, Residual Connection 与 LayerNorm):
+ *     Q_i = x_q W_i^Q + b_i^Q,  K_i = x_kv W_i^K + b_i^K,  V_i = x_kv W_i^V + b_i^V
+ *     head_i = Attention(Q_i, K_i, V_i)            (mask as above)
+ *     A = Concat(head_1..head_H) W^O + b_o
+ *     y = LayerNorm(x_q + A) * gamma + beta        (biased variance, eps = ln_eps)
+ *
+ *   x_q  [B,Nq,D];  x_kv [B,Nk,D], or NULL for self-attention (then Nk must equal Nq).
+ *   W_qkv [H*(2*d_k+d_v), D] in nn.Linear layout [out,in]: rows 0..H*d_k-1 are W^Q (head h
+ *         owns rows h*d_k..), then W^K, then W^V.   b_qkv [H*(2*d_k+d_v)] or NULL (= 0).
+ *   W_o  [D, H*d_v];  b_o [D] or NULL;  gamma, beta [D] or NULL (= 1 and 0).
+ *   y    [B,Nq,D] written; may not alias any input or the workspace.
+ *   All of the above share `dtype`.  key_len as for mha_sdpa_fwd.
+ *   workspace: device buffer of at least mha_layer_workspace_size() bytes, 256-byte aligned,
+ *         owned by the caller; its contents on entry do not matter.
+ *   dtype MHA_BF16 needs d_k == d_v == 64 and D a multiple of 64; MHA_F32 needs d_k, d_v <= 128.
+ * Launches: one or two projection GEMMs, the attention kernel, the W^O GEMM, the residual
+ * LayerNorm -- all on `stream`.
+ */
+int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                  const int32_t* key_len, float ln_eps,
+                  const void* x_q, const void* x_kv, const void* W_qkv, const void* b_qkv,
+                  const void* W_o, const void* b_o, const void* gamma, const void* beta,
+                  void* y, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * mha_linear_fwd -- Y[M,N] = X[M,K] W[N,K]^T + bias[N], the projection step of the sublayer
+ * ([JY] Multi-Head Attention: Q_i = X W_i^Q; the W^O projection of [LT] 3.2.2).
+ *   ldx, ldy: row pitch of X and Y in elements; W is dense [N,K].  bias may be NULL.
+ *   dtype MHA_BF16: K and N multiples of 64, ldx/ldy multiples of 8, 16-byte aligned pointers.
+ */
+int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
+                   const void* bias, void* Y, int64_t ldy, cudaStream_t stream);
+
+/*
+ * mha_residual_layernorm_fwd -- y = LayerNorm(x + a) * gamma + beta over rows of D features
+ * ([LT] 3.1: LayerNorm(x + Sublayer(x))).  x, a, y [M,D] dense; gamma/beta [D] or NULL.
+ *   D a multiple of 8 and at most 2048; 16-byte aligned pointers.
+ */
+int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x, const void* a,
+                               const void* gamma, const void* beta, void* y, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mha_status_string(int status);
+
+/*
+ * mha_debug_last_device_status -- synchronises `stream`, returns the first device-side error
+ * recorded on the current device since the previous call (MHA_OK if none) and clears it.
+ * Meant for tests and debugging; it blocks the host.
+ */
+int mha_debug_last_device_status(cudaStream_t stream);
+
+/*
+ * mha_debug_wait_selftest -- launches one block whose threads wait on a shared-memory
+ * barrier that nothing will complete, with a limit of `timeout_ns` nanoseconds (clamped to
+ * [1e3, 1e9]).  The wait gives up, records MHA_ERR_DEVICE_TIMEOUT in the device status word
+ * and the kernel returns normally.  Exercises the bounded-wait path every kernel uses,
+ * without hanging or faulting the GPU.  Returns the launch status; read the outcome with
+ * mha_debug_last_device_status().
+ */
+int mha_debug_wait_selftest(int64_t timeout_ns, cudaStream_t stream);
+
+/* Library ABI version (major*100 + minor). */
+int mha_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_GB300_H */

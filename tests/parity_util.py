@@ -1,0 +1,42 @@
+"""Comparison helpers and tolerances for the CUDA-vs-oracle parity tests.
+
+Tolerances (stated for the sublayer's outputs):
+* bf16 path (bf16 inputs, fp32 accumulation, bf16 outputs): max |gpu - ref| <= 2e-2 and
+  ||gpu - ref||_2 / ||ref||_2 <= 5e-3.
+* fp32 path: ||gpu - ref||_2 / ||ref||_2 <= 1e-5 and |gpu - ref| <= 1e-5 * max(1, |ref|)
+  elementwise.
+"""
+import numpy as np
+
+BF16_MAX_ABS = 2e-2
+BF16_REL_L2 = 5e-3
+F32_REL = 1e-5
+
+
+def errors(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    d = got - ref
+    max_abs = float(np.abs(d).max()) if d.size else 0.0
+    nref = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(d) / nref) if nref > 0 else float(np.linalg.norm(d))
+    return max_abs, rel
+
+
+def assert_bf16_close(got, ref, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    max_abs, rel = errors(got, ref)
+    assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2, \
+        f"{what}: max|d|={max_abs:.3e} (<= {BF16_MAX_ABS}), relL2={rel:.3e} (<= {BF16_REL_L2})"
+    return max_abs, rel
+
+
+def assert_f32_close(got, ref, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    _, rel = errors(got, ref)
+    bound = F32_REL * np.maximum(1.0, np.abs(ref))
+    worst = float((np.abs(got - ref) / bound).max())
+    assert rel <= F32_REL and worst <= 1.0, f"{what}: relL2={rel:.3e}, worst elem ratio={worst:.3f}"
+    return worst, rel

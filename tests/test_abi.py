@@ -1,0 +1,155 @@
+"""The C ABI on the host: the library builds, loads and exports every symbol include/mha.h
+declares, and argument validation returns its status codes before anything is launched.
+No call here reaches a GPU (they all fail validation first), so this runs without one."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from transformer_head_scaled_04_gb300 import _capi as C
+from transformer_head_scaled_04_gb300 import build as B
+
+HEADER = os.path.join(B.INCLUDE, "mha.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return C.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mha_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ["mha_sdpa_fwd", "mha_layer_fwd", "mha_layer_workspace_size", "mha_status_string",
+                 "mha_debug_last_device_status"]:
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libmha.so does not export {name}"
+    assert set(C.PROTOTYPES) == set(declared_functions())
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mha_abi_version() == 100
+    for code in range(0, -7, -1):
+        s = C.status_string(code)
+        assert s.startswith("MHA_")
+    assert C.status_string(-99) == "unknown mha status"
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: validation fails before any launch
+ODD = ctypes.c_void_p(0x10002)        # 2-byte aligned only
+
+
+def sdpa(lib, B=1, H=1, Nq=4, Nk=4, dk=64, dv=64, dt=1, mask=0, key_len=None, scale=0.0,
+         q=FAKE, k=FAKE, v=FAKE, o=FAKE, strides=None):
+    return lib.mha_sdpa_fwd(B, H, Nq, Nk, dk, dv, dt, mask, key_len, scale, q, k, v, o, strides,
+                            None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), C.MHA_ERR_INVALID),
+    (dict(H=-1), C.MHA_ERR_INVALID),
+    (dict(Nq=0), C.MHA_ERR_INVALID),
+    (dict(dt=7), C.MHA_ERR_INVALID),
+    (dict(mask=3), C.MHA_ERR_INVALID),
+    (dict(mask=1, Nq=4, Nk=5), C.MHA_ERR_INVALID),          # causal needs Nq == Nk
+    (dict(mask=2), C.MHA_ERR_INVALID),                       # key padding needs key_len
+    (dict(q=None), C.MHA_ERR_INVALID),
+    (dict(scale=float("nan")), C.MHA_ERR_INVALID),
+    (dict(dk=32), C.MHA_ERR_UNSUPPORTED),                    # bf16 path is d = 64
+    (dict(dt=0, dk=256), C.MHA_ERR_UNSUPPORTED),             # fp32 path d <= 128
+    (dict(q=ODD), C.MHA_ERR_ALIGN),
+    (dict(dt=0, o=ODD), C.MHA_ERR_ALIGN),
+])
+def test_sdpa_validation(lib, kw, code):
+    assert sdpa(lib, **kw) == code
+
+
+def test_sdpa_stride_validation(lib):
+    bad = (ctypes.c_int64 * 16)(*([256, 256, 64, 2] + [256, 256, 64, 1] * 3))
+    assert sdpa(lib, strides=ctypes.cast(bad, ctypes.c_void_p)) == C.MHA_ERR_UNSUPPORTED
+    bad = (ctypes.c_int64 * 16)(*([256, 256, 60, 1] + [256, 256, 64, 1] * 3))
+    assert sdpa(lib, strides=ctypes.cast(bad, ctypes.c_void_p)) == C.MHA_ERR_ALIGN
+    neg = (ctypes.c_int64 * 16)(*([256, -256, 64, 1] + [256, 256, 64, 1] * 3))
+    assert sdpa(lib, strides=ctypes.cast(neg, ctypes.c_void_p)) == C.MHA_ERR_INVALID
+
+
+def layer(lib, B=2, H=8, Nq=16, Nk=16, D=512, dk=64, dv=64, dt=1, mask=0, key_len=None,
+          eps=1e-5, x_q=FAKE, x_kv=None, W_qkv=FAKE, W_o=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    return lib.mha_layer_fwd(B, H, Nq, Nk, D, dk, dv, dt, mask, key_len, eps, x_q, x_kv, W_qkv,
+                             None, W_o, None, None, None, y, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), C.MHA_ERR_INVALID),
+    (dict(Nk=32), C.MHA_ERR_INVALID),                        # self-attention needs Nq == Nk
+    (dict(x_kv=FAKE, Nk=32, mask=1), C.MHA_ERR_INVALID),     # causal needs Nq == Nk
+    (dict(mask=2), C.MHA_ERR_INVALID),
+    (dict(W_o=None), C.MHA_ERR_INVALID),
+    (dict(eps=-1.0), C.MHA_ERR_INVALID),
+    (dict(dk=32, D=256), C.MHA_ERR_UNSUPPORTED),
+    (dict(D=520), C.MHA_ERR_UNSUPPORTED),
+    (dict(ws=None), C.MHA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), C.MHA_ERR_WORKSPACE),
+    (dict(x_q=ODD), C.MHA_ERR_ALIGN),
+])
+def test_layer_validation(lib, kw, code):
+    assert layer(lib, **kw) == code
+
+
+def test_workspace_size(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_layer_workspace_size(8, 16, 4096, 4096, 1024, 64, 64, 1, ctypes.byref(n)) == 0
+    M = 8 * 4096
+    # Q|K|V + concat + W^O output, bf16
+    assert n.value == 2 * (M * 3 * 1024 + M * 1024 + M * 1024)
+    assert lib.mha_layer_workspace_size(8, 16, 4096, 4096, 1024, 64, 64, 1, None) == \
+        C.MHA_ERR_INVALID
+    n2 = ctypes.c_size_t(0)
+    assert lib.mha_layer_workspace_size(32, 8, 128, 256, 512, 64, 64, 1, ctypes.byref(n2)) == 0
+    assert n2.value == 2 * (32 * 128 * 512 + 32 * 256 * 1024 + 2 * 32 * 128 * 512)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 64, 64, 1), C.MHA_ERR_INVALID),
+    ((8, 64, 60, 1), C.MHA_ERR_UNSUPPORTED),   # bf16 K multiple of 64
+    ((8, 96, 64, 1), C.MHA_ERR_UNSUPPORTED),   # bf16 N multiple of 64
+])
+def test_linear_validation(lib, args, code):
+    M, N, K, dt = args
+    assert lib.mha_linear_fwd(M, N, K, dt, FAKE, K, FAKE, None, FAKE, N, None) == code
+
+
+def test_linear_pitch_and_alignment(lib):
+    assert lib.mha_linear_fwd(8, 64, 64, 1, FAKE, 32, FAKE, None, FAKE, 64, None) == \
+        C.MHA_ERR_INVALID
+    assert lib.mha_linear_fwd(8, 64, 64, 1, FAKE, 68, FAKE, None, FAKE, 64, None) == \
+        C.MHA_ERR_ALIGN
+    assert lib.mha_linear_fwd(8, 64, 64, 1, ODD, 64, FAKE, None, FAKE, 64, None) == \
+        C.MHA_ERR_ALIGN
+
+
+def test_layernorm_validation(lib):
+    f = lib.mha_residual_layernorm_fwd
+    assert f(0, 64, 1, 1e-5, FAKE, FAKE, None, None, FAKE, None) == C.MHA_ERR_INVALID
+    assert f(4, 60, 1, 1e-5, FAKE, FAKE, None, None, FAKE, None) == C.MHA_ERR_UNSUPPORTED
+    assert f(4, 4096, 1, 1e-5, FAKE, FAKE, None, None, FAKE, None) == C.MHA_ERR_UNSUPPORTED
+    assert f(4, 64, 1, 1e-5, FAKE, ODD, None, None, FAKE, None) == C.MHA_ERR_ALIGN
+    assert f(4, 64, 1, float("nan"), FAKE, FAKE, None, None, FAKE, None) == C.MHA_ERR_INVALID
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(C, "_lib", None)
+    monkeypatch.setattr(C, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        C.load()

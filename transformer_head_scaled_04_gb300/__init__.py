@@ -1,0 +1,21 @@
+"""GB300 (sm_103a) multi-head attention sublayer forward: a C-ABI CUDA library
+(libmha.so, declared in include/mha.h) and a thin torch binding of it.
+
+The library itself is loaded lazily on first use; ``build.build()`` compiles it in-tree.
+"""
+from ._capi import (  # noqa: F401
+    LIB_PATH,
+    MASKS,
+    MhaError,
+    load as load_library,
+    status_string,
+)
+from .api import (  # noqa: F401
+    device_status,
+    layer_workspace_size,
+    linear,
+    mha_layer,
+    residual_layernorm,
+    sdpa,
+    wait_selftest,
+)

@@ -1,0 +1,149 @@
+"""torch-facing wrappers of the C ABI.
+
+Argument marshalling only: torch supplies device memory (outputs and workspace are
+allocated with torch when the caller does not pass them) and the current CUDA stream;
+every step of the computation runs in libmha.so's kernels.  There is no CPU fallback: a
+missing library raises, and so does any non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _capi as C
+
+_DTYPES = {torch.float32: C.MHA_F32, torch.bfloat16: C.MHA_BF16}
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+    return _DTYPES[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+
+
+def _stream(dev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _mask(mask) -> int:
+    if isinstance(mask, int):
+        return mask
+    return C.MASKS[mask]
+
+
+def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None):
+    """O = softmax(q k^T * scale) v per (batch, head) via ``mha_sdpa_fwd``.
+
+    q [B,H,Nq,d_k], k [B,H,Nk,d_k], v [B,H,Nk,d_v] (any strides the kernel accepts);
+    out [B,H,Nq,d_v] is allocated if not given and may be a strided view.
+    key_len: int32 CUDA tensor [B] for mask="key_padding".
+    """
+    _cuda(q, k, v, key_len, out)
+    B, H, Nq, d_k = q.shape
+    Nk, d_v = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, d_v), dtype=q.dtype, device=q.device)
+    strides = (ctypes.c_int64 * 16)(*(list(q.stride()) + list(k.stride()) + list(v.stride())
+                                      + list(out.stride())))
+    with torch.cuda.device(q.device):
+        code = C.load().mha_sdpa_fwd(B, H, Nq, Nk, d_k, d_v, _dt(q), _mask(mask), _ptr(key_len),
+                                     float(scale or 0.0), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     ctypes.cast(strides, ctypes.c_void_p), _stream(q.device))
+    C.check(code, "mha_sdpa_fwd")
+    return out
+
+
+def layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype) -> int:
+    n = ctypes.c_size_t(0)
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    C.check(C.load().mha_layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dt, ctypes.byref(n)),
+            "mha_layer_workspace_size")
+    return n.value
+
+
+def mha_layer(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, mask="none", key_len=None,
+              eps=1e-5, d_k=None, d_v=None, workspace=None, out=None):
+    """y = LayerNorm(x_q + MultiHead(x_q, x_kv, x_kv)) via ``mha_layer_fwd``.
+
+    x_q [B,Nq,D]; x_kv [B,Nk,D] or None (self-attention); W_qkv [H*(2d_k+d_v), D];
+    W_o [D, H*d_v]; biases, gamma, beta optional.  workspace: uint8 CUDA tensor of at least
+    ``layer_workspace_size(...)`` bytes (allocated here if None).
+    """
+    _cuda(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, key_len, workspace, out)
+    B, Nq, D = x_q.shape
+    Nk = Nq if x_kv is None else x_kv.shape[1]
+    d_k = D // H if d_k is None else d_k
+    d_v = D // H if d_v is None else d_v
+    for t in (x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("mha_layer takes contiguous tensors")
+    ws = layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, x_q.dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x_q.device)
+    if out is None:
+        out = torch.empty_like(x_q)
+    with torch.cuda.device(x_q.device):
+        code = C.load().mha_layer_fwd(
+            B, H, Nq, Nk, D, d_k, d_v, _dt(x_q), _mask(mask), _ptr(key_len), float(eps),
+            _ptr(x_q), _ptr(x_kv), _ptr(W_qkv), _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma),
+            _ptr(beta), _ptr(out), _ptr(workspace), workspace.numel(), _stream(x_q.device))
+    C.check(code, "mha_layer_fwd")
+    return out
+
+
+def linear(x, W, bias=None, out=None):
+    """Y = x W^T + bias via ``mha_linear_fwd``; x [M,K] (row pitch = x.stride(0)), W [N,K]."""
+    _cuda(x, W, bias, out)
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K or not W.is_contiguous() or x.stride(1) != 1:
+        raise ValueError("linear: x [M,K] with unit column stride and dense W [N,K] expected")
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if tuple(out.shape) != (M, N) or out.stride(1) != 1:
+        raise ValueError(f"linear: out must be [{M},{N}] with unit column stride")
+    with torch.cuda.device(x.device):
+        code = C.load().mha_linear_fwd(M, N, K, _dt(x), _ptr(x), x.stride(0), _ptr(W),
+                                       _ptr(bias), _ptr(out), out.stride(0), _stream(x.device))
+    C.check(code, "mha_linear_fwd")
+    return out
+
+
+def residual_layernorm(x, a, gamma=None, beta=None, eps=1e-5, out=None):
+    """y = LayerNorm(x + a) * gamma + beta over the last axis via ``mha_residual_layernorm_fwd``."""
+    _cuda(x, a, gamma, beta, out)
+    D = x.shape[-1]
+    M = x.numel() // D
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        code = C.load().mha_residual_layernorm_fwd(M, D, _dt(x), float(eps), _ptr(x), _ptr(a),
+                                                   _ptr(gamma), _ptr(beta), _ptr(out),
+                                                   _stream(x.device))
+    C.check(code, "mha_residual_layernorm_fwd")
+    return out
+
+
+def device_status(stream=None) -> int:
+    """First device-side error since the last call on the current device (0 = none); syncs."""
+    s = _stream(torch.cuda.current_device()) if stream is None else stream
+    return C.load().mha_debug_last_device_status(s)
+
+
+def wait_selftest(timeout_ns: int = 1_000_000) -> int:
+    """Run the bounded-wait self test and return the device status it left (expect -6)."""
+    device_status()  # clear anything older
+    C.check(C.load().mha_debug_wait_selftest(int(timeout_ns), _stream(torch.cuda.current_device())),
+            "mha_debug_wait_selftest")
+    return device_status()

@@ -1,0 +1,211 @@
+// gemm_bf16.cu -- Y[M,N] = X[M,K] W[N,K]^T + bias[N] on the sm_103a tensor cores.
+//
+// This is the projection step of the multi-head attention sublayer: the fused Q|K|V
+// projection of every head (N = 3*d_model) and the output projection W^O ("Attention Is All
+// You Need", lettle.cn translation, 3.2.2 多头注意力; "Transformer：抛弃循环与卷积的序列建模",
+// Multi-Head Attention).
+//
+// One CTA computes one 128 x BN output tile:
+//   warp 0     TMA producer: X and W K-slices (64 wide, 128-byte swizzle) into a STAGES ring
+//   warp 1     TMEM owner + MMA issuer: tcgen05.mma kind::f16 128xBNx16, fp32 accumulator in
+//              TMEM, tcgen05.commit frees a ring slot / publishes the finished accumulator
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane quarter per warp), add
+//              bias, round to bf16 (nearest even), store.
+// Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
+// in-flight copies and MMAs land, frees TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+#include "launchers.h"
+
+namespace mha {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;
+constexpr int kErrTimeout = -6;
+
+enum : int { kSiteGemmProducer = 11, kSiteGemmMma = 12, kSiteGemmEpilogue = 13 };
+
+template <int BN>
+struct GemmShape {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr uint32_t kTmemCols = BN;  // power of two >= 32
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
+                          const __grid_constant__ CUtensorMap tmW,
+                          const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ Y,
+                          int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns) {
+  using S = GemmShape<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S::kStages * S::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
+  // bars[0..ST) full, [ST..2ST) empty, [2ST] accumulator ready; tmem slot after them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM;
+  const int n0 = blockIdx.x * BN;
+  const int num_kb = K / kBK;
+
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + S::kStages + s); };
+  const uint32_t acc_bar = smem_u32(bars + 2 * S::kStages);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+    int issued = 0;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % S::kStages;
+      const uint32_t ph = (kb / S::kStages) & 1;
+      if (!mbar_wait(empty_bar(s), ph ^ 1, timeout_ns)) {
+        record_error(status, kErrTimeout, kSiteGemmProducer);
+        break;
+      }
+      mbar_arrive_expect_tx(full_bar(s), S::kStageBytes);
+      tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
+      tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
+      issued = kb + 1;
+    }
+    // let every copy this thread started land before the CTA can exit
+    for (int i = (issued > S::kStages ? issued - S::kStages : 0); i < issued; ++i)
+      (void)mbar_wait(full_bar(i % S::kStages), (i / S::kStages) & 1, timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
+    bool ok = true;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int s = kb % S::kStages;
+      const uint32_t ph = (kb / S::kStages) & 1;
+      if (!mbar_wait(full_bar(s), ph, timeout_ns)) {
+        record_error(status, kErrTimeout, kSiteGemmMma);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA + s * S::kABytes);
+      const uint32_t b0 = smem_u32(sB + s * S::kBBytes);
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
+        const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
+        mma_bf16_ss(tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+      }
+      mma_commit(empty_bar(s));
+    }
+    mma_commit(acc_bar);
+    if (!ok) (void)mbar_wait(acc_bar, 0, timeout_ns);  // drain issued MMAs before TMEM is freed
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row = m0 + quarter * 32 + lane;
+    const bool ok = mbar_wait(acc_bar, 0, timeout_ns);
+    if (!ok) record_error(status, kErrTimeout, kSiteGemmEpilogue);
+    tc_fence_after();
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, r);
+        tmem_wait_ld();
+        reg_fence(r);
+        const int col = n0 + c * 32;
+        if (row < M && col < N) {
+          float bv[32];
+          if (bias != nullptr) {
+            const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 u = __ldg(bp + v);
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float2 f = __bfloat1622float2(h[e]);
+                bv[v * 8 + e * 2] = f.x;
+                bv[v * 8 + e * 2 + 1] = f.y;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) bv[i] = 0.f;
+          }
+          uint4 out[4];
+          uint32_t* o32 = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            o32[i] = pack_bf16x2(__uint_as_float(r[2 * i]) + bv[2 * i],
+                                 __uint_as_float(r[2 * i + 1]) + bv[2 * i + 1]);
+          uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * ldy + col);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = out[v];
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, S::kTmemCols);
+  }
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void* bias, void* Y,
+                      int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+  using S = GemmShape<BN>;
+  auto kern = gemm_bias_bf16_kernel<BN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((N + BN - 1) / BN, (M + kBM - 1) / kBM);
+  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW,
+                                             static_cast<const __nv_bfloat16*>(bias),
+                                             static_cast<__nv_bfloat16*>(Y), M, N, K, ldy,
+                                             ctx.status, ctx.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
+                             const void* bias, void* Y, int M, int N, int K, int64_t ldy,
+                             const DevCtx& ctx, cudaStream_t s) {
+  if (block_n == 256) return launch_bn<256>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+  return launch_bn<128>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+}
+
+}  // namespace mha

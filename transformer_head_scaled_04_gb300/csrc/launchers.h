@@ -1,0 +1,53 @@
+// launchers.h -- host-side entry points of the kernels, used by the C ABI layer (capi.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mha {
+
+// Per-launch device context: where kernels record errors, and how long a bounded wait may
+// spin before it gives up.
+struct DevCtx {
+  int* status;          // 4-int device status block (see device_common.cuh)
+  uint64_t timeout_ns;  // limit of every mbarrier wait
+  int num_sms;
+};
+
+// ---- projections: Y[M,N] = X[M,K] W[N,K]^T + bias
+// bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W
+// {K, N}, box {64, block_n}; both 128-byte swizzled.  block_n is 128 or 256.
+cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
+                             const void* bias, void* Y, int M, int N, int K, int64_t ldy,
+                             const DevCtx& ctx, cudaStream_t s);
+cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
+                            float* Y, int64_t ldy, int M, int N, int K, cudaStream_t s);
+
+// ---- attention
+struct SdpaArgs {
+  int B, H, Nq, Nk, d_k, d_v;
+  int mask;                  // mha_mask
+  const int32_t* key_len;    // device, B entries (key padding) or null
+  float scale;               // multiplies q.k
+  const void* Q;             // used by the f32 path (the bf16 path reads through TMA maps)
+  const void* K;
+  const void* V;
+  void* O;
+  int64_t sq[4], sk[4], sv[4], so[4];  // element strides b, h, n, d
+};
+// bf16: Q/K/V through 4-D TMA maps {d, n, h, b} with box {64, 128, 1, 1}, 128-byte swizzle.
+cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, const SdpaArgs& a, const DevCtx& ctx,
+                             cudaStream_t s);
+cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s);
+
+// ---- residual + LayerNorm: y = LN(x + a) * gamma + beta
+cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,
+                                      const void* a, const void* gamma, const void* beta,
+                                      void* y, cudaStream_t s);
+
+// ---- bounded-wait self test (waits on a barrier nothing completes)
+cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t s);
+
+}  // namespace mha
