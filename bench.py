@@ -1,0 +1,447 @@
+#!/usr/bin/env python3
+"""Throughput of the multi-head attention sublayer forward on GB300; prints ONE JSON line.
+
+A step is one pass of the whole sublayer -- Q|K|V projection, fused attention, W^O
+projection, residual + LayerNorm -- over one batch of the big-model long-sequence workload
+(d_model=1024, 16 heads, d_k=d_v=64, B=8, n=4096, bf16, no mask), through the library's
+C ABI with inputs resident in HBM.  The causal variant of the same workload is measured too
+and reported beside it.  L2 is flushed (a 256 MiB buffer written) before every timed step;
+each step is timed on its stream with CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (float64 NumPy) on a bounded sample of the same
+workload per step, on the host cores; under torchrun only rank 0 does that work.
+With N > 1 (torchrun) every rank runs its own replica on its own GPU: the path needs no
+exchange, so there is no collective besides the barrier and the max of the step times.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "SDPA/MHA fwd TFLOP/s & % of GB300 bf16 tensor peak; MHA-layer tokens/s"
+WORKLOAD = "big_long_b8_n4096"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- work model
+
+def attention_pairs(B, H, Nq, Nk, mask, key_len=None) -> int:
+    """(query, key) pairs the mask allows, summed over batch and heads."""
+    if mask == "causal":
+        per = Nq * (Nq + 1) // 2
+        return B * H * per
+    if mask == "key_padding":
+        return H * Nq * int(np.clip(key_len, 0, Nk).sum())
+    return B * H * Nq * Nk
+
+
+def sdpa_flops(w: si.Workload, mask: str, key_len=None) -> float:
+    """Algorithmic attention FLOPs: 2*(d_k + d_v) per allowed (query, key) pair."""
+    return 2.0 * (w.d_k + w.d_v) * attention_pairs(w.B, w.H, w.Nq, w.Nk, mask, key_len)
+
+
+def layer_flops(w: si.Workload, mask: str, key_len=None) -> float:
+    Mq, Mk, D = w.B * w.Nq, w.B * w.Nk, w.D
+    proj = 2.0 * Mq * D * w.H * w.d_k + 2.0 * Mk * D * w.H * (w.d_k + w.d_v)
+    out = 2.0 * Mq * w.H * w.d_v * D
+    return proj + sdpa_flops(w, mask, key_len) + out
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (read only) in a thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import torch
+
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(torch_device_index)
+            uuid = ("GPU-" + str(props.uuid)).encode()
+            if nv.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(torch_device_index, ctypes.byref(h)) != 0:
+                    return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self._reasons_fn(self.h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml unavailable"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for bit, n in self.REASONS.items() if self.reasons & bit],
+                "samples": len(self.samples), "source": "nvml, polled during the timed steps"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (OpenBLAS query when available, else the core count)."""
+    try:
+        with open("/proc/self/maps") as f:
+            libs = {ln.split()[-1] for ln in f if "openblas" in ln.lower() and ".so" in ln}
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                         "openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    return int(fn())
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(inp, w, mask, b, rows):
+    """Run the oracle on query rows `rows` of batch element b; returns its algorithmic FLOPs."""
+    import oracle
+
+    oracle.mha_layer_rows_ref(inp["x_q"], None, inp["W_qkv"], inp["b_qkv"], inp["W_o"],
+                              inp["b_o"], inp["gamma"], inp["beta"], w.H, b, rows, mask)
+    n = len(rows)
+    D = w.D
+    proj = 2.0 * n * D * w.H * w.d_k + 2.0 * w.Nk * D * w.H * (w.d_k + w.d_v)
+    if mask == "causal":
+        pairs = int(np.sum(np.asarray(rows) + 1)) * w.H
+    else:
+        pairs = n * w.Nk * w.H
+    return proj + 2.0 * (w.d_k + w.d_v) * pairs + 2.0 * n * w.H * w.d_v * D
+
+
+def cpu_baseline(inp, w, mask, budget_s=12.0):
+    """The oracle as it stands, timed on this host on whole batch elements (all 4096 query
+    rows each) until about `budget_s` seconds of work have run."""
+    flops, t0, done = 0.0, time.perf_counter(), 0
+    rows = np.arange(w.Nq)
+    while done < w.B:
+        flops += oracle_sample(inp, w, mask, done, rows)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"{done} of {w.B} batch elements (all {w.Nq} query rows, {mask} mask) of "
+                      f"the same workload, float64 NumPy, {el:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def common_fields(args, world):
+    w = si.WORKLOADS[WORKLOAD]
+    return {
+        "metric": METRIC,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "data": "synthetic: seeded N(0,1) activations, Xavier-uniform weights, zero biases, "
+                "gamma=1, beta=0 (no datasets or trained weights involved)",
+        "config": {"workload": f"{WORKLOAD}: full MHA sublayer forward (QKV projection, fused "
+                               f"SDPA, W^O, residual+LayerNorm), d_model={w.D}, h={w.H}, "
+                               f"d_k=d_v={w.d_k}, B={w.B}, n={w.Nq}, mask none",
+                   "batch": w.B, "seq_len": w.Nq, "d_model": w.D, "heads": w.H, "mask": "none",
+                   "l2": "flushed: a 256 MiB buffer is written before every timed step",
+                   "parallelism": "replicas (each rank its own batch; no collective)"},
+    }
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = si.WORKLOADS[WORKLOAD]
+    inp = si.draw_layer(w)
+    g = np.random.Generator(np.random.PCG64(1234))
+    n_rows = 256
+
+    def step(i):
+        b = i % w.B
+        rows = np.sort(g.choice(w.Nq, n_rows, replace=False))
+        return oracle_sample(inp, w, "none", b, rows)
+
+    for i in range(args.warmup):
+        step(i)
+    flops, t0 = 0.0, time.perf_counter()
+    for i in range(args.steps):
+        flops += step(i)
+    el = time.perf_counter() - t0
+    value = flops / el / 1e12
+    out = common_fields(args, world)
+    out.update({
+        "impl": "reference",
+        "value": value,
+        "unit": "TFLOP/s",
+        "ms_per_step": el / args.steps * 1e3,
+        "dtype": "f64",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"per step: {n_rows} random query rows of one batch element "
+                                   f"(K/V projected in full), float64 NumPy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    })
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    from transformer_head_scaled_04_gb300 import _capi as C
+    from transformer_head_scaled_04_gb300 import build as B
+
+    if rank == 0:
+        B.build()
+    if pg:
+        pg.barrier()
+    lib = C.load()
+
+    w = si.WORKLOADS[WORKLOAD]
+    inp = si.draw_layer(w)
+    bf = torch.bfloat16
+    t = {k: (None if v is None else torch.from_numpy(v).to(dev, bf)) for k, v in inp.items()
+         if k != "key_len"}
+    ws_n = ctypes.c_size_t(0)
+    C.check(lib.mha_layer_workspace_size(w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16,
+                                         ctypes.byref(ws_n)), "workspace")
+    ws = torch.empty(ws_n.value, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(t["x_q"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+
+    def layer(mask, x_q=None, out=None, events=None):
+        xq = t["x_q"] if x_q is None else x_q
+        yo = y if out is None else out
+        a = (w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16, C.MASKS[mask], None, 1e-5,
+             vp(xq), None, vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]), vp(t["b_o"]),
+             vp(t["gamma"]), vp(t["beta"]), vp(yo), vp(ws), ws_n.value, sp)
+        if events is None:
+            C.check(lib.mha_layer_fwd(*a), "mha_layer_fwd")
+        else:
+            arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in events])
+            C.check(lib.mha_layer_fwd_timed(*a, ctypes.cast(arr, ctypes.c_void_p), 5),
+                    "mha_layer_fwd_timed")
+
+    def timed(mask, steps, warmup):
+        for _ in range(warmup):
+            flush.zero_()
+            layer(mask)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+        for row in evs:  # create the event handles before they go through the C ABI
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as clk:
+            for i in range(steps):
+                flush.zero_()
+                layer(mask, events=evs[i])
+            torch.cuda.synchronize(dev)
+        if pg:
+            pg.barrier()
+        per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(4)]
+                        for i in range(steps)])  # ms: projection, sdpa, out-proj, LN
+        return per, clk.summary()
+
+    per, clocks = timed("none", args.steps, args.warmup)
+    step_ms = float(per.sum(axis=1).mean())
+    if pg:
+        tt = torch.tensor([step_ms], device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    sdpa_ms = float(per[:, 1].mean())
+    fl_layer = layer_flops(w, "none")
+    fl_sdpa = sdpa_flops(w, "none")
+    value = world * fl_layer / (step_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    sdpa_tf = fl_sdpa / (sdpa_ms * 1e-3) / 1e12
+
+    # causal variant of the same workload (reported beside the headline)
+    per_c, _ = timed("causal", max(3, args.steps // 2), args.warmup)
+    c_step = float(per_c.sum(axis=1).mean())
+    c_sdpa = float(per_c[:, 1].mean())
+    fl_c = layer_flops(w, "causal")
+    fl_c_sdpa = sdpa_flops(w, "causal")
+
+    # end to end through the public API: pinned host x -> device, sublayer, y -> pinned host
+    x_host = t["x_q"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(t["x_q"])
+    y_dev = torch.empty_like(t["x_q"])
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer("none", x_q=x_dev, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_ms = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        layer("none", x_q=x_dev, out=y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e_ms.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.mean(e_ms))
+    status = lib.mha_debug_last_device_status(sp)
+    if status != 0:
+        raise SystemExit(f"device status {status}: {C.status_string(status)}")
+
+    out = common_fields(args, world)
+    out.update({
+        "value": value,
+        "unit": "TFLOP/s",
+        "ms_per_step": step_ms,
+        "dtype": "bf16",
+        "tokens_per_s": world * w.B * w.Nq / (step_ms * 1e-3),
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "layer_flops_per_step": fl_layer,
+        "step_breakdown_ms": {"qkv_proj": float(per[:, 0].mean()), "sdpa": sdpa_ms,
+                              "out_proj": float(per[:, 2].mean()),
+                              "residual_layernorm": float(per[:, 3].mean())},
+        "roofline": {"kernel": "sdpa_fwd_bf16_kernel", "bound": "tensor", "achieved": sdpa_tf,
+                     "peak": peak, "unit": "TFLOP/s", "frac": sdpa_tf / peak,
+                     "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
+                     if peak_src == "measured" else "fallback 1900 TFLOP/s",
+                     "algorithmic_flops_per_launch": fl_sdpa,
+                     "traffic": None},
+        "causal": {"value": fl_c / (c_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "ms_per_step": c_step, "sdpa_tflops": fl_c_sdpa / (c_sdpa * 1e-3) / 1e12,
+                   "sdpa_frac": fl_c_sdpa / (c_sdpa * 1e-3) / 1e12 / peak,
+                   "tokens_per_s": w.B * w.Nq / (c_step * 1e-3)},
+        "e2e": {"value": fl_layer / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    })
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(inp, w, "none")
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the timed CPU oracle sample")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # timing rule: at least three untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

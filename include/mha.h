@@ -111,6 +111,21 @@ int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
                   void* y, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * mha_layer_fwd_timed -- mha_layer_fwd plus profiling marks: events[0..4] (created by the
+ * caller, n_events >= 5) are recorded on `stream` before the Q/K/V projection(s), before the
+ * attention kernel, before the W^O projection, before the residual LayerNorm and after it, so
+ * that cudaEventElapsedTime between consecutive marks is each step's device time.  Same
+ * arguments, results and errors as mha_layer_fwd; MHA_ERR_INVALID if events is NULL,
+ * n_events < 5 or one of the five is NULL.
+ */
+int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps,
+                        const void* x_q, const void* x_kv, const void* W_qkv, const void* b_qkv,
+                        const void* W_o, const void* b_o, const void* gamma, const void* beta,
+                        void* y, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                        const cudaEvent_t* events, int n_events);
+
+/*
  * mha_linear_fwd -- Y[M,N] = X[M,K] W[N,K]^T + bias[N], the projection step of the sublayer
  * ([JY] Multi-Head Attention: Q_i = X W_i^Q; the W^O projection of [LT] 3.2.2).
  *   ldx, ldy: row pitch of X and Y in elements; W is dense [N,K].  bias may be NULL.

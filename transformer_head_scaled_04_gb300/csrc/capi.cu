@@ -302,11 +302,19 @@ int mha_layer_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d
   return MHA_OK;
 }
 
-int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
-                  const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
-                  const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
-                  const void* gamma, const void* beta, void* y, void* workspace,
-                  size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// ev: null, or 5 events recorded on `stream` at the step boundaries (before the projections,
+// before attention, before the output projection, before the residual LayerNorm, after it).
+int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+               const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+               const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+               const void* gamma, const void* beta, void* y, void* workspace, size_t ws_bytes,
+               cudaStream_t stream, const cudaEvent_t* ev) {
+  auto mark = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], stream);
+  };
   int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
   if (st != MHA_OK) return st;
   if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
@@ -341,6 +349,7 @@ int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
   a.key_len = (mask == MHA_MASK_KEY_PADDING) ? key_len : nullptr;
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
 
+  mark(0);
   if (self) {
     // one GEMM: [Mq, D] x [2*nqk + nv, D]^T -> Q|K|V interleaved per token
     const int ld = 2 * nqk + nv;
@@ -381,16 +390,45 @@ int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
   a.so[2] = nv;
   a.so[3] = 1;
   if (self) a.sv[1] = d_v;
+  mark(1);
   st = run_sdpa(a, dtype, ctx, stream);
   if (st != MHA_OK) return st;
   // A = C W_o^T + b_o
   uint8_t* A = ws + plan.off_a;
+  mark(2);
   st = run_linear(Mq, D, nv, dtype, C, nv, W_o, b_o, A, D, ctx, stream);
   if (st != MHA_OK) return st;
   // y = LayerNorm(x_q + A)
+  mark(3);
   cudaError_t e =
       mha::launch_residual_layernorm(dtype, Mq, D, ln_eps, x_q, A, gamma, beta, y, stream);
+  mark(4);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                  const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                  const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                  const void* gamma, const void* beta, void* y, void* workspace,
+                  size_t ws_bytes, cudaStream_t stream) {
+  return layer_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv, W_qkv,
+                    b_qkv, W_o, b_o, gamma, beta, y, workspace, ws_bytes, stream, nullptr);
+}
+
+int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps, const void* x_q,
+                        const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                        const void* b_o, const void* gamma, const void* beta, void* y,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream,
+                        const cudaEvent_t* events, int n_events) {
+  if (events == nullptr || n_events < 5) return MHA_ERR_INVALID;
+  for (int i = 0; i < 5; ++i)
+    if (events[i] == nullptr) return MHA_ERR_INVALID;
+  return layer_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv, W_qkv,
+                    b_qkv, W_o, b_o, gamma, beta, y, workspace, ws_bytes, stream, events);
 }
 
 int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
