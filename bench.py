@@ -63,6 +63,23 @@ def layer_flops(w: si.Workload, mask: str, key_len=None) -> float:
     return proj + sdpa_flops(w, mask, key_len) + out
 
 
+def recorded_traffic(kernel: str, sources: list[str]):
+    """Per-launch DRAM bytes from the committed ncu record, or None once the kernel's sources
+    no longer match the ones the counters were taken on."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        m = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
+        return rec["traffic_bytes"] if m.hexdigest()[:16] == rec["source_sha256_16"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -406,7 +423,10 @@ def run_ours(args):
                      "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
                      if peak_src == "measured" else "fallback 1900 TFLOP/s",
                      "algorithmic_flops_per_launch": fl_sdpa,
-                     "traffic": None},
+                     "traffic": recorded_traffic("sdpa_fwd_bf16_kernel", [
+                         "transformer_head_scaled_04_gb300/csrc/sdpa_bf16.cu",
+                         "transformer_head_scaled_04_gb300/csrc/device_common.cuh"]),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)"},
         "causal": {"value": fl_c / (c_step * 1e-3) / 1e12, "unit": "TFLOP/s",
                    "ms_per_step": c_step, "sdpa_tflops": fl_c_sdpa / (c_sdpa * 1e-3) / 1e12,
                    "sdpa_frac": fl_c_sdpa / (c_sdpa * 1e-3) / 1e12 / peak,
