@@ -126,6 +126,36 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         const cudaEvent_t* events, int n_events);
 
 /*
+ * mha_layer_fwd_noalloc -- mha_layer_fwd for callers that cannot supply a workspace.
+ * The pages have no counterpart: this is a packaging variant, not part of the method.
+ *
+ * Who needs it: code that may not allocate device memory -- e.g. a plugin whose host
+ * framework owns all GPU memory and forbids allocation inside its enqueue callback, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit device synchronisation.
+ * Instead of a caller buffer, it uses a 48 MiB scratch area built into the library (a
+ * file-scope __device__ array that stays resident on every GPU that loads the library until
+ * the process exits).  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, results and errors are those of mha_layer_fwd without workspace/ws_bytes.
+ * Sizes whose mha_layer_workspace_size() exceeds 48 MiB (50331648 bytes) return
+ * MHA_ERR_WORKSPACE before anything is launched.
+ * The first call on each device looks up the scratch area's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.
+ * All calls on one device share that device's scratch area, which keeps the previous
+ * call's intermediates; nothing in it needs clearing (every byte a call reads, the same call
+ * has written first).  Calls on the same device that can overlap on the GPU (issued to
+ * streams with no ordering between them) race on the scratch and corrupt each other's
+ * results: order them, e.g. issue them to one stream.  Each device has its own copy, so
+ * calls on different devices do not interfere.
+ */
+int mha_layer_fwd_noalloc(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                          int mask, const int32_t* key_len, float ln_eps,
+                          const void* x_q, const void* x_kv, const void* W_qkv,
+                          const void* b_qkv, const void* W_o, const void* b_o,
+                          const void* gamma, const void* beta, void* y, cudaStream_t stream);
+
+/*
  * mha_linear_fwd -- Y[M,N] = X[M,K] W[N,K]^T + bias[N], the projection step of the sublayer
  * ([JY] Multi-Head Attention: Q_i = X W_i^Q; the W^O projection of [LT] 3.2.2).
  *   ldx, ldy: row pitch of X and Y in elements; W is dense [N,K].  bias may be NULL.

@@ -27,6 +27,7 @@ PROTOTYPES = {
     "mha_layer_fwd": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10 + [_size, _vp]),
     "mha_layer_fwd_timed": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10
                             + [_size, _vp, _vp, _c_int]),
+    "mha_layer_fwd_noalloc": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 9 + [_vp]),
     "mha_linear_fwd": (_c_int, [_c_int] * 4 + [_vp, _i64, _vp, _vp, _vp, _i64, _vp]),
     "mha_residual_layernorm_fwd": (_c_int, [_c_int] * 3 + [_c_float] + [_vp] * 6),
     "mha_status_string": (ctypes.c_char_p, [_c_int]),

@@ -1,0 +1,75 @@
+// layer_noalloc.cu -- mha_layer_fwd_noalloc: the sublayer forward for callers that cannot
+// hand the library a workspace.
+//
+// mha_layer_fwd needs a caller-provided device workspace for its intermediates (the
+// projected Q/K/V, the head-concat buffer and the W^O output).  Some callers have no way to
+// obtain one: a plugin running inside a host framework that owns every byte of device memory
+// and forbids allocations from its enqueue callback, or code on a latency-critical path
+// where cudaMalloc's implicit device synchronisation is not acceptable.  For them this file
+// keeps a fixed scratch area in the library itself, in a file-scope __device__ array that the
+// CUDA runtime places in device memory when it loads this module on a device.  It stays
+// there, on every GPU that loads the library, until the process exits.
+//
+// Nothing here calls cudaMalloc, cudaFree or any allocating routine.  The entry point only
+// looks up the array's device address (once per device) and forwards to mha_layer_fwd.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/mha.h"
+
+// Largest workspace the no-alloc entry point can serve: 48 MiB, enough for every base-model
+// workload (d_model 512, up to 8192 query tokens of self-attention per call).
+static constexpr size_t kLayerScratchBytes = static_cast<size_t>(48) << 20;
+
+// The scratch itself.  Host code must not use this name as a pointer: on the host it is only
+// a stand-in for the symbol, so the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_layer_scratch[kLayerScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_layer_scratch on the current device, looked up on the first call per
+// device (with that device current) and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MHA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_layer_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return MHA_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" int mha_layer_fwd_noalloc(int B, int H, int Nq, int Nk, int D, int d_k, int d_v,
+                                     int dtype, int mask, const int32_t* key_len, float ln_eps,
+                                     const void* x_q, const void* x_kv, const void* W_qkv,
+                                     const void* b_qkv, const void* W_o, const void* b_o,
+                                     const void* gamma, const void* beta, void* y,
+                                     cudaStream_t stream) {
+  size_t need = 0;
+  int st = mha_layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype, &need);
+  if (st != MHA_OK) return st;
+  if (need > kLayerScratchBytes) return MHA_ERR_WORKSPACE;  // beyond the built-in 48 MiB
+  void* ws = nullptr;
+  st = scratch_address(&ws);
+  if (st != MHA_OK) return st;
+  // Every region of the workspace is fully written before it is read, so the previous
+  // call's contents need no clearing.
+  return mha_layer_fwd(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
+                       W_qkv, b_qkv, W_o, b_o, gamma, beta, y, ws, kLayerScratchBytes, stream);
+}
