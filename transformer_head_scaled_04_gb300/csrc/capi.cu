@@ -9,7 +9,7 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "../../include/mha.h"
+#include "mha.h"
 #include "device_common.cuh"
 #include "launchers.h"
 

@@ -16,7 +16,7 @@
 
 #include <mutex>
 
-#include "../../include/mha.h"
+#include "mha.h"
 
 // Largest workspace the no-alloc entry point can serve: 48 MiB, enough for every base-model
 // workload (d_model 512, up to 8192 query tokens of self-attention per call).

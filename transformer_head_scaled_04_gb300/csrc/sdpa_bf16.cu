@@ -7,20 +7,25 @@
 //
 // The n x n score matrix never leaves the SM.  One CTA owns 256 query rows (two 128-row
 // tiles t = 0, 1) of one (b, h) and streams K/V in 128-row tiles:
-//   warp 8     TMA producer: Q tiles once, then K_j and V_j into a 3-stage ring
-//   warp 9     TMEM owner + MMA issuer (one thread):
+//   warp 8     TMA producer: Q tiles once, then K and V through separate 4-stage rings
+//              (K one tile ahead; a K slot frees as soon as Q K^T has read it)
+//   warp 9     TMEM owner + MMA issuer (one thread) -- warps 8-11 form the control
+//              warpgroup, which hands most of its registers to the softmax warpgroups:
 //                S_t = Q_t K_j^T           tcgen05.mma 128x128x16 x4, fp32 in TMEM
-//                O_t += P_t V_j            tcgen05.mma 128x64x16 x8, P from smem, V MN-major
-//              The two tiles ping-pong so the tensor core works on one tile while the
-//              softmax warps of the other run.
+//                O_t += P_t V_j            tcgen05.mma 128x64x16 x8, P from TMEM, V MN-major
+//              S_t(j+1) is issued as soon as the softmax warps have read S_t(j) out of TMEM,
+//              so the next product runs during this tile's exponentials; the two tiles keep
+//              the tensor core busy while either tile's softmax runs.
 //   warps 0-7  softmax: warpgroup t owns tile t, one query row per thread (its TMEM lane).
-//              tcgen05.ld of the S row, mask, running max m and sum l, p = 2^(s*c - m*c)
-//              with c = scale*log2(e), P rounded to bf16 into a 128-byte-swizzled smem tile.
+//              One tcgen05.ld round trip brings the whole 128-key S row into registers;
+//              mask, running max m and sum l, p = 2^(s*c - m*c) with c = scale*log2(e)
+//              (paired fp32 FMA / add), P rounded to bf16 and stored back into TMEM.
 //              O is rescaled (in TMEM) only when the max grows by more than 2^8; the final
 //              O / l uses the same max as every p, so the result equals the softmax exactly
 //              up to rounding.  At the end: O / l -> bf16 -> global, in any strided layout
 //              (the head-concat layout [B, Nq, H*64] in the sublayer).
-// Whole K/V tiles past the causal diagonal or past key_len[b] are never loaded.
+// Whole K/V tiles past the causal diagonal or past key_len[b] are never loaded.  The query
+// blocks of one (b, h) are adjacent in the grid, so they run together and share K/V in L2.
 // Every wait is bounded (see device_common.cuh); a timeout records MHA_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -35,18 +40,28 @@ namespace {
 constexpr int kBQ = 128;       // query rows per tile
 constexpr int kBKV = 128;      // keys per K/V tile
 constexpr int kHD = 64;        // head dim (d_k = d_v)
-constexpr int kStages = 3;     // K/V ring depth
-constexpr int kThreads = 320;  // 8 softmax warps + producer + MMA
+constexpr int kKStages = 4;    // K ring depth
+constexpr int kVStages = 4;    // V ring depth
+constexpr int kThreads = 384;  // 8 softmax warps, then producer, MMA and two idle warps
+// register split (setmaxnreg): ptxas gives this 384-thread kernel 168 registers per thread,
+// a launch pool of 384 x 168 = 64512; the softmax warpgroups take 216, the control
+// warpgroup gives back down to 56: 256 x 216 + 128 x 56 = 62464 <= 64512.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 56;
+static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs <= kThreads * 168,
+              "register split exceeds the launch allocation");
 constexpr int kTileBytes = kBQ * kHD * 2;  // 16 KB: a 128 x 64 bf16 tile
-constexpr int kPBytes = kBQ * kBKV * 2;    // 32 KB: a 128 x 128 bf16 P tile
 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = 1024 + kOffBar + 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384) P0 [384,448) P1 [448,512)
+// (P holds 128 bf16 per row, two per 32-bit column)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
 
 constexpr int kErrTimeout = -6;
 enum : int {
@@ -60,10 +75,12 @@ enum : int {
 // barrier indices
 constexpr int kBarQ = 0;
 constexpr int kBarKFull = 1;
-constexpr int kBarVFull = kBarKFull + kStages;
-constexpr int kBarKVEmpty = kBarVFull + kStages;
-constexpr int kBarSFull = kBarKVEmpty + kStages;  // 2
-constexpr int kBarPFull = kBarSFull + 2;          // 2
+constexpr int kBarKEmpty = kBarKFull + kKStages;
+constexpr int kBarVFull = kBarKEmpty + kKStages;
+constexpr int kBarVEmpty = kBarVFull + kVStages;
+constexpr int kBarSFull = kBarVEmpty + kVStages;  // 2
+constexpr int kBarSFree = kBarSFull + 2;          // 2
+constexpr int kBarPFull = kBarSFree + 2;          // 2
 constexpr int kBarODone = kBarPFull + 2;          // 2
 constexpr int kBarDrain = kBarODone + 2;
 constexpr int kNumBars = kBarDrain + 1;
@@ -94,13 +111,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sK = smem_u32(smem + kOffK);
   const uint32_t sV = smem_u32(smem + kOffV);
-  uint8_t* const sP = smem + kOffP;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int b = blockIdx.y;
-  const int q0 = (gridDim.z - 1 - blockIdx.z) * (2 * kBQ);  // heaviest causal blocks first
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int q0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBQ);  // heaviest causal block first
 
   // keys a row may see: causal -> j <= row; otherwise j < L
   int L = p.Nk;
@@ -117,16 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       n_t[t] = (L + kBKV - 1) / kBKV;
   }
   const int nmax = max(n_t[0], n_t[1]);
+  const int n0 = n_t[0], n1 = n_t[1];
+  auto ntiles = [n0, n1](int t) { return t == 0 ? n0 : n1; };  // no dynamic array index
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarKVEmpty + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarSFree + t), 4);  // one arrival per softmax warp
       mbar_init(bar(kBarPFull + t), kBQ);
       mbar_init(bar(kBarODone + t), 1);
     }
@@ -142,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= 8) regs_dec<kControlRegs>();  // first thing: the softmax increase waits on it
   if (warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && nmax > 0) {
@@ -152,26 +175,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(kBarQ), qbytes);
       for (int t = 0; t < 2; ++t)
         if (n_t[t] > 0) tma_load_4d(sQ + t * kTileBytes, &tmQ, bar(kBarQ), 0, q0 + t * kBQ, h, b);
-      int issued = 0;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        if (!mbar_wait(bar(kBarKVEmpty + s), ph ^ 1, p.timeout_ns)) {
-          record_error(p.status, kErrTimeout, kSiteProducer);
-          break;
-        }
+      // K runs one tile ahead of V: S(j+1) = Q K(j+1)^T is issued before O += P(j) V(j).
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      auto load_k = [&](int j) {
+        const int s = j % kKStages;
+        if (!mbar_wait_backoff(bar(kBarKEmpty + s), ((j / kKStages) & 1) ^ 1, p.timeout_ns))
+          return false;
         mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
         tma_load_4d(sK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, j * kBKV, h, b);
+        issued_k = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) {
+        const int s = j % kVStages;
+        if (!mbar_wait_backoff(bar(kBarVEmpty + s), ((j / kVStages) & 1) ^ 1, p.timeout_ns))
+          return false;
         mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
         tma_load_4d(sV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, j * kBKV, h, b);
-        issued = j + 1;
+        issued_v = j + 1;
+        return true;
+      };
+      ok = load_k(0);
+      for (int j = 0; ok && j < nmax; ++j) {
+        if (j + 1 < nmax) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
       }
+      if (!ok) record_error(p.status, kErrTimeout, kSiteProducer);
       // every copy started here lands before the CTA may exit
       (void)mbar_wait(bar(kBarQ), 0, p.timeout_ns);
-      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
-        (void)mbar_wait(bar(kBarKFull + i % kStages), (i / kStages) & 1, p.timeout_ns);
-        (void)mbar_wait(bar(kBarVFull + i % kStages), (i / kStages) & 1, p.timeout_ns);
-      }
+      for (int i = (issued_k > kKStages ? issued_k - kKStages : 0); i < issued_k; ++i)
+        (void)mbar_wait(bar(kBarKFull + i % kKStages), (i / kKStages) & 1, p.timeout_ns);
+      for (int i = (issued_v > kVStages ? issued_v - kVStages : 0); i < issued_v; ++i)
+        (void)mbar_wait(bar(kBarVFull + i % kVStages), (i / kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
@@ -187,13 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
-        const uint32_t pbase = smem_u32(sP + t * kPBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk) {
-          const uint64_t ad =
-              smem_desc_sw128(pbase + (kk >> 2) * (kBQ * 128) + (kk & 3) * 32, 1024, 1024);
+        for (int kk = 0; kk < kBKV / 16; ++kk) {  // 16 keys = 8 TMEM columns of P per step
           const uint64_t bd = smem_desc_sw128(sV + s * kTileBytes + kk * 16 * 128, 1024, 1024);
-          mma_bf16_ss(tmem + 256 + t * kHD, ad, bd, idO, (acc || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kColO + t * kHD, tmem + kColP + t * 64 + kk * 8, bd, idO,
+                      (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns) &&
@@ -201,55 +235,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) {
+          if (ntiles(t) > 0) {
             issue_s(t, 0);
             mma_commit(bar(kBarSFull + t));
           }
+        mma_commit(bar(kBarKEmpty + 0));  // K(0) free once both products have read it
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        const int s = j % kStages;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= n_t[t]) continue;
+        // S_t(j+1) as soon as softmax t has read S_t(j) out of TMEM: the next Q K^T product
+        // overlaps this tile's exponentials
+        if (j + 1 < nmax) {
+          const int sk = (j + 1) % kKStages;
+          if (!mbar_wait(bar(kBarKFull + sk), ((j + 1) / kKStages) & 1, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < 2; ++t) {
+            if (j + 1 >= ntiles(t)) continue;
+            if (!mbar_wait(bar(kBarSFree + t), j & 1, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, sk);
+            mma_commit(bar(kBarSFull + t));
+          }
+          if (!ok) break;
+          mma_commit(bar(kBarKEmpty + sk));
+        }
+        // O_t += P_t(j) V_j once softmax t has written P_t(j)
+        const int sv = j % kVStages;
+        if (!mbar_wait(bar(kBarVFull + sv), (j / kVStages) & 1, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2; ++t) {
+          if (j >= ntiles(t)) continue;
           if (!mbar_wait(bar(kBarPFull + t), j & 1, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (j + 1 < n_t[t]) {
-            const int s1 = (j + 1) % kStages;
-            if (!mbar_wait(bar(kBarKFull + s1), ((j + 1) / kStages) & 1, p.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, s1);
-            mma_commit(bar(kBarSFull + t));
-          }
-          if (!mbar_wait(bar(kBarVFull + s), (j / kStages) & 1, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
+          issue_pv(t, sv, j > 0);
           mma_commit(bar(kBarODone + t));
         }
-        if (ok) mma_commit(bar(kBarKVEmpty + s));
+        if (ok) mma_commit(bar(kBarVEmpty + sv));
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteMma);
       mma_commit(bar(kBarDrain));
       (void)mbar_wait(bar(kBarDrain), 0, p.timeout_ns);  // no MMA in flight past this point
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------------ softmax warps
+    regs_inc<kSoftmaxRegs>();
     const int t = warp >> 2;
     const int quarter = warp & 3;
     const int r_local = quarter * 32 + lane;
     const int row = q0 + t * kBQ + r_local;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + t * kBKV + lane_off;
-    const uint32_t tO = tmem + 256 + t * kHD + lane_off;
-    uint8_t* const sPt = sP + t * kPBytes;
-    const int nt = (t == 0) ? n_t[0] : n_t[1];
+    const uint32_t tO = tmem + kColO + t * kHD + lane_off;
+    const uint32_t tP = tmem + kColP + t * 64 + lane_off;
+    const int nt = ntiles(t);
     const int limit = (p.mask == 1) ? row : L - 1;  // allowed keys: j <= limit
     const float c = p.scale_log2;
     float m_used = -INFINITY;
@@ -264,30 +311,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int col0 = j * kBKV;
-      const bool masked = col0 + kBKV - 1 > limit;
-      // pass 1: the row maximum over the allowed keys of this tile
-      float mt = -INFINITY;
-      {
-        uint32_t r[4][32];
+      // the whole S row of this tile: 128 fp32 in registers, one TMEM round trip
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(tS + 0, r0);
+      tmem_ld32(tS + 32, r1);
+      tmem_ld32(tS + 64, r2);
+      tmem_ld32(tS + 96, r3);
+      tmem_wait_ld();
+      reg_fence(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten
+      float sv[128];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) reg_fence(r[q]);
-        if (masked) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + q * 32 + i <= limit) mt = fmaxf(mt, __uint_as_float(r[q][i]));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              mt = fmax3(mt, __uint_as_float(r[q][i]), __uint_as_float(r[q][i + 1]));
-        }
+      for (int i = 0; i < 32; ++i) {
+        sv[i] = __uint_as_float(r0[i]);
+        sv[32 + i] = __uint_as_float(r1[i]);
+        sv[64 + i] = __uint_as_float(r2[i]);
+        sv[96 + i] = __uint_as_float(r3[i]);
       }
+      if (col0 + kBKV - 1 > limit) {  // diagonal / padding tile: exclude keys past limit
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (col0 + i > limit) sv[i] = -INFINITY;
+      }
+      float mt = fmax3(sv[0], sv[1], sv[2]);
+#pragma unroll
+      for (int i = 3; i < 127; i += 2) mt = fmax3(mt, sv[i], sv[i + 1]);
+      mt = fmaxf(mt, sv[127]);
 
       if (j > 0 && !warp_all(mbar_wait(bar(kBarODone + t), (j - 1) & 1, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteSoftmaxO);
@@ -320,38 +374,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
       }
-      // pass 2, 32 keys at a time: p = 2^(s*c - m*c), row sum, P (bf16) into the
-      // K-major 128-byte-swizzled smem tile: two 64-key halves of [128 rows][128 B]
-      const float neg = -m_used * c;
-      float rs = 0.f;
+      // p = 2^(s*c - m*c) two at a time; row sum in two independent pairs
+      const float2 c2 = make_float2(c, c);
+      const float2 n2 = make_float2(-m_used * c, -m_used * c);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      uint32_t pk[64];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t r[32];
-        tmem_ld32(tS + q * 32, r);
-        tmem_wait_ld();
-        reg_fence(r);
-        float pv[32];
+      for (int i = 0; i < 64; ++i) {
+        float2 x = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), c2, n2);
+        x.x = ex2_approx(x.x);
+        x.y = ex2_approx(x.y);
+        if (i & 1)
+          acc1 = fadd2(acc1, x);
+        else
+          acc0 = fadd2(acc0, x);
+        pk[i] = pack_bf16x2(x.x, x.y);
+      }
+      // P row -> TMEM (bf16 pairs, keys 2i and 2i+1 in column i), the A operand of P.V
+      {
+        uint32_t lo[32], hi[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float sv = (masked && col0 + q * 32 + i > limit) ? -INFINITY : __uint_as_float(r[i]);
-          pv[i] = ex2_approx(fmaf(sv, c, neg));
-          rs += pv[i];
+          lo[i] = pk[i];
+          hi[i] = pk[32 + i];
         }
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int u = q * 4 + w;  // 16-byte chunk index along the row (8 keys each)
-          uint4 v;
-          v.x = pack_bf16x2(pv[w * 8 + 0], pv[w * 8 + 1]);
-          v.y = pack_bf16x2(pv[w * 8 + 2], pv[w * 8 + 3]);
-          v.z = pack_bf16x2(pv[w * 8 + 4], pv[w * 8 + 5]);
-          v.w = pack_bf16x2(pv[w * 8 + 6], pv[w * 8 + 7]);
-          uint8_t* dst = sPt + (u >> 3) * (kBQ * 128) + r_local * 128 +
-                         (((u & 7) ^ (r_local & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = v;
-        }
+        tmem_st32(tP, lo);
+        tmem_st32(tP + 32, hi);
       }
-      l += rs;
-      fence_proxy_async_smem();
+      const float2 acc = fadd2(acc0, acc1);
+      l += acc.x + acc.y;
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + t));
     }
@@ -427,7 +479,14 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   cudaError_t e = cudaFuncSetAttribute(sdpa_fwd_bf16_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.H, a.B, (a.Nq + 2 * kBQ - 1) / (2 * kBQ));
+  // The setmaxnreg split must fit in what the block is launched with, or the increase would
+  // wait forever: refuse to launch if the compiled register count is too small for it.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, sdpa_fwd_bf16_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
+    return cudaErrorInvalidConfiguration;
+  dim3 grid((a.Nq + 2 * kBQ - 1) / (2 * kBQ), a.H, a.B);
   sdpa_fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
