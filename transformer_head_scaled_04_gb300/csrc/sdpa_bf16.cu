@@ -9,8 +9,8 @@
 // tiles t = 0, 1) of one (b, h) and streams K/V in 128-row tiles:
 //   warp 8     TMA producer: Q tiles once, then K and V through separate 4-stage rings
 //              (K one tile ahead; a K slot frees as soon as Q K^T has read it)
-//   warp 9     TMEM owner + MMA issuer (one thread) -- warps 8-11 form the control
-//              warpgroup, which hands most of its registers to the softmax warpgroups:
+//   warps 9-10 MMA issuers, one thread per query tile (warp 9 also owns TMEM); warps 8-11
+//              form the control warpgroup, which hands most of its registers to softmax:
 //                S_t = Q_t K_j^T           tcgen05.mma 128x128x16 x4, fp32 in TMEM
 //                O_t += P_t V_j            tcgen05.mma 128x64x16 x8, P from TMEM, V MN-major
 //              S_t(j+1) is issued as soon as the softmax warps have read S_t(j) out of TMEM,
@@ -73,11 +73,12 @@ enum : int {
 };
 
 // barrier indices
+static_assert(kKStages == kVStages, "one K/V-ready barrier per pipeline step");
 constexpr int kBarQ = 0;
-constexpr int kBarKFull = 1;
-constexpr int kBarKEmpty = kBarKFull + kKStages;
-constexpr int kBarVFull = kBarKEmpty + kKStages;
-constexpr int kBarVEmpty = kBarVFull + kVStages;
+constexpr int kBarK0 = 1;                         // K(0) landed
+constexpr int kBarKV = kBarK0 + 1;                // step j: K(j+1) and V(j) landed
+constexpr int kBarKEmpty = kBarKV + kKStages;     // K slot free (both issuers done)
+constexpr int kBarVEmpty = kBarKEmpty + kKStages; // V slot free (both issuers done)
 constexpr int kBarSFull = kBarVEmpty + kVStages;  // 2
 constexpr int kBarSFree = kBarSFull + 2;          // 2
 constexpr int kBarPFull = kBarSFree + 2;          // 2
@@ -138,13 +139,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
+    mbar_init(bar(kBarK0), 1);
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVEmpty + s), 1);
+      mbar_init(bar(kBarKV + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 2);
+      mbar_init(bar(kBarVEmpty + s), 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
@@ -152,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPFull + t), kBQ);
       mbar_init(bar(kBarODone + t), 1);
     }
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain), 2);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -175,111 +174,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(kBarQ), qbytes);
       for (int t = 0; t < 2; ++t)
         if (n_t[t] > 0) tma_load_4d(sQ + t * kTileBytes, &tmQ, bar(kBarQ), 0, q0 + t * kBQ, h, b);
-      // K runs one tile ahead of V: S(j+1) = Q K(j+1)^T is issued before O += P(j) V(j).
-      int issued_k = 0, issued_v = 0;
+      // K runs one tile ahead of V: step j brings K(j+1) and V(j), both onto one barrier,
+      // since S(j+1) = Q K(j+1)^T is issued right before O += P(j) V(j).
       bool ok = true;
-      auto load_k = [&](int j) {
-        const int s = j % kKStages;
-        if (!mbar_wait_backoff(bar(kBarKEmpty + s), ((j / kKStages) & 1) ^ 1, p.timeout_ns))
-          return false;
-        mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-        tma_load_4d(sK + s * kTileBytes, &tmK, bar(kBarKFull + s), 0, j * kBKV, h, b);
-        issued_k = j + 1;
-        return true;
-      };
-      auto load_v = [&](int j) {
-        const int s = j % kVStages;
-        if (!mbar_wait_backoff(bar(kBarVEmpty + s), ((j / kVStages) & 1) ^ 1, p.timeout_ns))
-          return false;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-        tma_load_4d(sV + s * kTileBytes, &tmV, bar(kBarVFull + s), 0, j * kBKV, h, b);
-        issued_v = j + 1;
-        return true;
-      };
-      ok = load_k(0);
-      for (int j = 0; ok && j < nmax; ++j) {
-        if (j + 1 < nmax) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
+      mbar_arrive_expect_tx(bar(kBarK0), kTileBytes);
+      tma_load_4d(sK, &tmK, bar(kBarK0), 0, 0, h, b);
+      int issued = 0;
+      for (int j = 0; j < nmax; ++j) {
+        const bool next_k = j + 1 < nmax;
+        const int sk = (j + 1) % kKStages, sv = j % kVStages;
+        if (next_k && !mbar_wait_backoff(bar(kBarKEmpty + sk), (((j + 1) / kKStages) & 1) ^ 1,
+                                         p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_backoff(bar(kBarVEmpty + sv), ((j / kVStages) & 1) ^ 1, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t kv = bar(kBarKV + j % kKStages);
+        mbar_arrive_expect_tx(kv, next_k ? 2 * kTileBytes : kTileBytes);
+        if (next_k) tma_load_4d(sK + sk * kTileBytes, &tmK, kv, 0, (j + 1) * kBKV, h, b);
+        tma_load_4d(sV + sv * kTileBytes, &tmV, kv, 0, j * kBKV, h, b);
+        issued = j + 1;
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteProducer);
       // every copy started here lands before the CTA may exit
       (void)mbar_wait(bar(kBarQ), 0, p.timeout_ns);
-      for (int i = (issued_k > kKStages ? issued_k - kKStages : 0); i < issued_k; ++i)
-        (void)mbar_wait(bar(kBarKFull + i % kKStages), (i / kKStages) & 1, p.timeout_ns);
-      for (int i = (issued_v > kVStages ? issued_v - kVStages : 0); i < issued_v; ++i)
-        (void)mbar_wait(bar(kBarVFull + i % kVStages), (i / kVStages) & 1, p.timeout_ns);
+      (void)mbar_wait(bar(kBarK0), 0, p.timeout_ns);
+      for (int i = (issued > kKStages ? issued - kKStages : 0); i < issued; ++i)
+        (void)mbar_wait(bar(kBarKV + i % kKStages), (i / kKStages) & 1, p.timeout_ns);
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One thread per query tile (warp 9: tile 0, warp 10: tile 1).  A single thread spends
+    // tens of cycles per tcgen05.mma and per barrier test, which would leave the tensor core
+    // idle between the short P.V products; two issuers keep it fed.
+    const int t = warp - 9;
+    const int nt = ntiles(t);
     if (lane == 0 && nmax > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBQ, kBKV, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(kBQ, kHD, false, true);
-      auto issue_s = [&](int t, int s) {
+      const uint32_t sQt = sQ + t * kTileBytes;
+      const uint32_t dS = tmem + t * kBKV;
+      const uint32_t dO = tmem + kColO + t * kHD;
+      const uint32_t aP = tmem + kColP + t * 64;
+      auto issue_s = [&](int sk) {
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(sQ + t * kTileBytes + kk * 32, 1024, 1024);
-          const uint64_t bd = smem_desc_sw128(sK + s * kTileBytes + kk * 32, 1024, 1024);
-          mma_bf16_ss(tmem + t * kBKV, ad, bd, idS, kk > 0 ? 1u : 0u);
+          const uint64_t ad = smem_desc_sw128(sQt + kk * 32, 1024, 1024);
+          const uint64_t bd = smem_desc_sw128(sK + sk * kTileBytes + kk * 32, 1024, 1024);
+          mma_bf16_ss(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
+      auto issue_pv = [&](int sv, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk) {  // 16 keys = 8 TMEM columns of P per step
-          const uint64_t bd = smem_desc_sw128(sV + s * kTileBytes + kk * 16 * 128, 1024, 1024);
-          mma_bf16_ts(tmem + kColO + t * kHD, tmem + kColP + t * 64 + kk * 8, bd, idO,
-                      (acc || kk > 0) ? 1u : 0u);
+          const uint64_t bd = smem_desc_sw128(sV + sv * kTileBytes + kk * 16 * 128, 1024, 1024);
+          mma_bf16_ts(dO, aP + kk * 8, bd, idO, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns) &&
-                mbar_wait(bar(kBarKFull + 0), 0, p.timeout_ns);
+      bool ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns) && mbar_wait(bar(kBarK0), 0, p.timeout_ns);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (ntiles(t) > 0) {
-            issue_s(t, 0);
-            mma_commit(bar(kBarSFull + t));
-          }
-        mma_commit(bar(kBarKEmpty + 0));  // K(0) free once both products have read it
+        if (nt > 0) {
+          issue_s(0);
+          mma_commit(bar(kBarSFull + t));
+        }
+        mma_commit(bar(kBarKEmpty + 0));  // this issuer is done with K(0)
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        // S_t(j+1) as soon as softmax t has read S_t(j) out of TMEM: the next Q K^T product
-        // overlaps this tile's exponentials
-        if (j + 1 < nmax) {
-          const int sk = (j + 1) % kKStages;
-          if (!mbar_wait(bar(kBarKFull + sk), ((j + 1) / kKStages) & 1, p.timeout_ns)) {
-            ok = false;
-            break;
-          }
-          for (int t = 0; t < 2; ++t) {
-            if (j + 1 >= ntiles(t)) continue;
-            if (!mbar_wait(bar(kBarSFree + t), j & 1, p.timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, sk);
-            mma_commit(bar(kBarSFull + t));
-          }
-          if (!ok) break;
-          mma_commit(bar(kBarKEmpty + sk));
-        }
-        // O_t += P_t(j) V_j once softmax t has written P_t(j)
-        const int sv = j % kVStages;
-        if (!mbar_wait(bar(kBarVFull + sv), (j / kVStages) & 1, p.timeout_ns)) {
+        if (!mbar_wait(bar(kBarKV + j % kKStages), (j / kKStages) & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
-        for (int t = 0; t < 2; ++t) {
-          if (j >= ntiles(t)) continue;
+        // S_t(j+1) as soon as softmax t has read S_t(j) out of TMEM
+        if (j + 1 < nt) {
+          if (!mbar_wait(bar(kBarSFree + t), j & 1, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s((j + 1) % kKStages);
+          mma_commit(bar(kBarSFull + t));
+        }
+        if (j + 1 < nmax) mma_commit(bar(kBarKEmpty + (j + 1) % kKStages));
+        // O_t += P_t(j) V_j once softmax t has written P_t(j)
+        if (j < nt) {
           if (!mbar_wait(bar(kBarPFull + t), j & 1, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(t, sv, j > 0);
+          issue_pv(j % kVStages, j > 0);
           mma_commit(bar(kBarODone + t));
         }
-        if (ok) mma_commit(bar(kBarVEmpty + sv));
+        mma_commit(bar(kBarVEmpty + j % kVStages));
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteMma);
       mma_commit(bar(kBarDrain));
