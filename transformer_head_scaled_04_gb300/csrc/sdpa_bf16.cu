@@ -20,6 +20,9 @@
 //              One tcgen05.ld round trip brings the whole 128-key S row into registers;
 //              mask, running max m and sum l, p = 2^(s*c - m*c) with c = scale*log2(e)
 //              (paired fp32 FMA / add), P rounded to bf16 and stored back into TMEM.
+//              The exponentials run before the wait for the previous P.V product, and tile 1
+//              starts its first exponentials only when tile 0 has finished its own, so the
+//              two warpgroups' MUFU-heavy phases interleave instead of colliding.
 //              O is rescaled (in TMEM) only when the max grows by more than 2^8; the final
 //              O / l uses the same max as every p, so the result equals the softmax exactly
 //              up to rounding.  At the end: O / l -> bf16 -> global, in any strided layout
@@ -83,7 +86,8 @@ constexpr int kBarSFull = kBarVEmpty + kVStages;  // 2
 constexpr int kBarSFree = kBarSFull + 2;          // 2
 constexpr int kBarPFull = kBarSFree + 2;          // 2
 constexpr int kBarODone = kBarPFull + 2;          // 2
-constexpr int kBarDrain = kBarODone + 2;
+constexpr int kBarStagger = kBarODone + 2;
+constexpr int kBarDrain = kBarStagger + 1;
 constexpr int kNumBars = kBarDrain + 1;
 
 struct Params {
@@ -152,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone + t), 1);
     }
     mbar_init(bar(kBarDrain), 2);
+    mbar_init(bar(kBarStagger), 4);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -333,38 +338,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 3; i < 127; i += 2) mt = fmax3(mt, sv[i], sv[i + 1]);
       mt = fmaxf(mt, sv[127]);
 
-      if (j > 0 && !warp_all(mbar_wait(bar(kBarODone + t), (j - 1) & 1, p.timeout_ns))) {
+      // new running max; O and l are rescaled only when it grows past 2^8 (exact: every p
+      // and l use the same m_used, and O / l is taken at the end)
+      const float m_new = fmaxf(m_used, mt);
+      float alpha = 1.f;
+      bool grow = false;
+      if (j == 0) {
+        m_used = (m_new == -INFINITY) ? 0.f : m_new;
+      } else if (m_new > m_used + p.tau) {
+        grow = true;
+        alpha = ex2_approx((m_used - m_new) * c);
+        l *= alpha;
+        m_used = m_new;
+      }
+      // p = 2^(s*c - m*c) two at a time; row sum in two independent pairs.  This runs while
+      // the previous P.V product may still be reading P from TMEM.
+      if (t == 1 && j == 0 && !warp_all(mbar_wait(bar(kBarStagger), 0, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteSoftmaxO);
         ok = false;
         break;
       }
-      const float m_new = fmaxf(m_used, mt);
-      if (j == 0) {
-        m_used = (m_new == -INFINITY) ? 0.f : m_new;
-      } else {
-        const bool grow = m_new > m_used + p.tau;
-        float alpha = 1.f;
-        if (grow) {
-          alpha = ex2_approx((m_used - m_new) * c);
-          l *= alpha;
-          m_used = m_new;
-        }
-        if (__any_sync(0xffffffffu, grow)) {  // TMEM access is warp-collective
-          tc_fence_after();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t o[32];
-            tmem_ld32(tO + half * 32, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + half * 32, o);
-          }
-          tmem_wait_st();
-        }
-      }
-      // p = 2^(s*c - m*c) two at a time; row sum in two independent pairs
       const float2 c2 = make_float2(c, c);
       const float2 n2 = make_float2(-m_used * c, -m_used * c);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -379,6 +372,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           acc0 = fadd2(acc0, x);
         pk[i] = pack_bf16x2(x.x, x.y);
+      }
+      if (t == 0 && j == 0) {  // tile 1 starts its first exponentials when tile 0 is done
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarStagger));
+      }
+      // the previous P.V product must be done before O is rescaled or P overwritten
+      if (j > 0 && !warp_all(mbar_wait(bar(kBarODone + t), (j - 1) & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteSoftmaxO);
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, grow)) {  // TMEM access is warp-collective
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tmem_ld32(tO + half * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + half * 32, o);
+        }
+        tmem_wait_st();
       }
       // P row -> TMEM (bf16 pairs, keys 2i and 2i+1 in column i), the A operand of P.V
       {
