@@ -5,12 +5,14 @@
 // You Need", lettle.cn translation, 3.2.2 多头注意力; "Transformer：抛弃循环与卷积的序列建模",
 // Multi-Head Attention).
 //
-// One CTA computes one 128 x BN output tile:
+// Persistent kernel: one CTA per SM walks the 128 x BN output tiles (N fastest, so the CTAs
+// running together share the same X rows in L2).
 //   warp 0     TMA producer: X and W K-slices (64 wide, 128-byte swizzle) into a STAGES ring
-//   warp 1     TMEM owner + MMA issuer: tcgen05.mma kind::f16 128xBNx16, fp32 accumulator in
-//              TMEM, tcgen05.commit frees a ring slot / publishes the finished accumulator
+//              that runs on across tile boundaries
+//   warp 1     TMEM owner + MMA issuer: tcgen05.mma kind::f16 128xBNx16 into one of two TMEM
+//              accumulators, so the epilogue of tile i overlaps the MMAs of tile i+1
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane quarter per warp), add
-//              bias, round to bf16 (nearest even), store.
+//              bias, round to bf16 (nearest even), store, hand the accumulator back.
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -36,7 +38,7 @@ struct GemmShape {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
-  static constexpr uint32_t kTmemCols = BN;  // power of two >= 32
+  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
 template <int BN>
@@ -52,25 +54,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S::kStages * S::kABytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
-  // bars[0..ST) full, [ST..2ST) empty, [2ST] accumulator ready; tmem slot after them
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 1);
+  // [0,ST) full, [ST,2ST) empty, then acc_full[2], acc_empty[2], drain; tmem slot after
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 5);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM;
-  const int n0 = blockIdx.x * BN;
   const int num_kb = K / kBK;
+  const int tiles_n = (N + BN - 1) / BN;
+  const int tiles = tiles_n * ((M + kBM - 1) / kBM);
 
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S::kStages + s); };
-  const uint32_t acc_bar = smem_u32(bars + 2 * S::kStages);
+  auto acc_full = [&](int b) { return smem_u32(bars + 2 * S::kStages + b); };
+  auto acc_empty = [&](int b) { return smem_u32(bars + 2 * S::kStages + 2 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 2 * S::kStages + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -86,59 +94,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
-    int issued = 0;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % S::kStages;
-      const uint32_t ph = (kb / S::kStages) & 1;
-      if (!mbar_wait(empty_bar(s), ph ^ 1, timeout_ns)) {
-        record_error(status, kErrTimeout, kSiteGemmProducer);
-        break;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+      const int m0 = (tile / tiles_n) * kBM;
+      const int n0 = (tile % tiles_n) * BN;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S::kStages;
+        if (!mbar_wait_backoff(empty_bar(s), ((it / S::kStages) & 1) ^ 1, timeout_ns)) {
+          record_error(status, kErrTimeout, kSiteGemmProducer);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), S::kStageBytes);
+        tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
+        tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
       }
-      mbar_arrive_expect_tx(full_bar(s), S::kStageBytes);
-      tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
-      tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
-      issued = kb + 1;
     }
     // let every copy this thread started land before the CTA can exit
-    for (int i = (issued > S::kStages ? issued - S::kStages : 0); i < issued; ++i)
+    for (int i = (it > S::kStages ? it - S::kStages : 0); i < it; ++i)
       (void)mbar_wait(full_bar(i % S::kStages), (i / S::kStages) & 1, timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
+    int it = 0, tcount = 0;
     bool ok = true;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % S::kStages;
-      const uint32_t ph = (kb / S::kStages) & 1;
-      if (!mbar_wait(full_bar(s), ph, timeout_ns)) {
-        record_error(status, kErrTimeout, kSiteGemmMma);
+    for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
+      const int buf = tcount & 1;
+      const uint32_t d = tmem + buf * BN;
+      if (!mbar_wait(acc_empty(buf), ((tcount >> 1) & 1) ^ 1, timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * S::kABytes);
-      const uint32_t b0 = smem_u32(sB + s * S::kBBytes);
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const int s = it % S::kStages;
+        if (!mbar_wait(full_bar(s), (it / S::kStages) & 1, timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + s * S::kABytes);
+        const uint32_t b0 = smem_u32(sB + s * S::kBBytes);
 #pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
-        mma_bf16_ss(tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
+          mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(empty_bar(s));
       }
-      mma_commit(empty_bar(s));
+      if (!ok) break;
+      mma_commit(acc_full(buf));
     }
-    mma_commit(acc_bar);
-    if (!ok) (void)mbar_wait(acc_bar, 0, timeout_ns);  // drain issued MMAs before TMEM is freed
+    if (!ok) record_error(status, kErrTimeout, kSiteGemmMma);
+    mma_commit(drain_bar);
+    (void)mbar_wait(drain_bar, 0, timeout_ns);  // no MMA in flight past this point
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int row = m0 + quarter * 32 + lane;
-    const bool ok = mbar_wait(acc_bar, 0, timeout_ns);
-    if (!ok) record_error(status, kErrTimeout, kSiteGemmEpilogue);
-    tc_fence_after();
-    if (ok) {
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+      const int buf = tcount & 1;
+      const int m0 = (tile / tiles_n) * kBM;
+      const int n0 = (tile % tiles_n) * BN;
+      const int row = m0 + quarter * 32 + lane;
+      if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (tcount >> 1) & 1, timeout_ns))) {
+        record_error(status, kErrTimeout, kSiteGemmEpilogue);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c * 32, r);
+        tmem_ld32(tbase + c * 32, r);
         tmem_wait_ld();
         reg_fence(r);
         const int col = n0 + c * 32;
@@ -149,10 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint4 u = __ldg(bp + v);
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+              const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                float2 f = __bfloat1622float2(h[e]);
+                float2 f = __bfloat1622float2(hv[e]);
                 bv[v * 8 + e * 2] = f.x;
                 bv[v * 8 + e * 2 + 1] = f.y;
               }
@@ -172,6 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 4; ++v) dst[v] = out[v];
         }
       }
+      // accumulator read: hand it back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(buf));
     }
   }
 
@@ -191,9 +225,9 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((N + BN - 1) / BN, (M + kBM - 1) / kBM);
-  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW,
-                                             static_cast<const __nv_bfloat16*>(bias),
+  const int64_t tiles = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM);
+  const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW, static_cast<const __nv_bfloat16*>(bias),
                                              static_cast<__nv_bfloat16*>(Y), M, N, K, ldy,
                                              ctx.status, ctx.timeout_ns);
   return cudaGetLastError();

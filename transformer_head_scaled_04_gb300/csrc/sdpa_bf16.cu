@@ -333,10 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (col0 + i > limit) sv[i] = -INFINITY;
       }
-      float mt = fmax3(sv[0], sv[1], sv[2]);
+      float m4[4];
 #pragma unroll
-      for (int i = 3; i < 127; i += 2) mt = fmax3(mt, sv[i], sv[i + 1]);
-      mt = fmaxf(mt, sv[127]);
+      for (int k = 0; k < 4; ++k) {  // four independent chains over 32-key blocks
+        const float* v = sv + 32 * k;
+        m4[k] = fmax3(v[0], v[1], v[2]);
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) m4[k] = fmax3(m4[k], v[i], v[i + 1]);
+        m4[k] = fmaxf(m4[k], v[31]);
+      }
+      const float mt = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
 
       // new running max; O and l are rescaled only when it grows past 2^8 (exact: every p
       // and l use the same m_used, and O / l is taken at the end)
