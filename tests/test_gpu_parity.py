@@ -71,6 +71,9 @@ SDPA_CASES = [
     (1, 2, 640, 640, "causal", None),
     (3, 2, 200, 390, "key_padding", [0, 1, 390]),
     (4, 1, 129, 256, "key_padding", [64, 127, 128, 129]),
+    # more key tiles than K/V ring slots while a block's second query tile is empty
+    (1, 2, 640, 1000, "none", None),
+    (2, 1, 100, 900, "key_padding", [900, 700]),
 ]
 
 

@@ -9,8 +9,9 @@
 // tiles t = 0, 1) of one (b, h) and streams K/V in 128-row tiles:
 //   warp 8     TMA producer: Q tiles once, then K and V through separate 4-stage rings
 //              (K one tile ahead; a K slot frees as soon as Q K^T has read it)
-//   warps 9-10 MMA issuers, one thread per query tile (warp 9 also owns TMEM); warps 8-11
-//              form the control warpgroup, which hands most of its registers to softmax:
+//   warps 9-11 MMA issuers: warp 9 (also TMEM owner) issues S for both tiles, warps 10/11 the
+//              P.V of tile 0/1; warps 8-11 form the control warpgroup, which hands most of
+//              its registers to the softmax warps:
 //                S_t = Q_t K_j^T           tcgen05.mma 128x128x16 x4, fp32 in TMEM
 //                O_t += P_t V_j            tcgen05.mma 128x64x16 x8, P from TMEM, V MN-major
 //              S_t(j+1) is issued as soon as the softmax warps have read S_t(j) out of TMEM,
@@ -56,7 +57,10 @@ static_assert(8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs <= kThreads * 168,
 constexpr int kTileBytes = kBQ * kHD * 2;  // 16 KB: a 128 x 64 bf16 tile
 
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
+// K(0) has its own buffer; K(i), i >= 1, uses ring slot (i - 1) % stages, so step j's K(j+1)
+// and V(j) both land in slot j % stages, freed together when step j - stages is done
+constexpr int kOffK0 = kOffQ + 2 * kTileBytes;
+constexpr int kOffK = kOffK0 + kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
 constexpr int kSmemBytes = 1024 + kOffBar + 256;
@@ -80,9 +84,8 @@ static_assert(kKStages == kVStages, "one K/V-ready barrier per pipeline step");
 constexpr int kBarQ = 0;
 constexpr int kBarK0 = 1;                         // K(0) landed
 constexpr int kBarKV = kBarK0 + 1;                // step j: K(j+1) and V(j) landed
-constexpr int kBarKEmpty = kBarKV + kKStages;     // K slot free (both issuers done)
-constexpr int kBarVEmpty = kBarKEmpty + kKStages; // V slot free (both issuers done)
-constexpr int kBarSFull = kBarVEmpty + kVStages;  // 2
+constexpr int kBarKVEmpty = kBarKV + kKStages;    // step-j slots free (both issuers done)
+constexpr int kBarSFull = kBarKVEmpty + kKStages; // 2
 constexpr int kBarSFree = kBarSFull + 2;          // 2
 constexpr int kBarPFull = kBarSFree + 2;          // 2
 constexpr int kBarODone = kBarPFull + 2;          // 2
@@ -114,14 +117,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const uint32_t sQ = smem_u32(smem + kOffQ);
+  const uint32_t sK0 = smem_u32(smem + kOffK0);
   const uint32_t sK = smem_u32(smem + kOffK);
   const uint32_t sV = smem_u32(smem + kOffV);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBQ);  // heaviest causal block first
+  // Without a causal mask every query block costs the same: the blocks of one (b, h) sit side
+  // by side so they share K/V in L2.  With it, block k costs ~4k+3 key tiles: all heads'
+  // heaviest blocks go first (longest-processing-time order), so no long block starts last.
+  int h, b, qblk;
+  if (p.mask == 1) {
+    const int bh = p.B * p.H;
+    const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    qblk = (gridDim.x - 1) - lin / bh;
+    h = (lin % bh) % p.H;
+    b = (lin % bh) / p.H;
+  } else {
+    h = blockIdx.y;
+    b = blockIdx.z;
+    qblk = gridDim.x - 1 - blockIdx.x;
+  }
+  const int q0 = qblk * (2 * kBQ);
 
   // keys a row may see: causal -> j <= row; otherwise j < L
   int L = p.Nk;
@@ -146,8 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarK0), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(kBarKV + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 2);
-      mbar_init(bar(kBarVEmpty + s), 2);
+      mbar_init(bar(kBarKVEmpty + s), 3);  // the three MMA issuers
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
@@ -155,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarPFull + t), kBQ);
       mbar_init(bar(kBarODone + t), 1);
     }
-    mbar_init(bar(kBarDrain), 2);
+    mbar_init(bar(kBarDrain), 3);
     mbar_init(bar(kBarStagger), 4);
     fence_mbar_init();
   }
@@ -183,17 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // since S(j+1) = Q K(j+1)^T is issued right before O += P(j) V(j).
       bool ok = true;
       mbar_arrive_expect_tx(bar(kBarK0), kTileBytes);
-      tma_load_4d(sK, &tmK, bar(kBarK0), 0, 0, h, b);
+      tma_load_4d(sK0, &tmK, bar(kBarK0), 0, 0, h, b);
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
         const bool next_k = j + 1 < nmax;
-        const int sk = (j + 1) % kKStages, sv = j % kVStages;
-        if (next_k && !mbar_wait_backoff(bar(kBarKEmpty + sk), (((j + 1) / kKStages) & 1) ^ 1,
-                                         p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_backoff(bar(kBarVEmpty + sv), ((j / kVStages) & 1) ^ 1, p.timeout_ns)) {
+        const int sk = j % kKStages, sv = j % kVStages;
+        // slot j % stages last held K(j+1-stages) and V(j-stages): both released together
+        // after step j - stages' P.V
+        if (!mbar_wait_backoff(bar(kBarKVEmpty + j % kKStages), ((j / kKStages) & 1) ^ 1,
+                               p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -210,71 +224,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = (issued > kKStages ? issued - kKStages : 0); i < issued; ++i)
         (void)mbar_wait(bar(kBarKV + i % kKStages), (i / kKStages) & 1, p.timeout_ns);
     }
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp >= 9) {
     // ------------------------------------------------------------------ MMA issuers
-    // One thread per query tile (warp 9: tile 0, warp 10: tile 1).  A single thread spends
-    // tens of cycles per tcgen05.mma and per barrier test, which would leave the tensor core
-    // idle between the short P.V products; two issuers keep it fed.
-    const int t = warp - 9;
-    const int nt = ntiles(t);
+    // A thread spends tens of cycles per tcgen05.mma and per barrier test, so the work is
+    // spread over three issuers: warp 9 issues both tiles' S = Q K^T products, warps 10 and
+    // 11 the O += P V products of tile 0 and tile 1.  Each releases the step's K/V slots.
     if (lane == 0 && nmax > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBQ, kBKV, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(kBQ, kHD, false, true);
-      const uint32_t sQt = sQ + t * kTileBytes;
-      const uint32_t dS = tmem + t * kBKV;
-      const uint32_t dO = tmem + kColO + t * kHD;
-      const uint32_t aP = tmem + kColP + t * 64;
-      auto issue_s = [&](int sk) {
+      // Descriptor start addresses are address >> 4 in the low 14 bits and every operand
+      // lies below 256 KB of shared memory, so moving an operand by `off` bytes adds off >> 4.
+      const uint64_t dQ = smem_desc_sw128(sQ, 1024, 1024);
+      const uint64_t dKfirst = smem_desc_sw128(sK0, 1024, 1024);
+      const uint64_t dK0 = smem_desc_sw128(sK, 1024, 1024);
+      const uint64_t dV0 = smem_desc_sw128(sV, 1024, 1024);
+      bool ok = true;
+      if (warp == 9) {
+        auto issue_s = [&](int t, int sk) {  // sk < 0: K(0) in its own buffer
+          const uint64_t aq = dQ + static_cast<uint64_t>((t * kTileBytes) >> 4);
+          const uint64_t bk =
+              sk < 0 ? dKfirst : dK0 + static_cast<uint64_t>((sk * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint64_t ad = smem_desc_sw128(sQt + kk * 32, 1024, 1024);
-          const uint64_t bd = smem_desc_sw128(sK + sk * kTileBytes + kk * 32, 1024, 1024);
-          mma_bf16_ss(dS, ad, bd, idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kHD / 16; ++kk)  // K steps of 16 = 32 B inside the swizzle row
+            mma_bf16_ss(tmem + t * kBKV, aq + kk * 2, bk + kk * 2, idS, kk > 0 ? 1u : 0u);
+        };
+        ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns) && mbar_wait(bar(kBarK0), 0, p.timeout_ns);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (ntiles(t) > 0) {
+              issue_s(t, -1);
+              mma_commit(bar(kBarSFull + t));
+            }
         }
-      };
-      auto issue_pv = [&](int sv, bool acc) {
-#pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk) {  // 16 keys = 8 TMEM columns of P per step
-          const uint64_t bd = smem_desc_sw128(sV + sv * kTileBytes + kk * 16 * 128, 1024, 1024);
-          mma_bf16_ts(dO, aP + kk * 8, bd, idO, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns) && mbar_wait(bar(kBarK0), 0, p.timeout_ns);
-      if (ok) {
-        tc_fence_after();
-        if (nt > 0) {
-          issue_s(0);
-          mma_commit(bar(kBarSFull + t));
-        }
-        mma_commit(bar(kBarKEmpty + 0));  // this issuer is done with K(0)
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        if (!mbar_wait(bar(kBarKV + j % kKStages), (j / kKStages) & 1, p.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        // S_t(j+1) as soon as softmax t has read S_t(j) out of TMEM
-        if (j + 1 < nt) {
-          if (!mbar_wait(bar(kBarSFree + t), j & 1, p.timeout_ns)) {
+        // Every issuer waits for step j's K/V barrier before it releases step j, even when it
+        // has nothing to issue: an issuer that ran a full ring ahead would otherwise put its
+        // release into an earlier phase of the same barrier.
+        for (int j = 0; ok && j < nmax; ++j) {
+          if (!mbar_wait(bar(kBarKV + j % kKStages), (j / kKStages) & 1, p.timeout_ns)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          issue_s((j + 1) % kKStages);
-          mma_commit(bar(kBarSFull + t));
+          if (j + 1 < nmax) {
+            // S_t(j+1) as soon as softmax t has read S_t(j) out of TMEM
+            for (int t = 0; t < 2; ++t) {
+              if (j + 1 >= ntiles(t)) continue;
+              if (!mbar_wait(bar(kBarSFree + t), j & 1, p.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(t, j % kKStages);
+              mma_commit(bar(kBarSFull + t));
+            }
+            if (!ok) break;
+          }
+          mma_commit(bar(kBarKVEmpty + j % kKStages));  // done with K(j+1)
         }
-        if (j + 1 < nmax) mma_commit(bar(kBarKEmpty + (j + 1) % kKStages));
-        // O_t += P_t(j) V_j once softmax t has written P_t(j)
-        if (j < nt) {
-          if (!mbar_wait(bar(kBarPFull + t), j & 1, p.timeout_ns)) {
+      } else {
+        const int t = warp - 10;
+        const int nt = ntiles(t);
+        const uint32_t dO = tmem + kColO + t * kHD;
+        const uint32_t aP = tmem + kColP + t * 64;
+        for (int j = 0; ok && j < nmax; ++j) {
+          if (!mbar_wait(bar(kBarKV + j % kKStages), (j / kKStages) & 1, p.timeout_ns)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          issue_pv(j % kVStages, j > 0);
-          mma_commit(bar(kBarODone + t));
+          // O_t += P_t(j) V_j once softmax t has written P_t(j)
+          if (j < nt) {
+            if (!mbar_wait(bar(kBarPFull + t), j & 1, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t bv = dV0 + static_cast<uint64_t>(((j % kVStages) * kTileBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBKV / 16; ++kk)  // 16 keys = 8 TMEM columns of P, 16 V rows
+              mma_bf16_ts(dO, aP + kk * 8, bv + kk * ((16 * 128) >> 4), idO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(kBarODone + t));
+          }
+          mma_commit(bar(kBarKVEmpty + j % kKStages));  // done with V(j)
         }
-        mma_commit(bar(kBarVEmpty + j % kVStages));
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteMma);
       mma_commit(bar(kBarDrain));
