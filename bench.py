@@ -211,6 +211,22 @@ def cpu_baseline(inp, w, mask, budget_s=12.0):
 
 # ----------------------------------------------------------------------------- helpers
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest value over all ranks (the whole job is as slow as its slowest rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, step_ms: float) -> float:
+    """Weak scaling: every rank runs the same step on its own batch."""
+    return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -358,15 +374,11 @@ def run_ours(args):
         return per, clk.summary()
 
     per, clocks = timed("none", args.steps, args.warmup)
-    step_ms = float(per.sum(axis=1).mean())
-    if pg:
-        tt = torch.tensor([step_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = max_over_ranks(float(per.sum(axis=1).mean()), pg, dev)
     sdpa_ms = float(per[:, 1].mean())
     fl_layer = layer_flops(w, "none")
     fl_sdpa = sdpa_flops(w, "none")
-    value = world * fl_layer / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, fl_layer, step_ms)
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     sdpa_tf = fl_sdpa / (sdpa_ms * 1e-3) / 1e12
