@@ -21,12 +21,13 @@
 //              One tcgen05.ld round trip brings the whole 128-key S row into registers;
 //              mask, running max m and sum l, p = 2^(s*c - m*c) with c = scale*log2(e)
 //              (paired fp32 FMA / add), P rounded to bf16 and stored back into TMEM.
-//              The exponentials run before the wait for the previous P.V product, and tile 1
+//              The reference max m_used is the exact max of the first key tile; later tiles
+//              exponentiate against it without taking their own max (any reference gives the
+//              exact softmax since p and l share it), and a tile whose row sum overflows
+//              2^64 is redone from TMEM with its true max after rescaling O and l.  The
+//              exponentials run before the wait for the previous P.V product, and tile 1
 //              starts its first exponentials only when tile 0 has finished its own, so the
-//              two warpgroups' MUFU-heavy phases interleave instead of colliding.
-//              O is rescaled (in TMEM) only when the max grows by more than 2^8; the final
-//              O / l uses the same max as every p, so the result equals the softmax exactly
-//              up to rounding.  At the end: O / l -> bf16 -> global, in any strided layout
+//              two warpgroups' MUFU-heavy phases interleave instead of colliding.  At the end: O / l -> bf16 -> global, in any strided layout
 //              (the head-concat layout [B, Nq, H*64] in the sublayer).
 // Whole K/V tiles past the causal diagonal or past key_len[b] are never loaded.  The query
 // blocks of one (b, h) are adjacent in the grid, so they run together and share K/V in L2.
@@ -97,7 +98,6 @@ struct Params {
   int B, H, Nq, Nk, mask;
   const int32_t* key_len;
   float scale_log2;  // scale * log2(e)
-  float tau;         // rescale threshold in raw score units (2^8 growth)
   __nv_bfloat16* O;
   int64_t so_b, so_h, so_n;
   int* status;
@@ -338,79 +338,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int col0 = j * kBKV;
-      // the whole S row of this tile: 128 fp32 in registers, one TMEM round trip
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS + 0, r0);
-      tmem_ld32(tS + 32, r1);
-      tmem_ld32(tS + 64, r2);
-      tmem_ld32(tS + 96, r3);
-      tmem_wait_ld();
-      reg_fence(r0);
-      reg_fence(r1);
-      reg_fence(r2);
-      reg_fence(r3);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten
+      const bool masked = col0 + kBKV - 1 > limit;  // diagonal / padding tile
       float sv[128];
+      // the whole S row of this tile: 128 fp32 in registers, one TMEM round trip
+      auto load_s = [&]() {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_wait_ld();
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sv[i] = __uint_as_float(r0[i]);
-        sv[32 + i] = __uint_as_float(r1[i]);
-        sv[64 + i] = __uint_as_float(r2[i]);
-        sv[96 + i] = __uint_as_float(r3[i]);
-      }
-      if (col0 + kBKV - 1 > limit) {  // diagonal / padding tile: exclude keys past limit
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(r0[i]);
+          sv[32 + i] = __uint_as_float(r1[i]);
+          sv[64 + i] = __uint_as_float(r2[i]);
+          sv[96 + i] = __uint_as_float(r3[i]);
+        }
+        if (masked) {  // exclude keys past limit
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (col0 + i > limit) sv[i] = -INFINITY;
-      }
-      float m4[4];
+          for (int i = 0; i < 128; ++i)
+            if (col0 + i > limit) sv[i] = -INFINITY;
+        }
+      };
+      auto row_max = [&]() {
+        float m4[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // four independent chains over 32-key blocks
-        const float* v = sv + 32 * k;
-        m4[k] = fmax3(v[0], v[1], v[2]);
+        for (int k = 0; k < 4; ++k) {  // four independent chains over 32-key blocks
+          const float* v = sv + 32 * k;
+          m4[k] = fmax3(v[0], v[1], v[2]);
 #pragma unroll
-        for (int i = 3; i < 31; i += 2) m4[k] = fmax3(m4[k], v[i], v[i + 1]);
-        m4[k] = fmaxf(m4[k], v[31]);
-      }
-      const float mt = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-
-      // new running max; O and l are rescaled only when it grows past 2^8 (exact: every p
-      // and l use the same m_used, and O / l is taken at the end)
-      const float m_new = fmaxf(m_used, mt);
-      float alpha = 1.f;
-      bool grow = false;
+          for (int i = 3; i < 31; i += 2) m4[k] = fmax3(m4[k], v[i], v[i + 1]);
+          m4[k] = fmaxf(m4[k], v[31]);
+        }
+        return fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+      };
+      const float2 c2 = make_float2(c, c);
+      uint32_t pk[64];
+      float tile_sum;
+      // p = 2^(s*c - m_used*c) two at a time, the tile's row sum in two independent pairs
+      auto exp_tile = [&]() {
+        const float2 n2 = make_float2(-m_used * c, -m_used * c);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float2 x = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), c2, n2);
+          x.x = ex2_approx(x.x);
+          x.y = ex2_approx(x.y);
+          if (i & 1)
+            acc1 = fadd2(acc1, x);
+          else
+            acc0 = fadd2(acc0, x);
+          pk[i] = pack_bf16x2(x.x, x.y);
+        }
+        const float2 acc = fadd2(acc0, acc1);
+        tile_sum = acc.x + acc.y;
+      };
+      load_s();
+      // The running max m_used only guards the exponentials against overflow: every p and l
+      // use the same m_used and O / l is taken at the end, so any m_used gives the exact
+      // softmax as long as nothing overflows.  It is the exact max of the first tile; later
+      // tiles reuse it, and a tile whose row sum leaves [0, 2^64] (overflow, inf or nan) is
+      // redone with the true max after rescaling O and l.
       if (j == 0) {
-        m_used = (m_new == -INFINITY) ? 0.f : m_new;
-      } else if (m_new > m_used + p.tau) {
-        grow = true;
-        alpha = ex2_approx((m_used - m_new) * c);
-        l *= alpha;
-        m_used = m_new;
+        const float mt = row_max();
+        m_used = (mt == -INFINITY) ? 0.f : mt;
       }
-      // p = 2^(s*c - m*c) two at a time; row sum in two independent pairs.  This runs while
-      // the previous P.V product may still be reading P from TMEM.
       if (t == 1 && j == 0 && !warp_all(mbar_wait(bar(kBarStagger), 0, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteSoftmaxO);
         ok = false;
         break;
       }
-      const float2 c2 = make_float2(c, c);
-      const float2 n2 = make_float2(-m_used * c, -m_used * c);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      uint32_t pk[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float2 x = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), c2, n2);
-        x.x = ex2_approx(x.x);
-        x.y = ex2_approx(x.y);
-        if (i & 1)
-          acc1 = fadd2(acc1, x);
-        else
-          acc0 = fadd2(acc0, x);
-        pk[i] = pack_bf16x2(x.x, x.y);
+      exp_tile();
+      float alpha = 1.f;
+      bool grow = false;
+      const bool redo = j > 0 && !(tile_sum <= 1.8446744e19f);  // 2^64
+      if (__any_sync(0xffffffffu, redo)) {  // rare; S_t(j) is still in TMEM
+        load_s();
+        const float m_new = fmaxf(m_used, row_max());
+        if (m_new > m_used) {
+          grow = true;
+          alpha = ex2_approx((m_used - m_new) * c);
+          l *= alpha;
+          m_used = m_new;
+        }
+        exp_tile();
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSFree + t));  // S_t may now be overwritten
       if (t == 0 && j == 0) {  // tile 1 starts its first exponentials when tile 0 is done
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarStagger));
@@ -446,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(tP, lo);
         tmem_st32(tP + 32, hi);
       }
-      const float2 acc = fadd2(acc0, acc1);
-      l += acc.x + acc.y;
+      l += tile_sum;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + t));
@@ -514,7 +533,6 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.key_len = a.key_len;
   const double c = static_cast<double>(a.scale) * 1.4426950408889634;  // log2(e)
   p.scale_log2 = static_cast<float>(c);
-  p.tau = static_cast<float>(8.0 / c);
   p.O = static_cast<__nv_bfloat16*>(a.O);
   p.so_b = a.so[0];
   p.so_h = a.so[1];
