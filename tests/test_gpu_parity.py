@@ -92,7 +92,8 @@ def test_sdpa_bf16(B, H, Nq, Nk, mask, kl):
 
 
 def test_sdpa_bf16_large_scores_stay_finite():
-    # scores of +-40: the running max grows across tiles and forces the O rescale path
+    # scores of +-40 whose tile maxima grow along the keys: later tiles are exponentiated
+    # against the smaller first-tile max (large but finite exponentials)
     g = np.random.Generator(np.random.PCG64(5))
     B, H, N = 1, 2, 700
     Q = si.round_bf16(2.5 * g.standard_normal((B, H, N, 64)))
@@ -102,6 +103,31 @@ def test_sdpa_bf16_large_scores_stay_finite():
         O = mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
                      to_dev(V, torch.bfloat16), mask)
         assert_bf16_close(host(O), oracle.sdpa_ref(Q, K, V, mask), f"sdpa bf16 large {mask}")
+
+
+def test_sdpa_bf16_later_tiles_overflowing_the_first_tile_max():
+    # Key tile k has its keys scaled by 0.05 * 3^k, so a row's scores jump by far more than
+    # 64 / (scale * log2 e) between tiles: the exponentials taken against an earlier tile's
+    # max would overflow, and the kernel must rebuild those tiles with the larger max
+    # (thousands of such tiles over these rows, several per row, with every mask).  The
+    # rows end up nearly one-hot, so O is close to a single value row: V is drawn at half
+    # scale to keep |O| below ~2.5, where a bf16 output's own rounding stays well inside the
+    # absolute tolerance.
+    g = np.random.Generator(np.random.PCG64(7))
+    B, H, N = 2, 2, 900
+    Q = si.round_bf16(4.0 * g.standard_normal((B, H, N, 64)))
+    ramp = 0.05 * 3.0 ** (np.arange(N) // 128)
+    K = si.round_bf16(g.standard_normal((B, H, N, 64)) * ramp[:, None])
+    V = si.round_bf16(0.5 * g.standard_normal((B, H, N, 64)))
+    key_len = np.array([900, 650], dtype=np.int32)
+    for mask in ["none", "causal", "key_padding"]:
+        kl = key_len if mask == "key_padding" else None
+        O = mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
+                     to_dev(V, torch.bfloat16), mask,
+                     key_len=None if kl is None else torch.from_numpy(kl).cuda())
+        got = host(O)
+        assert np.all(np.isfinite(got))
+        assert_bf16_close(got, oracle.sdpa_ref(Q, K, V, mask, kl), f"sdpa bf16 overflow {mask}")
 
 
 def test_sdpa_bf16_packed_qkv_and_concat_layout():
