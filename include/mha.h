@@ -6,9 +6,14 @@
  *   [LT] lettle.cn translation: 3.1 Encoder and Decoder Stacks (post-norm sublayer),
  *        3.2.1 缩放点积注意力 (Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V),
  *        3.2.2 多头注意力 (per-head projections, concat, output projection).
+ *   [TC] "Transformer 为什么抛弃循环网络" (treecat.cn): 编码器和解码器 (the encoder layer, the
+ *        feed-forward formula and its 512 -> 2048 -> 512 sizes).
+ *   [LC] "Attention Is All You Need" (likecs.com): 1.3 按地址的前向反馈网络 (two linear maps
+ *        with a ReLU between them, applied to every position with the same parameters).
  *   [JY] "Transformer：抛弃循环与卷积的序列建模" (jiashun-ye.github.io): Multi-Head Attention,
- *        Transformer 中的三种 Attention (self / masked self / cross attention),
- *        Residual Connection 与 LayerNorm, 训练样本 (the causal mask), 反向传播 (padding mask).
+ *        Transformer 中的三种 Attention (self / masked self / cross attention), FFN,
+ *        Residual Connection 与 LayerNorm, 训练样本 (the causal mask), 反向传播 (padding mask),
+ *        模型变体与消融实验 (d_ff = 2048 base, 4096 big).
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no
@@ -41,7 +46,7 @@ typedef enum {
   MHA_ERR_INVALID = -1,        /* bad shape, null pointer, unknown enum, causal with Nq != Nk */
   MHA_ERR_UNSUPPORTED = -2,    /* valid request this build does not implement (e.g. bf16 d_k != 64) */
   MHA_ERR_ALIGN = -3,          /* pointer or stride not aligned as the kernel requires */
-  MHA_ERR_WORKSPACE = -4,      /* workspace missing or smaller than mha_layer_workspace_size() */
+  MHA_ERR_WORKSPACE = -4,      /* workspace missing or smaller than the matching *_workspace_size() */
   MHA_ERR_CUDA = -5,           /* a CUDA runtime/driver call or a launch failed */
   MHA_ERR_DEVICE_TIMEOUT = -6  /* a device-side bounded wait ran out (see mha_debug_*) */
 } mha_status;
@@ -163,6 +168,80 @@ int mha_layer_fwd_noalloc(int B, int H, int Nq, int Nk, int D, int d_k, int d_v,
  */
 int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
                    const void* bias, void* Y, int64_t ldy, cudaStream_t stream);
+
+/*
+ * mha_linear_relu_fwd -- Y[M,N] = max(0, X[M,K] W[N,K]^T + bias[N]): the first linear map of
+ * the position-wise feed-forward network with its ReLU ([LC] 1.3; [JY] FFN).  Arguments,
+ * layouts, limits and errors exactly as mha_linear_fwd.
+ */
+int mha_linear_relu_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx,
+                        const void* W, const void* bias, void* Y, int64_t ldy,
+                        cudaStream_t stream);
+
+/*
+ * mha_ffn_workspace_size -- bytes of device workspace mha_ffn_fwd needs: the hidden
+ * activations [M, d_ff] and the second linear map's output [M, D].
+ */
+int mha_ffn_workspace_size(int M, int D, int d_ff, int dtype, size_t* bytes);
+
+/*
+ * mha_ffn_fwd -- one post-norm position-wise feed-forward sublayer ([LT] 3.1; [TC]
+ * 编码器和解码器; [LC] 1.3; [JY] FFN, Residual Connection 与 LayerNorm):
+ *     FFN(x) = max(0, x W1 + b1) W2 + b2       (applied to every row with the same weights)
+ *     y = LayerNorm(x + FFN(x)) * gamma + beta  (biased variance, eps = ln_eps)
+ *
+ *   x, y [M, D] dense row-major (M = tokens); y may not alias x or the workspace.
+ *   W1 [d_ff, D] and W2 [D, d_ff] in nn.Linear layout [out,in]; b1 [d_ff], b2 [D], gamma and
+ *   beta [D], each nullable (= 0, 0, 1, 0).  All share `dtype`; 16-byte aligned pointers.
+ *   workspace: at least mha_ffn_workspace_size() bytes, 256-byte aligned, caller-owned; its
+ *   contents on entry do not matter.
+ *   dtype MHA_BF16: D and d_ff multiples of 64.  Both dtypes: D a multiple of 8, <= 2048.
+ * Launches: the ReLU GEMM, the second GEMM and the residual LayerNorm, all on `stream`.
+ */
+int mha_ffn_fwd(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, const void* W1,
+                const void* b1, const void* W2, const void* b2, const void* gamma,
+                const void* beta, void* y, void* workspace, size_t ws_bytes,
+                cudaStream_t stream);
+
+/*
+ * mha_ffn_fwd_timed -- mha_ffn_fwd plus profiling marks: events[0..3] (caller-created,
+ * n_events >= 4) are recorded on `stream` before the first linear map, before the second,
+ * before the residual LayerNorm and after it.  Same arguments, results and errors as
+ * mha_ffn_fwd; MHA_ERR_INVALID if events is NULL, n_events < 4 or one of the four is NULL.
+ */
+int mha_ffn_fwd_timed(int M, int D, int d_ff, int dtype, float ln_eps, const void* x,
+                      const void* W1, const void* b1, const void* W2, const void* b2,
+                      const void* gamma, const void* beta, void* y, void* workspace,
+                      size_t ws_bytes, cudaStream_t stream, const cudaEvent_t* events,
+                      int n_events);
+
+/*
+ * mha_encoder_layer_workspace_size -- bytes of device workspace mha_encoder_layer_fwd needs
+ * (the attention sublayer's output plus the larger of the two sublayers' workspaces).
+ */
+int mha_encoder_layer_workspace_size(int B, int N, int H, int D, int d_ff, int dtype,
+                                     size_t* bytes);
+
+/*
+ * mha_encoder_layer_fwd -- one encoder layer: the self-attention sublayer, then the
+ * feed-forward sublayer, each with its residual and LayerNorm ([LT] 3.1; [TC] 编码器和解码器;
+ * [JY] Encoder-Decoder):
+ *     h = LayerNorm(x + MultiHead(x, x, x)) * gamma1 + beta1
+ *     y = LayerNorm(h + FFN(h)) * gamma2 + beta2
+ *   x, y [B, N, D]; y may not alias x or the workspace.  H heads of d_k = d_v = D / H.
+ *   W_qkv, b_qkv, W_o, b_o, mask and key_len as for mha_layer_fwd (self-attention; a causal
+ *   mask gives the masked self-attention layer); W1, b1, W2, b2 as for mha_ffn_fwd; gamma1,
+ *   beta1, gamma2, beta2 [D] or NULL.  One ln_eps for both LayerNorms.
+ *   workspace: at least mha_encoder_layer_workspace_size() bytes, 256-byte aligned.
+ *   Limits: those of mha_layer_fwd and mha_ffn_fwd (bf16: D / H == 64).
+ */
+int mha_encoder_layer_fwd(int B, int N, int H, int D, int d_ff, int dtype, int mask,
+                          const int32_t* key_len, float ln_eps, const void* x,
+                          const void* W_qkv, const void* b_qkv, const void* W_o,
+                          const void* b_o, const void* gamma1, const void* beta1,
+                          const void* W1, const void* b1, const void* W2, const void* b2,
+                          const void* gamma2, const void* beta2, void* y, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream);
 
 /*
  * mha_residual_layernorm_fwd -- y = LayerNorm(x + a) * gamma + beta over rows of D features

@@ -1,4 +1,5 @@
-"""CPU oracle for the multi-head attention sublayer forward pass.
+"""CPU oracle for the multi-head attention sublayer forward pass, the position-wise
+feed-forward sublayer and the encoder layer they form.
 
 TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check of ``__graft_entry__``
 and the CPU-baseline leg of ``bench.py`` may import this package.  The product
@@ -6,7 +7,8 @@ path (the CUDA library and its Python binding) never calls it and shares no code
 with it.
 
 Every function computes in float64 with NumPy, following the definitions on the
-pages one step at a time.  See ``oracle.mha_ref`` for the citations.
+pages one step at a time.  See ``oracle.mha_ref`` and ``oracle.ffn`` for the
+citations.
 """
 from .mha_ref import (  # noqa: F401
     allowed_keys,
@@ -16,4 +18,10 @@ from .mha_ref import (  # noqa: F401
     layernorm_ref,
     mha_layer_ref,
     mha_layer_rows_ref,
+)
+from .ffn import (  # noqa: F401
+    relu_ref,
+    ffn_ref,
+    ffn_layer_ref,
+    encoder_layer_ref,
 )

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the multi-head attention sublayer workloads.
+"""Seeded synthetic inputs for the multi-head attention sublayer, the position-wise
+feed-forward sublayer and the encoder layer workloads.
 
 This module draws random numbers and rounds them to bf16; it holds none of the
 attention method's arithmetic.  Both the CPU oracle (through the tests and the
@@ -19,6 +20,13 @@ d_model=1024, h=16 for the big model).  Recipe:
   (drawn after everything above, so the main draws do not move);
 * every floating value is rounded to bf16 (round-to-nearest-even) for the bf16
   workloads; fp32 workloads keep float32 values.
+
+Feed-forward workloads use the pages' inner sizes (d_ff = 2048 for the base model, 4096 for
+the big one): x ~ N(0, 1) [B, N, D], then W1 [d_ff, D] and W2 [D, d_ff], each
+Xavier-uniform on [-sqrt(6/(D+d_ff)), +sqrt(6/(D+d_ff))]; b1, b2 are 0 (or, with
+``affine=True``, 0.1 N(0, 1)), gamma 1 and beta 0 (or 1 + 0.1 N(0, 1) and 0.1 N(0, 1)).
+An encoder-layer workload draws the attention sublayer's inputs exactly as ``draw_layer``
+does and then, from a second generator seeded with seed + 1, the feed-forward weights.
 """
 from __future__ import annotations
 
@@ -33,13 +41,15 @@ __all__ = [
     "draw_sdpa",
     "draw_layer",
     "draw_qkv",
+    "draw_ffn",
+    "draw_encoder",
 ]
 
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str  # "sdpa" or "layer"
+    kind: str  # "sdpa", "layer", "ffn" or "encoder"
     dtype: str  # "f32" or "bf16"
     B: int
     H: int
@@ -50,6 +60,7 @@ class Workload:
     mask: str = "none"  # "none" | "causal" | "key_padding"
     cross: bool = False
     seed: int = 0
+    d_ff: int = 0  # feed-forward inner size ("ffn" and "encoder" workloads)
 
     @property
     def D(self) -> int:
@@ -69,6 +80,17 @@ WORKLOADS = {
         Workload("cross_pad_base_b32_q128_k256", "layer", "bf16", B=32, H=8, Nq=128, Nk=256,
                  mask="key_padding", cross=True, seed=20260004),
         Workload("big_long_b8_n4096", "layer", "bf16", B=8, H=16, Nq=4096, Nk=4096, seed=20260005),
+        # position-wise feed-forward sublayer (D = H * d_k; H only fixes D here)
+        Workload("ffn_f32_b2_n50", "ffn", "f32", B=2, H=1, Nq=50, Nk=50, d_ff=256, seed=20260006),
+        Workload("ffn_base_b32_n128", "ffn", "bf16", B=32, H=8, Nq=128, Nk=128, d_ff=2048,
+                 seed=20260007),
+        Workload("ffn_big_b8_n4096", "ffn", "bf16", B=8, H=16, Nq=4096, Nk=4096, d_ff=4096,
+                 seed=20260008),
+        # encoder layer: self-attention sublayer, then feed-forward sublayer
+        Workload("encoder_base_b32_n128", "encoder", "bf16", B=32, H=8, Nq=128, Nk=128,
+                 d_ff=2048, seed=20260009),
+        Workload("encoder_base_pad_b32_n128", "encoder", "bf16", B=32, H=8, Nq=128, Nk=128,
+                 d_ff=2048, mask="key_padding", seed=20260010),
     ]
 }
 
@@ -143,3 +165,42 @@ def draw_layer(w: Workload, affine: bool = False, batch: slice | None = None):
         key_len = key_len[batch] if key_len is not None else None
     return dict(x_q=x_q, x_kv=x_kv, W_qkv=W_qkv, b_qkv=b_qkv, W_o=W_o, b_o=b_o,
                 gamma=gamma, beta=beta, key_len=key_len)
+
+
+def _ffn_weights(g, D: int, d_ff: int, dt: str, affine: bool):
+    bound = float(np.sqrt(6.0 / (D + d_ff)))
+    W1 = _finish(g.uniform(-bound, bound, (d_ff, D)), dt)
+    W2 = _finish(g.uniform(-bound, bound, (D, d_ff)), dt)
+    if affine:
+        b1 = _finish(0.1 * g.standard_normal(d_ff), dt)
+        b2 = _finish(0.1 * g.standard_normal(D), dt)
+        gamma = _finish(1.0 + 0.1 * g.standard_normal(D), dt)
+        beta = _finish(0.1 * g.standard_normal(D), dt)
+    else:
+        b1 = np.zeros(d_ff, np.float32)
+        b2 = np.zeros(D, np.float32)
+        gamma = np.ones(D, np.float32)
+        beta = np.zeros(D, np.float32)
+    return dict(W1=W1, b1=b1, W2=W2, b2=b2, gamma=gamma, beta=beta)
+
+
+def draw_ffn(w: Workload, affine: bool = False, batch: slice | None = None):
+    """Inputs of one feed-forward sublayer call: x [B,N,D], W1 [d_ff,D], b1 [d_ff],
+    W2 [D,d_ff], b2 [D], gamma [D], beta [D] (float32, bf16-exact for bf16 workloads).
+    ``batch`` keeps only some batch rows of x after drawing all of it."""
+    g = np.random.Generator(np.random.PCG64(w.seed))
+    x = _finish(g.standard_normal((w.B, w.Nq, w.D)), w.dtype)
+    out = _ffn_weights(g, w.D, w.d_ff, w.dtype, affine)
+    out["x"] = x[batch] if batch is not None else x
+    return out
+
+
+def draw_encoder(w: Workload, affine: bool = False):
+    """Inputs of one encoder layer: the attention sublayer's (``draw_layer``: x_q is the
+    layer input, x_kv None) plus the feed-forward weights W1, b1, W2, b2, gamma2, beta2."""
+    att = draw_layer(w, affine=affine)
+    g = np.random.Generator(np.random.PCG64(w.seed + 1))
+    f = _ffn_weights(g, w.D, w.d_ff, w.dtype, affine)
+    att.update(W1=f["W1"], b1=f["b1"], W2=f["W2"], b2=f["b2"], gamma2=f["gamma"],
+               beta2=f["beta"])
+    return att

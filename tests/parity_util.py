@@ -5,11 +5,18 @@ Tolerances (stated for the sublayer's outputs):
   ||gpu - ref||_2 / ||ref||_2 <= 5e-3.
 * fp32 path: ||gpu - ref||_2 / ||ref||_2 <= 1e-5 and |gpu - ref| <= 1e-5 * max(1, |ref|)
   elementwise.
+* bf16 encoder layer (two sublayers in a row, the first one's LayerNorm output h stored in
+  bf16 before the second reads it): max |gpu - ref| <= 4e-2, relative L2 <= 5e-3.  The
+  oracle keeps h exact; rounding h to bf16 moves it by up to 2^-9 |h| (about 0.011 at
+  |h| = 5.5, the largest LayerNorm outputs of these workloads), that error reaches y
+  through the second residual with gain about 1, and y's own bf16 rounding adds as much
+  again: about twice the single-sublayer bound.
 """
 import numpy as np
 
 BF16_MAX_ABS = 2e-2
 BF16_REL_L2 = 5e-3
+BF16_TWO_SUBLAYER_MAX_ABS = 4e-2
 F32_REL = 1e-5
 
 
@@ -23,11 +30,11 @@ def errors(got, ref):
     return max_abs, rel
 
 
-def assert_bf16_close(got, ref, what=""):
+def assert_bf16_close(got, ref, what="", max_abs_bound=BF16_MAX_ABS):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     max_abs, rel = errors(got, ref)
-    assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_L2, \
-        f"{what}: max|d|={max_abs:.3e} (<= {BF16_MAX_ABS}), relL2={rel:.3e} (<= {BF16_REL_L2})"
+    assert max_abs <= max_abs_bound and rel <= BF16_REL_L2, \
+        f"{what}: max|d|={max_abs:.3e} (<= {max_abs_bound}), relL2={rel:.3e} (<= {BF16_REL_L2})"
     return max_abs, rel
 
 

@@ -148,6 +148,87 @@ def test_layernorm_validation(lib):
     assert f(4, 64, 1, float("nan"), FAKE, FAKE, None, None, FAKE, None) == C.MHA_ERR_INVALID
 
 
+def test_linear_relu_validation_matches_linear(lib):
+    for (M, N, K, dt), code in [((0, 64, 64, 1), C.MHA_ERR_INVALID),
+                                ((8, 64, 60, 1), C.MHA_ERR_UNSUPPORTED),
+                                ((8, 96, 64, 1), C.MHA_ERR_UNSUPPORTED)]:
+        assert lib.mha_linear_relu_fwd(M, N, K, dt, FAKE, K, FAKE, None, FAKE, N, None) == code
+    assert lib.mha_linear_relu_fwd(8, 64, 64, 1, ODD, 64, FAKE, None, FAKE, 64, None) == \
+        C.MHA_ERR_ALIGN
+
+
+def ffn(lib, M=64, D=512, d_ff=2048, dt=1, eps=1e-5, x=FAKE, W1=FAKE, W2=FAKE, y=FAKE, ws=FAKE,
+        ws_bytes=1 << 30):
+    return lib.mha_ffn_fwd(M, D, d_ff, dt, eps, x, W1, None, W2, None, None, None, y, ws,
+                           ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), C.MHA_ERR_INVALID),
+    (dict(d_ff=0), C.MHA_ERR_INVALID),
+    (dict(dt=7), C.MHA_ERR_INVALID),
+    (dict(x=None), C.MHA_ERR_INVALID),
+    (dict(W2=None), C.MHA_ERR_INVALID),
+    (dict(eps=float("nan")), C.MHA_ERR_INVALID),
+    (dict(D=520), C.MHA_ERR_UNSUPPORTED),          # bf16: D multiple of 64
+    (dict(d_ff=2000), C.MHA_ERR_UNSUPPORTED),      # bf16: d_ff multiple of 64
+    (dict(D=4096, d_ff=4096), C.MHA_ERR_UNSUPPORTED),  # LayerNorm rows up to 2048
+    (dict(dt=0, D=36), C.MHA_ERR_UNSUPPORTED),     # LayerNorm rows a multiple of 8
+    (dict(ws=None), C.MHA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), C.MHA_ERR_WORKSPACE),
+    (dict(x=ODD), C.MHA_ERR_ALIGN),
+    (dict(ws=ctypes.c_void_p(0x10010)), C.MHA_ERR_ALIGN),  # workspace 256-byte aligned
+])
+def test_ffn_validation(lib, kw, code):
+    assert ffn(lib, **kw) == code
+
+
+def test_ffn_workspace_and_timed_marks(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_ffn_workspace_size(32768, 1024, 4096, 1, ctypes.byref(n)) == 0
+    assert n.value == 2 * (32768 * 4096 + 32768 * 1024)   # hidden + second map, bf16
+    assert lib.mha_ffn_workspace_size(100, 64, 256, 0, ctypes.byref(n)) == 0
+    assert n.value == 102400 + 25600                      # f32, each region 256-byte padded
+    assert lib.mha_ffn_workspace_size(0, 64, 256, 0, ctypes.byref(n)) == C.MHA_ERR_INVALID
+    assert lib.mha_ffn_fwd_timed(64, 512, 2048, 1, 1e-5, FAKE, FAKE, None, FAKE, None, None,
+                                 None, FAKE, FAKE, 1 << 30, None, None, 4) == C.MHA_ERR_INVALID
+    ev = (ctypes.c_void_p * 4)(FAKE, FAKE, None, FAKE)
+    assert lib.mha_ffn_fwd_timed(64, 512, 2048, 1, 1e-5, FAKE, FAKE, None, FAKE, None, None,
+                                 None, FAKE, FAKE, 1 << 30, None,
+                                 ctypes.cast(ev, ctypes.c_void_p), 4) == C.MHA_ERR_INVALID
+
+
+def test_encoder_layer_workspace_and_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_encoder_layer_workspace_size(8, 4096, 16, 1024, 4096, 1,
+                                                ctypes.byref(n)) == 0
+    M = 8 * 4096
+    h = 2 * M * 1024
+    attention = 2 * (M * 3 * 1024 + M * 1024 + M * 1024)
+    feed_forward = 2 * (M * 4096 + M * 1024)
+    assert n.value == h + max(attention, feed_forward)
+    assert lib.mha_encoder_layer_workspace_size(8, 4096, 16, 1000, 4096, 1,
+                                                ctypes.byref(n)) == C.MHA_ERR_INVALID  # D % H
+    assert lib.mha_encoder_layer_workspace_size(8, 4096, 16, 1024, 4000, 1,
+                                                ctypes.byref(n)) == C.MHA_ERR_UNSUPPORTED
+
+    def enc(**kw):
+        a = dict(B=2, N=16, H=8, D=512, d_ff=2048, dt=1, mask=0, x=FAKE, y=ctypes.c_void_p(0x20000),
+                 ws=FAKE, ws_bytes=1 << 30)
+        a.update(kw)
+        return lib.mha_encoder_layer_fwd(a["B"], a["N"], a["H"], a["D"], a["d_ff"], a["dt"],
+                                         a["mask"], None, 1e-5, a["x"], FAKE, None, FAKE, None,
+                                         None, None, FAKE, None, FAKE, None, None, None, a["y"],
+                                         a["ws"], a["ws_bytes"], None)
+
+    assert enc(B=0) == C.MHA_ERR_INVALID
+    assert enc(ws_bytes=4096) == C.MHA_ERR_WORKSPACE
+    assert enc(ws=None) == C.MHA_ERR_WORKSPACE
+    assert enc(y=FAKE) == C.MHA_ERR_INVALID          # y aliases x
+    assert enc(mask=2) == C.MHA_ERR_INVALID          # key padding without key_len
+    assert enc(x=ODD) == C.MHA_ERR_ALIGN
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(C, "_lib", None)
     monkeypatch.setattr(C, "LIB_PATH", str(tmp_path / "missing.so"))

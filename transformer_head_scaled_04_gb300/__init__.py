@@ -1,5 +1,6 @@
-"""GB300 (sm_103a) multi-head attention sublayer forward: a C-ABI CUDA library
-(libmha.so, declared in include/mha.h) and a thin torch binding of it.
+"""GB300 (sm_103a) multi-head attention sublayer forward, with the position-wise
+feed-forward sublayer and the encoder layer they form: a C-ABI CUDA library (libmha.so,
+declared in include/mha.h) and a thin torch binding of it.
 
 The library itself is loaded lazily on first use; ``build.build()`` compiles it in-tree.
 """
@@ -12,6 +13,10 @@ from ._capi import (  # noqa: F401
 )
 from .api import (  # noqa: F401
     device_status,
+    encoder_layer,
+    encoder_layer_workspace_size,
+    ffn,
+    ffn_workspace_size,
     layer_workspace_size,
     linear,
     mha_layer,

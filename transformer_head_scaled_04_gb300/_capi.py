@@ -29,6 +29,14 @@ PROTOTYPES = {
                             + [_size, _vp, _vp, _c_int]),
     "mha_layer_fwd_noalloc": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 9 + [_vp]),
     "mha_linear_fwd": (_c_int, [_c_int] * 4 + [_vp, _i64, _vp, _vp, _vp, _i64, _vp]),
+    "mha_linear_relu_fwd": (_c_int, [_c_int] * 4 + [_vp, _i64, _vp, _vp, _vp, _i64, _vp]),
+    "mha_ffn_workspace_size": (_c_int, [_c_int] * 4 + [ctypes.POINTER(_size)]),
+    "mha_ffn_fwd": (_c_int, [_c_int] * 4 + [_c_float] + [_vp] * 9 + [_size, _vp]),
+    "mha_ffn_fwd_timed": (_c_int, [_c_int] * 4 + [_c_float] + [_vp] * 9
+                          + [_size, _vp, _vp, _c_int]),
+    "mha_encoder_layer_workspace_size": (_c_int, [_c_int] * 6 + [ctypes.POINTER(_size)]),
+    "mha_encoder_layer_fwd": (_c_int, [_c_int] * 7 + [_vp, _c_float] + [_vp] * 15
+                              + [_size, _vp]),
     "mha_residual_layernorm_fwd": (_c_int, [_c_int] * 3 + [_c_float] + [_vp] * 6),
     "mha_status_string": (ctypes.c_char_p, [_c_int]),
     "mha_debug_last_device_status": (_c_int, [_vp]),

@@ -102,8 +102,9 @@ def mha_layer(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, mask="none", ke
     return out
 
 
-def linear(x, W, bias=None, out=None):
-    """Y = x W^T + bias via ``mha_linear_fwd``; x [M,K] (row pitch = x.stride(0)), W [N,K]."""
+def linear(x, W, bias=None, out=None, relu=False):
+    """Y = x W^T + bias via ``mha_linear_fwd`` (``mha_linear_relu_fwd``: max(0, .) when relu);
+    x [M,K] (row pitch = x.stride(0)), W [N,K]."""
     _cuda(x, W, bias, out)
     M, K = x.shape
     N = W.shape[0]
@@ -113,10 +114,84 @@ def linear(x, W, bias=None, out=None):
         out = torch.empty((M, N), dtype=x.dtype, device=x.device)
     if tuple(out.shape) != (M, N) or out.stride(1) != 1:
         raise ValueError(f"linear: out must be [{M},{N}] with unit column stride")
+    fn = C.load().mha_linear_relu_fwd if relu else C.load().mha_linear_fwd
     with torch.cuda.device(x.device):
-        code = C.load().mha_linear_fwd(M, N, K, _dt(x), _ptr(x), x.stride(0), _ptr(W),
-                                       _ptr(bias), _ptr(out), out.stride(0), _stream(x.device))
-    C.check(code, "mha_linear_fwd")
+        code = fn(M, N, K, _dt(x), _ptr(x), x.stride(0), _ptr(W), _ptr(bias), _ptr(out),
+                  out.stride(0), _stream(x.device))
+    C.check(code, "mha_linear_relu_fwd" if relu else "mha_linear_fwd")
+    return out
+
+
+def ffn_workspace_size(M, D, d_ff, dtype) -> int:
+    n = ctypes.c_size_t(0)
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    C.check(C.load().mha_ffn_workspace_size(M, D, d_ff, dt, ctypes.byref(n)),
+            "mha_ffn_workspace_size")
+    return n.value
+
+
+def _contiguous(name, *ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} takes contiguous tensors")
+
+
+def ffn(x, W1, b1, W2, b2, gamma=None, beta=None, eps=1e-5, workspace=None, out=None):
+    """y = LayerNorm(x + max(0, x W1^T + b1) W2^T + b2) over the last axis via ``mha_ffn_fwd``.
+
+    x [..., D] (every row is a position); W1 [d_ff, D]; W2 [D, d_ff]; biases, gamma, beta
+    optional.  workspace: uint8 CUDA tensor of at least ``ffn_workspace_size(...)`` bytes.
+    """
+    _cuda(x, W1, b1, W2, b2, gamma, beta, workspace, out)
+    _contiguous("ffn", x, W1, b1, W2, b2, gamma, beta)
+    D = x.shape[-1]
+    M = x.numel() // D
+    d_ff = W1.shape[0]
+    if tuple(W1.shape) != (d_ff, D) or tuple(W2.shape) != (D, d_ff):
+        raise ValueError(f"ffn: W1 [d_ff, {D}] and W2 [{D}, d_ff] expected")
+    ws = ffn_workspace_size(M, D, d_ff, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        code = C.load().mha_ffn_fwd(M, D, d_ff, _dt(x), float(eps), _ptr(x), _ptr(W1), _ptr(b1),
+                                    _ptr(W2), _ptr(b2), _ptr(gamma), _ptr(beta), _ptr(out),
+                                    _ptr(workspace), workspace.numel(), _stream(x.device))
+    C.check(code, "mha_ffn_fwd")
+    return out
+
+
+def encoder_layer_workspace_size(B, N, H, D, d_ff, dtype) -> int:
+    n = ctypes.c_size_t(0)
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    C.check(C.load().mha_encoder_layer_workspace_size(B, N, H, D, d_ff, dt, ctypes.byref(n)),
+            "mha_encoder_layer_workspace_size")
+    return n.value
+
+
+def encoder_layer(x, W_qkv, b_qkv, W_o, b_o, gamma1, beta1, W1, b1, W2, b2, gamma2, beta2, H,
+                  mask="none", key_len=None, eps=1e-5, workspace=None, out=None):
+    """One encoder layer via ``mha_encoder_layer_fwd``:
+    h = LayerNorm(x + MultiHead(x, x, x)), y = LayerNorm(h + FFN(h)).  x [B,N,D]."""
+    _cuda(x, W_qkv, b_qkv, W_o, b_o, gamma1, beta1, W1, b1, W2, b2, gamma2, beta2, key_len,
+          workspace, out)
+    _contiguous("encoder_layer", x, W_qkv, b_qkv, W_o, b_o, gamma1, beta1, W1, b1, W2, b2,
+                gamma2, beta2)
+    B, N, D = x.shape
+    d_ff = W1.shape[0]
+    ws = encoder_layer_workspace_size(B, N, H, D, d_ff, x.dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        code = C.load().mha_encoder_layer_fwd(
+            B, N, H, D, d_ff, _dt(x), _mask(mask), _ptr(key_len), float(eps), _ptr(x),
+            _ptr(W_qkv), _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma1), _ptr(beta1), _ptr(W1),
+            _ptr(b1), _ptr(W2), _ptr(b2), _ptr(gamma2), _ptr(beta2), _ptr(out),
+            _ptr(workspace), workspace.numel(), _stream(x.device))
+    C.check(code, "mha_encoder_layer_fwd")
     return out
 
 

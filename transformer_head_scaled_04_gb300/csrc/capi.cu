@@ -133,7 +133,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // ------------------------------------------------------------------ step launchers
 int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
-               const void* bias, void* Y, int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+               const void* bias, void* Y, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
+               bool relu = false) {
   cudaError_t e;
   if (dtype == MHA_BF16) {
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);
@@ -141,11 +142,11 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
     CUtensorMap tmX, tmW;
     if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, bn))
       return MHA_ERR_CUDA;
-    e = mha::launch_gemm_bf16(tmX, tmW, bn, bias, Y, M, N, K, ldy, ctx, s);
+    e = mha::launch_gemm_bf16(tmX, tmW, bn, relu, bias, Y, M, N, K, ldy, ctx, s);
   } else {
     e = mha::launch_gemm_f32(static_cast<const float*>(X), ldx, static_cast<const float*>(W),
-                             static_cast<const float*>(bias), static_cast<float*>(Y), ldy, M, N,
-                             K, s);
+                             static_cast<const float*>(bias), relu, static_cast<float*>(Y), ldy,
+                             M, N, K, s);
   }
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -201,6 +202,46 @@ int check_layer_shape(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int
   if (D % 8 != 0 || D > 2048) return MHA_ERR_UNSUPPORTED;  // residual LayerNorm kernel limits
   return MHA_OK;
 }
+
+// Feed-forward sublayer scratch: the hidden activations H [M, d_ff], then FFN(x) [M, D].
+struct FfnPlan {
+  size_t off_h, off_f, total;
+};
+FfnPlan plan_ffn(int M, int D, int d_ff, int dtype) {
+  const size_t es = elem_size(dtype);
+  FfnPlan p;
+  p.off_h = 0;
+  p.off_f = round_up(static_cast<size_t>(M) * d_ff * es, 256);
+  p.total = p.off_f + round_up(static_cast<size_t>(M) * D * es, 256);
+  return p;
+}
+
+int check_ffn_shape(int M, int D, int d_ff, int dtype) {
+  if (M < 1 || D < 1 || d_ff < 1 || !valid_dtype(dtype)) return MHA_ERR_INVALID;
+  if (M > (1 << 24)) return MHA_ERR_UNSUPPORTED;
+  if (dtype == MHA_BF16 && (D % 64 != 0 || d_ff % 64 != 0)) return MHA_ERR_UNSUPPORTED;
+  if (D % 8 != 0 || D > 2048) return MHA_ERR_UNSUPPORTED;  // residual LayerNorm kernel limits
+  return MHA_OK;
+}
+
+// Encoder layer scratch: the attention sublayer's output h [M, D], then one region that the
+// attention sublayer's workspace and, after it, the feed-forward sublayer's workspace share.
+struct EncoderPlan {
+  size_t off_h, off_ws, total;
+};
+EncoderPlan plan_encoder(int B, int N, int H, int D, int d_ff, int dtype) {
+  EncoderPlan p;
+  p.off_h = 0;
+  p.off_ws = round_up(static_cast<size_t>(B) * N * D * elem_size(dtype), 256);
+  const size_t a = plan_layer(B, H, N, N, D, D / H, D / H, dtype).total;
+  const size_t f = plan_ffn(B * N, D, d_ff, dtype).total;
+  p.total = p.off_ws + (a > f ? a : f);
+  return p;
+}
+
+// argument checks shared by the linear-map entry points (defined with them below)
+int check_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
+                 const void* bias, const void* Y, int64_t ldy);
 
 __global__ void wait_selftest_kernel(int* status, uint64_t timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -407,6 +448,48 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
 }
 }  // namespace
 
+namespace {
+// ev: null, or 4 events recorded on `stream` at the step boundaries (before the first linear
+// map, before the second, before the residual LayerNorm, after it).
+int ffn_impl(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, const void* W1,
+             const void* b1, const void* W2, const void* b2, const void* gamma,
+             const void* beta, void* y, void* workspace, size_t ws_bytes, cudaStream_t stream,
+             const cudaEvent_t* ev) {
+  auto mark = [&](int i) {
+    if (ev != nullptr) cudaEventRecord(ev[i], stream);
+  };
+  int st = check_ffn_shape(M, D, d_ff, dtype);
+  if (st != MHA_OK) return st;
+  if (x == nullptr || W1 == nullptr || W2 == nullptr || y == nullptr) return MHA_ERR_INVALID;
+  if (std::isnan(ln_eps) || ln_eps < 0.f) return MHA_ERR_INVALID;
+  const FfnPlan plan = plan_ffn(M, D, d_ff, dtype);
+  if (workspace == nullptr || ws_bytes < plan.total) return MHA_ERR_WORKSPACE;
+  const void* all[] = {x, W1, b1, W2, b2, gamma, beta, y};
+  for (const void* p : all)
+    if (p != nullptr && !aligned(p, 16)) return MHA_ERR_ALIGN;
+  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  DevCtx ctx;
+  st = device_ctx(&ctx);
+  if (st != MHA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* Hb = ws + plan.off_h;
+  uint8_t* F = ws + plan.off_f;
+  mark(0);
+  // H = max(0, x W1^T + b1)
+  st = run_linear(M, d_ff, D, dtype, x, D, W1, b1, Hb, d_ff, ctx, stream, /*relu=*/true);
+  if (st != MHA_OK) return st;
+  mark(1);
+  // F = H W2^T + b2
+  st = run_linear(M, D, d_ff, dtype, Hb, d_ff, W2, b2, F, D, ctx, stream);
+  if (st != MHA_OK) return st;
+  mark(2);
+  // y = LayerNorm(x + F)
+  cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, ln_eps, x, F, gamma, beta, y, stream);
+  mark(3);
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
 int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
@@ -433,6 +516,19 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
 
 int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
                    const void* bias, void* Y, int64_t ldy, cudaStream_t stream) {
+  const int st = check_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy);
+  if (st != MHA_OK) return st;
+  DevCtx ctx;
+  const int sc = device_ctx(&ctx);
+  if (sc != MHA_OK) return sc;
+  return run_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy, ctx, stream);
+}
+
+}  // extern "C"
+
+namespace {
+int check_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
+                 const void* bias, const void* Y, int64_t ldy) {
   if (M < 1 || N < 1 || K < 1 || !valid_dtype(dtype)) return MHA_ERR_INVALID;
   if (M > (1 << 24)) return MHA_ERR_UNSUPPORTED;  // grid.y = M / 128 (or / 64) <= 65535
   if (X == nullptr || W == nullptr || Y == nullptr) return MHA_ERR_INVALID;
@@ -448,10 +544,87 @@ int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, c
         (bias != nullptr && !aligned(bias, 4)))
       return MHA_ERR_ALIGN;
   }
-  DevCtx ctx;
-  const int st = device_ctx(&ctx);
+  return MHA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int mha_linear_relu_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx,
+                        const void* W, const void* bias, void* Y, int64_t ldy,
+                        cudaStream_t stream) {
+  const int st = check_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy);
   if (st != MHA_OK) return st;
-  return run_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy, ctx, stream);
+  DevCtx ctx;
+  const int sc = device_ctx(&ctx);
+  if (sc != MHA_OK) return sc;
+  return run_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy, ctx, stream, /*relu=*/true);
+}
+
+int mha_ffn_workspace_size(int M, int D, int d_ff, int dtype, size_t* bytes) {
+  if (bytes == nullptr) return MHA_ERR_INVALID;
+  const int st = check_ffn_shape(M, D, d_ff, dtype);
+  if (st != MHA_OK) return st;
+  *bytes = plan_ffn(M, D, d_ff, dtype).total;
+  return MHA_OK;
+}
+
+int mha_ffn_fwd(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, const void* W1,
+                const void* b1, const void* W2, const void* b2, const void* gamma,
+                const void* beta, void* y, void* workspace, size_t ws_bytes,
+                cudaStream_t stream) {
+  return ffn_impl(M, D, d_ff, dtype, ln_eps, x, W1, b1, W2, b2, gamma, beta, y, workspace,
+                  ws_bytes, stream, nullptr);
+}
+
+int mha_ffn_fwd_timed(int M, int D, int d_ff, int dtype, float ln_eps, const void* x,
+                      const void* W1, const void* b1, const void* W2, const void* b2,
+                      const void* gamma, const void* beta, void* y, void* workspace,
+                      size_t ws_bytes, cudaStream_t stream, const cudaEvent_t* events,
+                      int n_events) {
+  if (events == nullptr || n_events < 4) return MHA_ERR_INVALID;
+  for (int i = 0; i < 4; ++i)
+    if (events[i] == nullptr) return MHA_ERR_INVALID;
+  return ffn_impl(M, D, d_ff, dtype, ln_eps, x, W1, b1, W2, b2, gamma, beta, y, workspace,
+                  ws_bytes, stream, events);
+}
+
+int mha_encoder_layer_workspace_size(int B, int N, int H, int D, int d_ff, int dtype,
+                                     size_t* bytes) {
+  if (bytes == nullptr) return MHA_ERR_INVALID;
+  if (H < 1 || D < 1 || D % H != 0) return MHA_ERR_INVALID;
+  int st = check_layer_shape(B, H, N, N, D, D / H, D / H, dtype);
+  if (st != MHA_OK) return st;
+  st = check_ffn_shape(B * N, D, d_ff, dtype);
+  if (st != MHA_OK) return st;
+  *bytes = plan_encoder(B, N, H, D, d_ff, dtype).total;
+  return MHA_OK;
+}
+
+int mha_encoder_layer_fwd(int B, int N, int H, int D, int d_ff, int dtype, int mask,
+                          const int32_t* key_len, float ln_eps, const void* x,
+                          const void* W_qkv, const void* b_qkv, const void* W_o,
+                          const void* b_o, const void* gamma1, const void* beta1,
+                          const void* W1, const void* b1, const void* W2, const void* b2,
+                          const void* gamma2, const void* beta2, void* y, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+  size_t need = 0;
+  int st = mha_encoder_layer_workspace_size(B, N, H, D, d_ff, dtype, &need);
+  if (st != MHA_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return MHA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  if (y == x) return MHA_ERR_INVALID;  // x is read again by the second residual
+  const EncoderPlan plan = plan_encoder(B, N, H, D, d_ff, dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* h = ws + plan.off_h;
+  // h = LayerNorm(x + MultiHead(x, x, x))
+  st = layer_impl(B, H, N, N, D, D / H, D / H, dtype, mask, key_len, ln_eps, x, nullptr, W_qkv,
+                  b_qkv, W_o, b_o, gamma1, beta1, h, ws + plan.off_ws, need - plan.off_ws,
+                  stream, nullptr);
+  if (st != MHA_OK) return st;
+  // y = LayerNorm(h + FFN(h))
+  return ffn_impl(B * N, D, d_ff, dtype, ln_eps, h, W1, b1, W2, b2, gamma2, beta2, y,
+                  ws + plan.off_ws, need - plan.off_ws, stream, nullptr);
 }
 
 int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x, const void* a,

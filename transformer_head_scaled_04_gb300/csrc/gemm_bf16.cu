@@ -1,9 +1,12 @@
-// gemm_bf16.cu -- Y[M,N] = X[M,K] W[N,K]^T + bias[N] on the sm_103a tensor cores.
+// gemm_bf16.cu -- Y[M,N] = act(X[M,K] W[N,K]^T + bias[N]) on the sm_103a tensor cores,
+// act = identity or ReLU.
 //
-// This is the projection step of the multi-head attention sublayer: the fused Q|K|V
-// projection of every head (N = 3*d_model) and the output projection W^O ("Attention Is All
-// You Need", lettle.cn translation, 3.2.2 多头注意力; "Transformer：抛弃循环与卷积的序列建模",
-// Multi-Head Attention).
+// These are the projection steps of the sublayers: the fused Q|K|V projection of every head
+// (N = 3*d_model) and the output projection W^O ("Attention Is All You Need", lettle.cn
+// translation, 3.2.2 多头注意力; "Transformer：抛弃循环与卷积的序列建模", Multi-Head
+// Attention), and the two linear maps of the position-wise feed-forward network, the first
+// followed by ReLU ("Attention Is All You Need" on likecs.com, 1.3 按地址的前向反馈网络;
+// "Transformer：抛弃循环与卷积的序列建模", FFN).
 //
 // Persistent kernel: one CTA per SM walks the 128 x BN output tiles (N fastest, so the CTAs
 // running together share the same X rows in L2).
@@ -12,7 +15,8 @@
 //   warp 1     TMEM owner + MMA issuer: tcgen05.mma kind::f16 128xBNx16 into one of two TMEM
 //              accumulators, so the epilogue of tile i overlaps the MMAs of tile i+1
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane quarter per warp), add
-//              bias, round to bf16 (nearest even), store, hand the accumulator back.
+//              bias, ReLU if asked, round to bf16 (nearest even), store, hand the
+//              accumulator back.
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -41,7 +45,7 @@ struct GemmShape {
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
-template <int BN>
+template <int BN, bool kRelu>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
@@ -194,9 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 out[4];
           uint32_t* o32 = reinterpret_cast<uint32_t*>(out);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o32[i] = pack_bf16x2(__uint_as_float(r[2 * i]) + bv[2 * i],
-                                 __uint_as_float(r[2 * i + 1]) + bv[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) {
+            float v0 = __uint_as_float(r[2 * i]) + bv[2 * i];
+            float v1 = __uint_as_float(r[2 * i + 1]) + bv[2 * i + 1];
+            if (kRelu) {
+              v0 = fmaxf(v0, 0.f);
+              v1 = fmaxf(v1, 0.f);
+            }
+            o32[i] = pack_bf16x2(v0, v1);
+          }
           uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * ldy + col);
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[v] = out[v];
@@ -217,11 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN>
+template <int BN, bool kRelu>
 cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void* bias, void* Y,
                       int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
   using S = GemmShape<BN>;
-  auto kern = gemm_bias_bf16_kernel<BN>;
+  auto kern = gemm_bias_bf16_kernel<BN, kRelu>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -236,10 +246,14 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
 }  // namespace
 
 cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
-                             const void* bias, void* Y, int M, int N, int K, int64_t ldy,
-                             const DevCtx& ctx, cudaStream_t s) {
-  if (block_n == 256) return launch_bn<256>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
-  return launch_bn<128>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+                             bool relu, const void* bias, void* Y, int M, int N, int K,
+                             int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+  if (relu) {
+    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+    return launch_bn<128, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+  }
+  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+  return launch_bn<128, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
 }
 
 }  // namespace mha

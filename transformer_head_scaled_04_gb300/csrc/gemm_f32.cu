@@ -1,7 +1,9 @@
-// gemm_f32.cu -- Y[M,N] = X[M,K] W[N,K]^T + bias[N] in fp32 FFMA (SIMT, no TF32).
-// The fp32 variant of the sublayer's projections ("Attention Is All You Need", lettle.cn
-// translation, 3.2.2 多头注意力).  64x64 output tile per 256-thread block, 4x4 per thread,
-// K staged through shared memory 16 at a time.
+// gemm_f32.cu -- Y[M,N] = act(X[M,K] W[N,K]^T + bias[N]) in fp32 FFMA (SIMT, no TF32),
+// act = identity or ReLU.
+// The fp32 variant of the sublayers' projections ("Attention Is All You Need", lettle.cn
+// translation, 3.2.2 多头注意力; "Attention Is All You Need" on likecs.com, 1.3 按地址的前向
+// 反馈网络).  64x64 output tile per 256-thread block, 4x4 per thread, K staged through
+// shared memory 16 at a time.
 #include "launchers.h"
 
 namespace mha {
@@ -12,8 +14,8 @@ constexpr int kKT = 16;
 
 __global__ void __launch_bounds__(256)
     gemm_f32_kernel(const float* __restrict__ X, int64_t ldx, const float* __restrict__ W,
-                    const float* __restrict__ bias, float* __restrict__ Y, int64_t ldy, int M,
-                    int N, int K) {
+                    const float* __restrict__ bias, bool relu, float* __restrict__ Y,
+                    int64_t ldy, int M, int N, int K) {
   __shared__ float sx[kKT][kT + 4];
   __shared__ float sw[kKT][kT + 4];
   const int tx = threadIdx.x & 15;  // column group
@@ -52,7 +54,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int jn = 0; jn < 4; ++jn) {
       const int gn = n0 + tx * 4 + jn;
-      if (gn < N) Y[static_cast<int64_t>(gm) * ldy + gn] = acc[i][jn] + (bias ? bias[gn] : 0.f);
+      if (gn >= N) continue;
+      const float v = acc[i][jn] + (bias ? bias[gn] : 0.f);
+      Y[static_cast<int64_t>(gm) * ldy + gn] = relu ? fmaxf(v, 0.f) : v;
     }
   }
 }
@@ -60,9 +64,10 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
-                            float* Y, int64_t ldy, int M, int N, int K, cudaStream_t s) {
+                            bool relu, float* Y, int64_t ldy, int M, int N, int K,
+                            cudaStream_t s) {
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
-  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, W, bias, Y, ldy, M, N, K);
+  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, W, bias, relu, Y, ldy, M, N, K);
   return cudaGetLastError();
 }
 

@@ -15,14 +15,15 @@ struct DevCtx {
   int num_sms;
 };
 
-// ---- projections: Y[M,N] = X[M,K] W[N,K]^T + bias
+// ---- projections: Y[M,N] = act(X[M,K] W[N,K]^T + bias), act = identity or ReLU (relu)
 // bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W
 // {K, N}, box {64, block_n}; both 128-byte swizzled.  block_n is 128 or 256.
 cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
-                             const void* bias, void* Y, int M, int N, int K, int64_t ldy,
-                             const DevCtx& ctx, cudaStream_t s);
+                             bool relu, const void* bias, void* Y, int M, int N, int K,
+                             int64_t ldy, const DevCtx& ctx, cudaStream_t s);
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
-                            float* Y, int64_t ldy, int M, int N, int K, cudaStream_t s);
+                            bool relu, float* Y, int64_t ldy, int M, int N, int K,
+                            cudaStream_t s);
 
 // ---- attention
 struct SdpaArgs {
