@@ -28,12 +28,15 @@ Readings where the pages leave a step open (each one is also listed in the desig
 * A query row with no allowed key (only possible with key_len = 0) has output 0.
 * Causal masking is defined only for Nq == Nk (self-attention); other shapes raise.
 * Key padding keeps keys j < key_len[b] of batch element b; queries are not masked.
+* Restricted self-attention ([JY] Self-Attention的优势, 总结): each position attends only
+  a neighbourhood of size r; the pages give its size and its O(r n d) cost but not where it
+  sits, so it is read as centred on the query: keys j with |i - j| <= w, r = 2 w + 1.
 """
 from __future__ import annotations
 
 import numpy as np
 
-MASKS = ("none", "causal", "key_padding")
+MASKS = ("none", "causal", "key_padding", "window")
 
 
 def _f64(a):
@@ -41,7 +44,7 @@ def _f64(a):
 
 
 def allowed_keys(mask: str, Nq: int, Nk: int, key_len: int | None = None,
-                 rows: np.ndarray | None = None) -> np.ndarray:
+                 rows: np.ndarray | None = None, window: int | None = None) -> np.ndarray:
     """Boolean [len(rows), Nk] table: True where query row i may attend key j.
 
     * "none": every key ([LT] 3.2.1: the query is compared with all keys).
@@ -49,6 +52,8 @@ def allowed_keys(mask: str, Nq: int, Nk: int, key_len: int | None = None,
       三种 Attention; the 4x4 matrix M of [JY] 训练样本 has its diagonal allowed).
     * "key_padding": j < key_len ([JY] 反向传播: padded <PAD> positions are excluded by a
       padding mask; here the mask is applied to the keys).
+    * "window": |i - j| <= window, the neighbourhood of restricted self-attention ([JY]
+      Self-Attention的优势), self-attention only.
     """
     if mask not in MASKS:
         raise ValueError(f"unknown mask kind {mask!r}")
@@ -60,6 +65,12 @@ def allowed_keys(mask: str, Nq: int, Nk: int, key_len: int | None = None,
         if Nq != Nk:
             raise ValueError("causal mask needs Nq == Nk")
         return j <= i
+    if mask == "window":
+        if Nq != Nk:
+            raise ValueError("window mask needs Nq == Nk")
+        if window is None or int(window) < 0:
+            raise ValueError("window mask needs a radius window >= 0")
+        return np.abs(j - i) <= int(window)
     if key_len is None:
         raise ValueError("key_padding needs key_len")
     L = min(max(int(key_len), 0), Nk)
@@ -88,7 +99,8 @@ def attention_weights_ref(q, k, allowed, scale=None) -> np.ndarray:
     return w
 
 
-def sdpa_ref(Q, K, V, mask: str = "none", key_len=None, scale=None) -> np.ndarray:
+def sdpa_ref(Q, K, V, mask: str = "none", key_len=None, scale=None,
+             window: int | None = None) -> np.ndarray:
     """Attention(Q,K,V) = softmax(QK^T/sqrt(d_k)) V per (batch, head).
 
     Q [B,H,Nq,d_k], K [B,H,Nk,d_k], V [B,H,Nk,d_v] -> O [B,H,Nq,d_v] (float64).
@@ -99,7 +111,8 @@ def sdpa_ref(Q, K, V, mask: str = "none", key_len=None, scale=None) -> np.ndarra
     Nk = K.shape[2]
     O = np.zeros((B, H, Nq, V.shape[3]))
     for b in range(B):
-        allowed = allowed_keys(mask, Nq, Nk, None if key_len is None else key_len[b])
+        allowed = allowed_keys(mask, Nq, Nk, None if key_len is None else key_len[b],
+                               window=window)
         for h in range(H):
             w = attention_weights_ref(Q[b, h], K[b, h], allowed, scale)
             O[b, h] = w @ V[b, h]
