@@ -36,6 +36,7 @@ import seeded_inputs as si  # noqa: E402
 
 METRIC = "SDPA/MHA fwd TFLOP/s & % of GB300 bf16 tensor peak; MHA-layer tokens/s"
 WORKLOAD = "big_long_b8_n4096"
+FFN_WORKLOAD = "ffn_big_b8_n4096"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -61,6 +62,109 @@ def layer_flops(w: si.Workload, mask: str, key_len=None) -> float:
     proj = 2.0 * Mq * D * w.H * w.d_k + 2.0 * Mk * D * w.H * (w.d_k + w.d_v)
     out = 2.0 * Mq * w.H * w.d_v * D
     return proj + sdpa_flops(w, mask, key_len) + out
+
+
+def ffn_flops(M: int, D: int, d_ff: int) -> float:
+    """The two linear maps of the feed-forward sublayer: 2 M D d_ff FLOPs each."""
+    return 4.0 * M * D * d_ff
+
+
+def measure_ffn(lib, C, dev, stream, flush, steps, warmup, peak):
+    """The position-wise feed-forward sublayer of the big model on the same token count."""
+    import torch
+
+    w = si.WORKLOADS[FFN_WORKLOAD]
+    inp = si.draw_ffn(w)
+    t = {k: torch.from_numpy(v).to(dev, torch.bfloat16) for k, v in inp.items()}
+    M = w.B * w.Nq
+    n = ctypes.c_size_t(0)
+    C.check(lib.mha_ffn_workspace_size(M, w.D, w.d_ff, C.MHA_BF16, ctypes.byref(n)), "ffn ws")
+    ws = torch.empty(n.value, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(t["x"])
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    args = (M, w.D, w.d_ff, C.MHA_BF16, 1e-5, vp(t["x"]), vp(t["W1"]), vp(t["b1"]), vp(t["W2"]),
+            vp(t["b2"]), vp(t["gamma"]), vp(t["beta"]), vp(y), vp(ws), n.value, sp)
+    for _ in range(warmup):
+        flush.zero_()
+        C.check(lib.mha_ffn_fwd(*args), "mha_ffn_fwd")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.zero_()
+        arr = (ctypes.c_void_p * 4)(*[e.cuda_event for e in evs[i]])
+        C.check(lib.mha_ffn_fwd_timed(*args, ctypes.cast(arr, ctypes.c_void_p), 4),
+                "mha_ffn_fwd_timed")
+    torch.cuda.synchronize(dev)
+    per = np.array([[evs[i][k].elapsed_time(evs[i][k + 1]) for k in range(3)]
+                    for i in range(steps)])
+    ms = float(per.sum(axis=1).mean())
+    g1 = float(per[:, 0].mean())
+    fl = ffn_flops(M, w.D, w.d_ff)
+    g1_tf = fl / 2 / (g1 * 1e-3) / 1e12
+    return {
+        "workload": f"{FFN_WORKLOAD}: FFN sublayer y = LN(x + max(0, x W1 + b1) W2 + b2), "
+                    f"tokens={M}, d_model={w.D}, d_ff={w.d_ff}",
+        "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+        "flops_per_step": fl, "tokens_per_s": M / (ms * 1e-3),
+        "step_breakdown_ms": {"linear1_relu": g1, "linear2": float(per[:, 1].mean()),
+                              "residual_layernorm": float(per[:, 2].mean())},
+        "roofline": {"kernel": "gemm_bias_bf16_kernel (ReLU epilogue, first linear map)",
+                     "bound": "tensor", "achieved": g1_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": g1_tf / peak, "algorithmic_flops_per_launch": fl / 2},
+        "gpu_launches_per_step": 3,
+    }
+
+
+def measure_encoder(lib, C, dev, stream, flush, steps, warmup):
+    """One encoder layer (self-attention sublayer, then feed-forward sublayer) of the big
+    model on the headline workload's batch."""
+    import torch
+
+    w = si.WORKLOADS[WORKLOAD]
+    wf = si.WORKLOADS[FFN_WORKLOAD]
+    inp = si.draw_layer(w)
+    f = si.draw_ffn(wf)
+    bf = torch.bfloat16
+    t = {k: torch.from_numpy(v).to(dev, bf) for k, v in inp.items()
+         if v is not None and k != "key_len"}
+    tf = {k: torch.from_numpy(v).to(dev, bf) for k, v in f.items() if k != "x"}
+    n = ctypes.c_size_t(0)
+    C.check(lib.mha_encoder_layer_workspace_size(w.B, w.Nq, w.H, w.D, wf.d_ff, C.MHA_BF16,
+                                                 ctypes.byref(n)), "encoder ws")
+    ws = torch.empty(n.value, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(t["x_q"])
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    args = (w.B, w.Nq, w.H, w.D, wf.d_ff, C.MHA_BF16, C.MASKS["none"], None, 1e-5,
+            vp(t["x_q"]), vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]), vp(t["b_o"]),
+            vp(t["gamma"]), vp(t["beta"]), vp(tf["W1"]), vp(tf["b1"]), vp(tf["W2"]),
+            vp(tf["b2"]), vp(tf["gamma"]), vp(tf["beta"]), vp(y), vp(ws), n.value, sp)
+    for _ in range(warmup):
+        flush.zero_()
+        C.check(lib.mha_encoder_layer_fwd(*args), "mha_encoder_layer_fwd")
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        C.check(lib.mha_encoder_layer_fwd(*args), "mha_encoder_layer_fwd")
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    step = float(np.mean(ms))
+    fl = layer_flops(w, "none") + ffn_flops(w.B * w.Nq, w.D, wf.d_ff)
+    return {
+        "workload": f"encoder layer of the big model: self-attention sublayer then FFN "
+                    f"sublayer, B={w.B}, n={w.Nq}, d_model={w.D}, h={w.H}, d_ff={wf.d_ff}",
+        "value": fl / (step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": step,
+        "flops_per_step": fl, "tokens_per_s": w.B * w.Nq / (step * 1e-3),
+        "gpu_launches_per_step": 7,
+    }
 
 
 def recorded_traffic(kernel: str, sources: list[str]):
@@ -390,6 +494,10 @@ def run_ours(args):
     fl_c = layer_flops(w, "causal")
     fl_c_sdpa = sdpa_flops(w, "causal")
 
+    # the feed-forward sublayer and the whole encoder layer on the same tokens
+    ffn = measure_ffn(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
+    encoder = measure_encoder(lib, C, dev, stream, flush, max(3, args.steps // 2), args.warmup)
+
     # end to end through the public API: pinned host x -> device, sublayer, y -> pinned host
     x_host = t["x_q"].cpu().pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
@@ -449,6 +557,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
+        "ffn": ffn,
+        "encoder_layer": encoder,
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, w, "none")

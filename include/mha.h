@@ -12,6 +12,7 @@
  *        with a ReLU between them, applied to every position with the same parameters).
  *   [JY] "Transformer：抛弃循环与卷积的序列建模" (jiashun-ye.github.io): Multi-Head Attention,
  *        Transformer 中的三种 Attention (self / masked self / cross attention), FFN,
+ *        Self-Attention的优势 and 总结 (restricted self-attention over a neighbourhood r),
  *        Residual Connection 与 LayerNorm, 训练样本 (the causal mask), 反向传播 (padding mask),
  *        模型变体与消融实验 (d_ff = 2048 base, 4096 big).
  *
@@ -81,6 +82,21 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
                  const int32_t* key_len, float scale,
                  const void* Q, const void* K, const void* V, void* O,
                  const int64_t* strides, cudaStream_t stream);
+
+/*
+ * mha_sdpa_window_fwd -- restricted self-attention ([JY] Self-Attention的优势, 总结): every
+ * position attends only the neighbourhood of size r = 2*window + 1 centred on it,
+ *     O[b,h,i] = softmax_j(Q[b,h,i] . K[b,h,j] * scale, |i - j| <= window) V[b,h,j]
+ * so the work is O(r n d) instead of O(n^2 d).  The pages give the neighbourhood's size,
+ * not its placement; centred on the query is the reading taken here.
+ *   Q, K, V, O [B,H,N,d] (self-attention: Nq = Nk = N); strides, scale, dtype limits and
+ *   errors as for mha_sdpa_fwd.  window >= 0 (0: each position sees itself only; N - 1 or
+ *   more: full attention); window < 0 is MHA_ERR_INVALID.  Only the key tiles that a query
+ *   block's band touches are read.
+ */
+int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
+                        float scale, const void* Q, const void* K, const void* V, void* O,
+                        const int64_t* strides, cudaStream_t stream);
 
 /*
  * mha_layer_workspace_size -- bytes of device workspace mha_layer_fwd needs for these sizes.

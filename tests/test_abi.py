@@ -234,3 +234,16 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(C, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         C.load()
+
+
+def test_sdpa_window_validation(lib):
+    f = lib.mha_sdpa_window_fwd
+    assert f(1, 1, 8, 64, 64, 1, -1, 0.0, FAKE, FAKE, FAKE, FAKE, None, None) == C.MHA_ERR_INVALID
+    assert f(0, 1, 8, 64, 64, 1, 2, 0.0, FAKE, FAKE, FAKE, FAKE, None, None) == C.MHA_ERR_INVALID
+    assert f(1, 1, 8, 32, 64, 1, 2, 0.0, FAKE, FAKE, FAKE, FAKE, None, None) == \
+        C.MHA_ERR_UNSUPPORTED
+    assert f(1, 1, 8, 64, 64, 1, 2, 0.0, ODD, FAKE, FAKE, FAKE, None, None) == C.MHA_ERR_ALIGN
+    assert f(1, 1, 8, 64, 64, 1, 2, 0.0, FAKE, FAKE, FAKE, None, None, None) == C.MHA_ERR_INVALID
+    # the window is not one of mha_sdpa_fwd's mask kinds
+    assert lib.mha_sdpa_fwd(1, 1, 8, 8, 64, 64, 1, 3, None, 0.0, FAKE, FAKE, FAKE, FAKE, None,
+                            None) == C.MHA_ERR_INVALID

@@ -120,14 +120,74 @@ def test_sdpa_bf16_later_tiles_overflowing_the_first_tile_max():
     K = si.round_bf16(g.standard_normal((B, H, N, 64)) * ramp[:, None])
     V = si.round_bf16(0.5 * g.standard_normal((B, H, N, 64)))
     key_len = np.array([900, 650], dtype=np.int32)
-    for mask in ["none", "causal", "key_padding"]:
+    for mask in ["none", "causal", "key_padding", "window"]:
         kl = key_len if mask == "key_padding" else None
+        win = 300 if mask == "window" else None
         O = mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
                      to_dev(V, torch.bfloat16), mask,
-                     key_len=None if kl is None else torch.from_numpy(kl).cuda())
+                     key_len=None if kl is None else torch.from_numpy(kl).cuda(), window=win)
         got = host(O)
         assert np.all(np.isfinite(got))
-        assert_bf16_close(got, oracle.sdpa_ref(Q, K, V, mask, kl), f"sdpa bf16 overflow {mask}")
+        assert_bf16_close(got, oracle.sdpa_ref(Q, K, V, mask, kl, window=win),
+                          f"sdpa bf16 overflow {mask}")
+
+
+WINDOW_CASES = [
+    (1, 2, 640, 0), (1, 2, 640, 1), (1, 1, 640, 63), (2, 1, 700, 128), (1, 2, 1000, 300),
+    (1, 1, 129, 5), (1, 1, 1, 3), (1, 1, 300, 299), (1, 1, 300, 5000),
+]
+
+
+@pytest.mark.parametrize("B,H,N,win", WINDOW_CASES)
+def test_sdpa_bf16_window(B, H, N, win):
+    Q, K, V, _ = si.draw_sdpa(B, H, N, N, dtype="bf16", seed=300 + N + win)
+    O = mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16), to_dev(V, torch.bfloat16),
+                 "window", window=win)
+    assert_bf16_close(host(O), oracle.sdpa_ref(Q, K, V, "window", window=win),
+                      f"sdpa bf16 window {B}x{H} N={N} w={win}")
+
+
+@pytest.mark.parametrize("N,win,dk,dv", [(77, 3, 64, 64), (50, 0, 32, 48), (40, 100, 128, 16)])
+def test_sdpa_f32_window(N, win, dk, dv):
+    Q, K, V, _ = si.draw_sdpa(2, 2, N, N, dk, dv, "f32", seed=17)
+    O = mha.sdpa(to_dev(Q, torch.float32), to_dev(K, torch.float32), to_dev(V, torch.float32),
+                 "window", window=win)
+    assert_f32_close(host(O), oracle.sdpa_ref(Q, K, V, "window", window=win),
+                     f"sdpa f32 window N={N} w={win}")
+
+
+def test_sdpa_bf16_window_keys_outside_band_cannot_change_outputs_bitwise():
+    B, H, N, win = 1, 2, 900, 100
+    Q, K, V, _ = si.draw_sdpa(B, H, N, N, dtype="bf16", seed=33)
+    tq = to_dev(Q, torch.bfloat16)
+    O = host(mha.sdpa(tq, to_dev(K, torch.bfloat16), to_dev(V, torch.bfloat16), "window",
+                      window=win))
+    rows = slice(400, 500)   # their bands cover keys 300..599
+    K2, V2 = K.copy(), V.copy()
+    K2[:, :, :300] = si.round_bf16(K2[:, :, :300] * -2.0 + 1.0)
+    K2[:, :, 600:] = 3.0
+    V2[:, :, :300] = -6.0
+    V2[:, :, 600:] = 6.0
+    O2 = host(mha.sdpa(tq, to_dev(K2, torch.bfloat16), to_dev(V2, torch.bfloat16), "window",
+                       window=win))
+    assert np.array_equal(O[:, :, rows], O2[:, :, rows])
+    assert not np.array_equal(O[:, :, :200], O2[:, :, :200])
+
+
+def test_sdpa_bf16_window_big_workload_sampled_rows():
+    # the big model's heads at n = 4096 with a 513-key neighbourhood, rows sampled per (b, h)
+    w = si.WORKLOADS["big_long_b8_n4096"]
+    win = 256
+    Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="bf16", seed=w.seed)
+    O = host(mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
+                      to_dev(V, torch.bfloat16), "window", window=win))
+    g = np.random.Generator(np.random.PCG64(81))
+    for b, h in [(0, 0), (w.B - 1, w.H - 1), (3, 7)]:
+        rows = np.unique(np.concatenate([[0, 255, 256, w.Nq - 1], g.integers(0, w.Nq, 28)]))
+        allowed = oracle.allowed_keys("window", w.Nq, w.Nk, rows=rows, window=win)
+        ref = oracle.attention_weights_ref(Q[b, h, rows], K[b, h], allowed) @ \
+            np.asarray(V[b, h], np.float64)
+        assert_bf16_close(O[b, h, rows], ref, f"sdpa bf16 window big b={b} h={h}")
 
 
 def test_sdpa_bf16_packed_qkv_and_concat_layout():

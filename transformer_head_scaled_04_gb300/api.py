@@ -42,8 +42,9 @@ def _mask(mask) -> int:
     return C.MASKS[mask]
 
 
-def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None):
-    """O = softmax(q k^T * scale) v per (batch, head) via ``mha_sdpa_fwd``.
+def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None, window=None):
+    """O = softmax(q k^T * scale) v per (batch, head) via ``mha_sdpa_fwd``
+    (``mha_sdpa_window_fwd`` for mask="window": keys within ``window`` positions of the query).
 
     q [B,H,Nq,d_k], k [B,H,Nk,d_k], v [B,H,Nk,d_v] (any strides the kernel accepts);
     out [B,H,Nq,d_v] is allocated if not given and may be a strided view.
@@ -56,6 +57,16 @@ def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None):
         out = torch.empty((B, H, Nq, d_v), dtype=q.dtype, device=q.device)
     strides = (ctypes.c_int64 * 16)(*(list(q.stride()) + list(k.stride()) + list(v.stride())
                                       + list(out.stride())))
+    if mask == "window":
+        if window is None or Nq != Nk:
+            raise ValueError("mask='window' needs self-attention shapes and a window radius")
+        with torch.cuda.device(q.device):
+            code = C.load().mha_sdpa_window_fwd(B, H, Nq, d_k, d_v, _dt(q), int(window),
+                                                float(scale or 0.0), _ptr(q), _ptr(k), _ptr(v),
+                                                _ptr(out), ctypes.cast(strides, ctypes.c_void_p),
+                                                _stream(q.device))
+        C.check(code, "mha_sdpa_window_fwd")
+        return out
     with torch.cuda.device(q.device):
         code = C.load().mha_sdpa_fwd(B, H, Nq, Nk, d_k, d_v, _dt(q), _mask(mask), _ptr(key_len),
                                      float(scale or 0.0), _ptr(q), _ptr(k), _ptr(v), _ptr(out),

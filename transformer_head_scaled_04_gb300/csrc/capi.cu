@@ -283,12 +283,18 @@ const char* mha_status_string(int st) {
   }
 }
 
-int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
-                 const int32_t* key_len, float scale, const void* Q, const void* K, const void* V,
-                 void* O, const int64_t* strides, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// mask: an mha_mask value or mha::kMaskWindow (then `window` is the neighbourhood radius)
+int sdpa_entry(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+               const int32_t* key_len, int window, float scale, const void* Q, const void* K,
+               const void* V, void* O, const int64_t* strides, cudaStream_t stream) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d_k < 1 || d_v < 1) return MHA_ERR_INVALID;
-  if (!valid_dtype(dtype) || mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING)
+  if (!valid_dtype(dtype) || mask < MHA_MASK_NONE ||
+      (mask > MHA_MASK_KEY_PADDING && mask != mha::kMaskWindow))
     return MHA_ERR_INVALID;
+  if (mask == mha::kMaskWindow && (Nq != Nk || window < 0)) return MHA_ERR_INVALID;
   if (mask == MHA_MASK_CAUSAL && Nq != Nk) return MHA_ERR_INVALID;
   if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
   if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return MHA_ERR_INVALID;
@@ -301,6 +307,8 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
   a.B = B; a.H = H; a.Nq = Nq; a.Nk = Nk; a.d_k = d_k; a.d_v = d_v;
   a.mask = mask;
   a.key_len = (mask == MHA_MASK_KEY_PADDING) ? key_len : nullptr;
+  // a radius of Nk or more already reaches every key
+  a.window = (mask == mha::kMaskWindow) ? (window < Nk ? window : Nk) : 0;
   a.Q = Q; a.K = K; a.V = V; a.O = O;
   const int64_t cont[4][4] = {
       {static_cast<int64_t>(H) * Nq * d_k, static_cast<int64_t>(Nq) * d_k, d_k, 1},
@@ -332,6 +340,24 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
   if (st != MHA_OK) return st;
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
   return run_sdpa(a, dtype, ctx, stream);
+}
+}  // namespace
+
+extern "C" {
+
+int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                 const int32_t* key_len, float scale, const void* Q, const void* K, const void* V,
+                 void* O, const int64_t* strides, cudaStream_t stream) {
+  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
+  return sdpa_entry(B, H, Nq, Nk, d_k, d_v, dtype, mask, key_len, 0, scale, Q, K, V, O, strides,
+                    stream);
+}
+
+int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
+                        float scale, const void* Q, const void* K, const void* V, void* O,
+                        const int64_t* strides, cudaStream_t stream) {
+  return sdpa_entry(B, H, N, N, d_k, d_v, dtype, mha::kMaskWindow, nullptr, window, scale, Q, K,
+                    V, O, strides, stream);
 }
 
 int mha_layer_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,

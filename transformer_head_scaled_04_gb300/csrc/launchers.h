@@ -26,9 +26,14 @@ cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const f
                             cudaStream_t s);
 
 // ---- attention
+// Mask kinds beyond the public mha_mask values: restricted self-attention, where query i
+// attends keys j with |i - j| <= SdpaArgs::window.
+constexpr int kMaskWindow = 3;
+
 struct SdpaArgs {
   int B, H, Nq, Nk, d_k, d_v;
-  int mask;                  // mha_mask
+  int mask;                  // mha_mask, or kMaskWindow
+  int window = 0;            // radius of the restricted-attention neighbourhood (kMaskWindow)
   const int32_t* key_len;    // device, B entries (key padding) or null
   float scale;               // multiplies q.k
   const void* Q;             // used by the f32 path (the bf16 path reads through TMA maps)

@@ -96,6 +96,7 @@ constexpr int kNumBars = kBarDrain + 1;
 
 struct Params {
   int B, H, Nq, Nk, mask;
+  int window;  // kMaskWindow: query i attends keys j with |i - j| <= window
   const int32_t* key_len;
   float scale_log2;  // scale * log2(e)
   __nv_bfloat16* O;
@@ -143,6 +144,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // keys a row may see: causal -> j <= row; otherwise j < L
   int L = p.Nk;
   if (p.mask == 2) L = min(max(__ldg(p.key_len + b), 0), p.Nk);
+  // Restricted attention: both query tiles walk the key tiles that the block's whole band
+  // [q0 - window, last row + window] touches, starting at key tile kt0; rows mask the keys
+  // outside their own band, so a tile can be fully masked for one of the two query tiles.
+  int kt0 = 0, n_band = 0;
+  if (p.mask == kMaskWindow) {
+    const int last = min(q0 + 2 * kBQ, p.Nq) - 1;
+    kt0 = max(q0 - p.window, 0) / kBKV;
+    n_band = min(last + p.window, p.Nk - 1) / kBKV - kt0 + 1;
+  }
   int n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
@@ -151,6 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       n_t[t] = 0;
     else if (p.mask == 1)
       n_t[t] = min(p.Nq - 1, row0 + kBQ - 1) / kBKV + 1;
+    else if (p.mask == kMaskWindow)
+      n_t[t] = n_band;
     else
       n_t[t] = (L + kBKV - 1) / kBKV;
   }
@@ -199,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // since S(j+1) = Q K(j+1)^T is issued right before O += P(j) V(j).
       bool ok = true;
       mbar_arrive_expect_tx(bar(kBarK0), kTileBytes);
-      tma_load_4d(sK0, &tmK, bar(kBarK0), 0, 0, h, b);
+      tma_load_4d(sK0, &tmK, bar(kBarK0), 0, kt0 * kBKV, h, b);
       int issued = 0;
       for (int j = 0; j < nmax; ++j) {
         const bool next_k = j + 1 < nmax;
@@ -213,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t kv = bar(kBarKV + j % kKStages);
         mbar_arrive_expect_tx(kv, next_k ? 2 * kTileBytes : kTileBytes);
-        if (next_k) tma_load_4d(sK + sk * kTileBytes, &tmK, kv, 0, (j + 1) * kBKV, h, b);
-        tma_load_4d(sV + sv * kTileBytes, &tmV, kv, 0, j * kBKV, h, b);
+        if (next_k)
+          tma_load_4d(sK + sk * kTileBytes, &tmK, kv, 0, (kt0 + j + 1) * kBKV, h, b);
+        tma_load_4d(sV + sv * kTileBytes, &tmV, kv, 0, (kt0 + j) * kBKV, h, b);
         issued = j + 1;
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteProducer);
@@ -324,7 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + kColO + t * kHD + lane_off;
     const uint32_t tP = tmem + kColP + t * 64 + lane_off;
     const int nt = ntiles(t);
-    const int limit = (p.mask == 1) ? row : L - 1;  // allowed keys: j <= limit
+    // allowed keys: first <= j <= limit
+    const int limit = (p.mask == 1)             ? row
+                      : (p.mask == kMaskWindow) ? min(row + p.window, p.Nk - 1)
+                                                : L - 1;
+    const int first = (p.mask == kMaskWindow) ? row - p.window : 0;
     const float c = p.scale_log2;
     float m_used = -INFINITY;
     float l = 0.f;
@@ -337,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int col0 = j * kBKV;
-      const bool masked = col0 + kBKV - 1 > limit;  // diagonal / padding tile
+      const int col0 = (kt0 + j) * kBKV;
+      const bool masked = col0 + kBKV - 1 > limit || col0 < first;  // diagonal / edge tile
       float sv[128];
       // the whole S row of this tile: 128 fp32 in registers, one TMEM round trip
       auto load_s = [&]() {
@@ -362,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (masked) {  // exclude keys past limit
 #pragma unroll
           for (int i = 0; i < 128; ++i)
-            if (col0 + i > limit) sv[i] = -INFINITY;
+            if (col0 + i > limit || col0 + i < first) sv[i] = -INFINITY;
         }
       };
       auto row_max = [&]() {
@@ -530,6 +547,7 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.mask = a.mask;
+  p.window = a.window;
   p.key_len = a.key_len;
   const double c = static_cast<double>(a.scale) * 1.4426950408889634;  // log2(e)
   p.scale_log2 = static_cast<float>(c);
