@@ -37,6 +37,7 @@ import seeded_inputs as si  # noqa: E402
 METRIC = "SDPA/MHA fwd TFLOP/s & % of GB300 bf16 tensor peak; MHA-layer tokens/s"
 WORKLOAD = "big_long_b8_n4096"
 FFN_WORKLOAD = "ffn_big_b8_n4096"
+WINDOW = 256
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -62,6 +63,51 @@ def layer_flops(w: si.Workload, mask: str, key_len=None) -> float:
     proj = 2.0 * Mq * D * w.H * w.d_k + 2.0 * Mk * D * w.H * (w.d_k + w.d_v)
     out = 2.0 * Mq * w.H * w.d_v * D
     return proj + sdpa_flops(w, mask, key_len) + out
+
+
+def window_pairs(B: int, H: int, N: int, window: int) -> int:
+    """Allowed (query, key) pairs of restricted self-attention: |i - j| <= window."""
+    i = np.arange(N)
+    per_row = np.minimum(i + window, N - 1) - np.maximum(i - window, 0) + 1
+    return int(B * H * per_row.sum())
+
+
+def measure_window(lib, C, dev, stream, flush, steps, warmup, peak, window=WINDOW):
+    """Restricted self-attention on the big model's heads at n = 4096 (neighbourhood
+    2 * window + 1), as one attention launch on contiguous [B, H, N, 64] Q, K, V."""
+    import torch
+
+    w = si.WORKLOADS[WORKLOAD]
+    Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="bf16", seed=w.seed)
+    tq, tk, tv = (torch.from_numpy(a).to(dev, torch.bfloat16) for a in (Q, K, V))
+    O = torch.empty_like(tq)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    args = (w.B, w.H, w.Nq, 64, 64, C.MHA_BF16, window, 0.0, vp(tq), vp(tk), vp(tv), vp(O),
+            None, sp)
+    for _ in range(warmup):
+        flush.zero_()
+        C.check(lib.mha_sdpa_window_fwd(*args), "mha_sdpa_window_fwd")
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        C.check(lib.mha_sdpa_window_fwd(*args), "mha_sdpa_window_fwd")
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = float(np.mean(ms))
+    fl = 2.0 * (64 + 64) * window_pairs(w.B, w.H, w.Nq, window)
+    tf = fl / (t * 1e-3) / 1e12
+    return {
+        "workload": f"restricted self-attention, B={w.B}, H={w.H}, n={w.Nq}, d=64, "
+                    f"neighbourhood |i-j| <= {window} ({2 * window + 1} keys)",
+        "value": tf, "unit": "TFLOP/s (allowed pairs only)", "ms": t,
+        "flops_per_launch": fl, "frac_of_peak": tf / peak,
+        "speedup_vs_full_attention_time": None,
+    }
 
 
 def ffn_flops(M: int, D: int, d_ff: int) -> float:
@@ -496,6 +542,8 @@ def run_ours(args):
 
     # the feed-forward sublayer and the whole encoder layer on the same tokens
     ffn = measure_ffn(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
+    window = measure_window(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
+    window["speedup_vs_full_attention_time"] = sdpa_ms / window["ms"]
     encoder = measure_encoder(lib, C, dev, stream, flush, max(3, args.steps // 2), args.warmup)
 
     # end to end through the public API: pinned host x -> device, sublayer, y -> pinned host
@@ -559,6 +607,7 @@ def run_ours(args):
         "clocks": clocks,
         "ffn": ffn,
         "encoder_layer": encoder,
+        "window": window,
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, w, "none")
