@@ -31,12 +31,17 @@ Readings where the pages leave a step open (each one is also listed in the desig
 * Restricted self-attention ([JY] Self-Attention的优势, 总结): each position attends only
   a neighbourhood of size r; the pages give its size and its O(r n d) cost but not where it
   sits, so it is read as centred on the query: keys j with |i - j| <= w, r = 2 w + 1.
+* Autoregressive decoding ([JY] Transformer 翻译样例 > Decoder, Transformer 训练样例): at each
+  step the newest target positions attend every earlier position and themselves.  Keys and
+  values of earlier positions never change under the causal mask, so they are read from a
+  cache of the first L = key_len[b] positions; the Nq new queries are the last Nq of those L
+  positions (query i sits at position L - Nq + i): the causal mask aligned bottom-right.
 """
 from __future__ import annotations
 
 import numpy as np
 
-MASKS = ("none", "causal", "key_padding", "window")
+MASKS = ("none", "causal", "key_padding", "window", "causal_cache")
 
 
 def _f64(a):
@@ -54,6 +59,9 @@ def allowed_keys(mask: str, Nq: int, Nk: int, key_len: int | None = None,
       padding mask; here the mask is applied to the keys).
     * "window": |i - j| <= window, the neighbourhood of restricted self-attention ([JY]
       Self-Attention的优势), self-attention only.
+    * "causal_cache": decoding against a cache holding the first L = key_len positions; query
+      i is position L - Nq + i and attends j <= L - Nq + i ([JY] Transformer 翻译样例 >
+      Decoder: the masked self-attention of one generation step).
     """
     if mask not in MASKS:
         raise ValueError(f"unknown mask kind {mask!r}")
@@ -72,8 +80,12 @@ def allowed_keys(mask: str, Nq: int, Nk: int, key_len: int | None = None,
             raise ValueError("window mask needs a radius window >= 0")
         return np.abs(j - i) <= int(window)
     if key_len is None:
-        raise ValueError("key_padding needs key_len")
+        raise ValueError(f"{mask} needs key_len")
     L = min(max(int(key_len), 0), Nk)
+    if mask == "causal_cache":
+        if Nq > L:
+            raise ValueError("causal_cache needs Nq <= key_len (the new queries are cached)")
+        return j <= (L - Nq) + i
     return np.broadcast_to(j < L, (i.shape[0], Nk)).copy()
 
 
