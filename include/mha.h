@@ -13,6 +13,7 @@
  *   [JY] "Transformer：抛弃循环与卷积的序列建模" (jiashun-ye.github.io): Multi-Head Attention,
  *        Transformer 中的三种 Attention (self / masked self / cross attention), FFN,
  *        Self-Attention的优势 and 总结 (restricted self-attention over a neighbourhood r),
+ *        Transformer 翻译样例 > Decoder (one generation step at a time),
  *        Residual Connection 与 LayerNorm, 训练样本 (the causal mask), 反向传播 (padding mask),
  *        模型变体与消融实验 (d_ff = 2048 base, 4096 big).
  *
@@ -97,6 +98,42 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
 int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
                         float scale, const void* Q, const void* K, const void* V, void* O,
                         const int64_t* strides, cudaStream_t stream);
+
+/*
+ * mha_decode_workspace_size -- bytes of device workspace mha_sdpa_decode_fwd needs: for
+ * MHA_BF16 one fp32 partial result (64 columns, a max and a sum) per (batch, head, 256-key
+ * chunk of the cache, query); for MHA_F32 a token 256 bytes (that path keeps no partials).
+ * MHA_ERR_UNSUPPORTED for bf16 with Nq > 16.
+ */
+int mha_decode_workspace_size(int B, int H, int Nq, int Lmax, int dtype, size_t* bytes);
+
+/*
+ * mha_sdpa_decode_fwd -- attention for one autoregressive generation step against a
+ * key/value cache ([JY] Transformer 翻译样例 > Decoder: each step's newest target positions
+ * attend every position generated so far, and the encoder output Z; Transformer 训练样例:
+ * the causal mask during training, one position at a time during generation):
+ *     O[b,h,i] = softmax_j(Q[b,h,i] . K[b,h,j] * scale, allowed) V[b,h,j]
+ *   allowed: j < L_b = cache_len[b] (the cache's valid prefix; cross-attention to Z), and
+ *   with causal = 1 also j <= L_b - Nq + i: the Nq queries are the newest of the L_b cached
+ *   positions, i.e. the causal mask aligned bottom-right (masked self-attention).
+ *   Keys and values of earlier positions never change under the causal mask, so caching
+ *   them computes the same result as re-running the whole prefix.
+ *
+ *   Q [B,H,Nq,d_k] (the new positions' queries); K, V caches [B,H,Lmax,d] (capacity Lmax,
+ *   the new positions already written at L_b - Nq .. L_b - 1); O [B,H,Nq,d_v] (written).
+ *   strides: NULL for contiguous, or 16 element strides {Q, K, V, O} x {b, h, n, d} as for
+ *   mha_sdpa_fwd.  cache_len: device int32[B], clamped to [0, Lmax] on the device; rows that
+ *   end up with no allowed key (L_b = 0, or L_b < Nq with causal = 1) are written as zeros.
+ *   scale: > 0 uses it, <= 0 means 1/sqrt(d_k).  causal must be 0 or 1; Nq <= Lmax.
+ *   workspace: at least mha_decode_workspace_size() bytes, 256-byte aligned, caller-owned.
+ *   dtype MHA_BF16: d_k == d_v == 64, 1 <= Nq <= 16, strides and pointers as for
+ *   mha_sdpa_fwd's bf16 path; memory-bound split-K kernel (256-key chunks of the cache per
+ *   CTA, then one merge launch).  dtype MHA_F32: d_k, d_v <= 128 (SIMT kernel).
+ */
+int mha_sdpa_decode_fwd(int B, int H, int Nq, int Lmax, int d_k, int d_v, int dtype, int causal,
+                        const int32_t* cache_len, float scale, const void* Q, const void* K,
+                        const void* V, void* O, const int64_t* strides, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream);
 
 /*
  * mha_layer_workspace_size -- bytes of device workspace mha_layer_fwd needs for these sizes.

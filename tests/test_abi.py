@@ -247,3 +247,33 @@ def test_sdpa_window_validation(lib):
     # the window is not one of mha_sdpa_fwd's mask kinds
     assert lib.mha_sdpa_fwd(1, 1, 8, 8, 64, 64, 1, 3, None, 0.0, FAKE, FAKE, FAKE, FAKE, None,
                             None) == C.MHA_ERR_INVALID
+
+
+def test_decode_workspace_and_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_decode_workspace_size(64, 16, 1, 4096, 1, ctypes.byref(n)) == 0
+    assert n.value == 64 * 16 * 16 * 1 * 66 * 4           # 16 chunks of 256 keys, fp32 partials
+    assert lib.mha_decode_workspace_size(2, 2, 3, 300, 1, ctypes.byref(n)) == 0
+    assert n.value == (2 * 2 * 2 * 3 * 66 * 4 + 255) // 256 * 256
+    assert lib.mha_decode_workspace_size(1, 1, 17, 300, 1, ctypes.byref(n)) == \
+        C.MHA_ERR_UNSUPPORTED
+    assert lib.mha_decode_workspace_size(1, 1, 17, 300, 0, ctypes.byref(n)) == 0   # fp32: any Nq
+
+    def dec(**kw):
+        a = dict(B=2, H=2, Nq=1, L=300, dk=64, dv=64, dt=1, causal=1, cl=FAKE, Q=FAKE, ws=FAKE,
+                 ws_bytes=1 << 20)
+        a.update(kw)
+        return lib.mha_sdpa_decode_fwd(a["B"], a["H"], a["Nq"], a["L"], a["dk"], a["dv"], a["dt"],
+                                       a["causal"], a["cl"], 0.0, a["Q"], FAKE, FAKE, FAKE, None,
+                                       a["ws"], a["ws_bytes"], None)
+
+    assert dec(B=0) == C.MHA_ERR_INVALID
+    assert dec(causal=2) == C.MHA_ERR_INVALID
+    assert dec(Nq=301) == C.MHA_ERR_INVALID            # more queries than cache slots
+    assert dec(cl=None) == C.MHA_ERR_INVALID
+    assert dec(Nq=17) == C.MHA_ERR_UNSUPPORTED
+    assert dec(dk=32) == C.MHA_ERR_UNSUPPORTED
+    assert dec(ws=None) == C.MHA_ERR_WORKSPACE
+    assert dec(ws_bytes=64) == C.MHA_ERR_WORKSPACE
+    assert dec(Q=ODD) == C.MHA_ERR_ALIGN
+    assert dec(cl=ctypes.c_void_p(0x10002)) == C.MHA_ERR_ALIGN

@@ -12,6 +12,7 @@ from ._capi import (  # noqa: F401
     status_string,
 )
 from .api import (  # noqa: F401
+    decode_workspace_size,
     device_status,
     encoder_layer,
     encoder_layer_workspace_size,
@@ -22,5 +23,6 @@ from .api import (  # noqa: F401
     mha_layer,
     residual_layernorm,
     sdpa,
+    sdpa_decode,
     wait_selftest,
 )

@@ -24,6 +24,9 @@ _i64, _size = ctypes.c_int64, ctypes.c_size_t
 PROTOTYPES = {
     "mha_sdpa_fwd": (_c_int, [_c_int] * 8 + [_vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mha_sdpa_window_fwd": (_c_int, [_c_int] * 7 + [_c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mha_decode_workspace_size": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_size)]),
+    "mha_sdpa_decode_fwd": (_c_int, [_c_int] * 8 + [_vp, _c_float] + [_vp] * 5
+                            + [_vp, _size, _vp]),
     "mha_layer_workspace_size": (_c_int, [_c_int] * 8 + [ctypes.POINTER(_size)]),
     "mha_layer_fwd": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10 + [_size, _vp]),
     "mha_layer_fwd_timed": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10

@@ -75,6 +75,43 @@ def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None, window=None):
     return out
 
 
+def decode_workspace_size(B, H, Nq, Lmax, dtype) -> int:
+    n = ctypes.c_size_t(0)
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    C.check(C.load().mha_decode_workspace_size(B, H, Nq, Lmax, dt, ctypes.byref(n)),
+            "mha_decode_workspace_size")
+    return n.value
+
+
+def sdpa_decode(q, k_cache, v_cache, cache_len, causal=True, scale=None, workspace=None,
+                out=None):
+    """One generation step against a key/value cache via ``mha_sdpa_decode_fwd``.
+
+    q [B,H,Nq,d] (the new positions), k_cache / v_cache [B,H,Lmax,d] (any strides the kernel
+    accepts), cache_len int32 CUDA tensor [B] (valid positions, the new ones included).
+    causal: the queries are the newest Nq of the cached positions (bottom-right causal mask);
+    otherwise every cached position j < cache_len is attended (cross-attention to Z).
+    """
+    _cuda(q, k_cache, v_cache, cache_len, workspace, out)
+    B, H, Nq, d_k = q.shape
+    Lmax, d_v = k_cache.shape[2], v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, d_v), dtype=q.dtype, device=q.device)
+    ws = decode_workspace_size(B, H, Nq, Lmax, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=q.device)
+    strides = (ctypes.c_int64 * 16)(*(list(q.stride()) + list(k_cache.stride())
+                                      + list(v_cache.stride()) + list(out.stride())))
+    with torch.cuda.device(q.device):
+        code = C.load().mha_sdpa_decode_fwd(
+            B, H, Nq, Lmax, d_k, d_v, _dt(q), 1 if causal else 0, _ptr(cache_len),
+            float(scale or 0.0), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+            ctypes.cast(strides, ctypes.c_void_p), _ptr(workspace), workspace.numel(),
+            _stream(q.device))
+    C.check(code, "mha_sdpa_decode_fwd")
+    return out
+
+
 def layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype) -> int:
     n = ctypes.c_size_t(0)
     dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)

@@ -353,6 +353,94 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
                     stream);
 }
 
+int mha_decode_workspace_size(int B, int H, int Nq, int Lmax, int dtype, size_t* bytes) {
+  if (bytes == nullptr || B < 1 || H < 1 || Nq < 1 || Lmax < 1 || !valid_dtype(dtype))
+    return MHA_ERR_INVALID;
+  if (dtype == MHA_BF16 && Nq > mha::kDecodeMaxQ) return MHA_ERR_UNSUPPORTED;
+  // bf16: one fp32 partial (64 columns, max, sum) per (batch, head, 256-key chunk, query);
+  // the fp32 path needs none (at least 256 bytes are asked for so a buffer always exists)
+  const size_t parts = static_cast<size_t>(B) * H * mha::decode_num_splits(Lmax) * Nq;
+  *bytes = dtype == MHA_BF16 ? round_up(parts * 66 * sizeof(float), 256) : 256;
+  return MHA_OK;
+}
+
+int mha_sdpa_decode_fwd(int B, int H, int Nq, int Lmax, int d_k, int d_v, int dtype, int causal,
+                        const int32_t* cache_len, float scale, const void* Q, const void* K,
+                        const void* V, void* O, const int64_t* strides, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+  if (B < 1 || H < 1 || Nq < 1 || Lmax < 1 || d_k < 1 || d_v < 1 || !valid_dtype(dtype))
+    return MHA_ERR_INVALID;
+  if ((causal != 0 && causal != 1) || Nq > Lmax) return MHA_ERR_INVALID;
+  if (cache_len == nullptr || Q == nullptr || K == nullptr || V == nullptr || O == nullptr)
+    return MHA_ERR_INVALID;
+  if (std::isnan(scale) || std::isinf(scale)) return MHA_ERR_INVALID;
+  if (!aligned(cache_len, 4)) return MHA_ERR_ALIGN;
+  if (B > 65535 || H > 65535) return MHA_ERR_UNSUPPORTED;
+  size_t need = 0;
+  int st = mha_decode_workspace_size(B, H, Nq, Lmax, dtype, &need);
+  if (st != MHA_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return MHA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  const int64_t cont[4][4] = {
+      {static_cast<int64_t>(H) * Nq * d_k, static_cast<int64_t>(Nq) * d_k, d_k, 1},
+      {static_cast<int64_t>(H) * Lmax * d_k, static_cast<int64_t>(Lmax) * d_k, d_k, 1},
+      {static_cast<int64_t>(H) * Lmax * d_v, static_cast<int64_t>(Lmax) * d_v, d_v, 1},
+      {static_cast<int64_t>(H) * Nq * d_v, static_cast<int64_t>(Nq) * d_v, d_v, 1}};
+  int64_t str[4][4];
+  for (int t = 0; t < 4; ++t)
+    for (int i = 0; i < 4; ++i) {
+      str[t][i] = strides ? strides[4 * t + i] : cont[t][i];
+      if (str[t][i] < 0) return MHA_ERR_INVALID;
+    }
+  const void* ptrs[4] = {Q, K, V, O};
+  const float sc =
+      scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+  if (dtype == MHA_BF16) {
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    for (int t = 0; t < 4; ++t) {
+      if (str[t][3] != 1) return MHA_ERR_UNSUPPORTED;
+      for (int i = 0; i < 3; ++i)
+        if (str[t][i] == 0 || str[t][i] % 8 != 0) return MHA_ERR_ALIGN;
+      if (!aligned(ptrs[t], 16)) return MHA_ERR_ALIGN;
+    }
+    DevCtx ctx;
+    st = device_ctx(&ctx);
+    if (st != MHA_OK) return st;
+    CUtensorMap tk, tv;
+    if (!map_bhnd_bf16(&tk, K, B, H, Lmax, str[1]) || !map_bhnd_bf16(&tv, V, B, H, Lmax, str[2]))
+      return MHA_ERR_CUDA;
+    mha::DecodeArgs a;
+    a.B = B; a.H = H; a.Nq = Nq; a.Lmax = Lmax; a.causal = causal;
+    a.cache_len = cache_len;
+    a.scale = sc;
+    a.Q = Q; a.O = O;
+    for (int i = 0; i < 4; ++i) {
+      a.sq[i] = str[0][i];
+      a.so[i] = str[3][i];
+    }
+    cudaError_t e = mha::launch_sdpa_decode_bf16(tk, tv, a, static_cast<float*>(workspace), ctx,
+                                                 stream);
+    return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
+  // fp32: the SIMT attention kernel with the cache's masks (one warp per query row)
+  if (d_k > 128 || d_v > 128) return MHA_ERR_UNSUPPORTED;
+  for (int t = 0; t < 4; ++t)
+    if (!aligned(ptrs[t], 4)) return MHA_ERR_ALIGN;
+  DevCtx ctx;
+  st = device_ctx(&ctx);
+  if (st != MHA_OK) return st;
+  mha::SdpaArgs a;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nk = Lmax; a.d_k = d_k; a.d_v = d_v;
+  a.mask = causal ? mha::kMaskCausalCache : MHA_MASK_KEY_PADDING;
+  a.key_len = cache_len;
+  a.scale = sc;
+  a.Q = Q; a.K = K; a.V = V; a.O = O;
+  int64_t* dst[4] = {a.sq, a.sk, a.sv, a.so};
+  for (int t = 0; t < 4; ++t)
+    for (int i = 0; i < 4; ++i) dst[t][i] = str[t][i];
+  return run_sdpa(a, dtype, ctx, stream);
+}
+
 int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
                         float scale, const void* Q, const void* K, const void* V, void* O,
                         const int64_t* strides, cudaStream_t stream) {

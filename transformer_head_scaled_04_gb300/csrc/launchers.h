@@ -27,8 +27,10 @@ cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const f
 
 // ---- attention
 // Mask kinds beyond the public mha_mask values: restricted self-attention, where query i
-// attends keys j with |i - j| <= SdpaArgs::window.
+// attends keys j with |i - j| <= SdpaArgs::window; decoding against a cache of
+// L = key_len[b] positions, where query i (one of the Nq newest) attends j <= L - Nq + i.
 constexpr int kMaskWindow = 3;
+constexpr int kMaskCausalCache = 4;
 
 struct SdpaArgs {
   int B, H, Nq, Nk, d_k, d_v;
@@ -47,6 +49,24 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, const SdpaArgs& a, const DevCtx& ctx,
                              cudaStream_t s);
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s);
+
+// ---- one generation step against a key/value cache (split-K over the cached keys)
+constexpr int kDecodeMaxQ = 16;  // new query rows per call on the bf16 path
+struct DecodeArgs {
+  int B, H, Nq, Lmax;
+  int causal;                // 1: query i attends keys j <= L - Nq + i; 0: every j < L
+  const int32_t* cache_len;  // device, B entries: L (clamped to [0, Lmax] on the device)
+  float scale;
+  const void* Q;             // [B, H, Nq, 64] with element strides sq (d stride 1)
+  void* O;                   // [B, H, Nq, 64] with element strides so
+  int64_t sq[4], so[4];
+};
+int decode_num_splits(int Lmax);  // 256-key chunks per (batch, head)
+// bf16: the caches through 4-D TMA maps {64, Lmax, H, B}, box {64, 128, 1, 1}; part: fp32
+// scratch of B * H * decode_num_splits(Lmax) * Nq * 66 floats.
+cudaError_t launch_sdpa_decode_bf16(const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                    const DecodeArgs& a, float* part, const DevCtx& ctx,
+                                    cudaStream_t s);
 
 // ---- residual + LayerNorm: y = LN(x + a) * gamma + beta
 cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,

@@ -1,7 +1,8 @@
 // sdpa_f32.cu -- fp32 scaled dot-product attention (SIMT, no tensor cores, no TF32).
 //
-//   O = softmax(Q K^T * scale) V per (batch, head), optional causal / key-padding mask, or
-//   the neighbourhood |i - j| <= window of restricted self-attention
+//   O = softmax(Q K^T * scale) V per (batch, head), optional causal / key-padding mask, the
+//   neighbourhood |i - j| <= window of restricted self-attention, or a generation step's
+//   bottom-right causal mask over a key/value cache
 //   ("Attention Is All You Need", lettle.cn translation, 3.2.1 缩放点积注意力;
 //    "Transformer：抛弃循环与卷积的序列建模", Self-Attention的优势).
 //
@@ -48,6 +49,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   } else if (mask == kMaskWindow) {
     limit = min(row + window, Nk - 1);
     first = max(row - window, 0);
+  } else if (mask == kMaskCausalCache) {
+    // the Nq queries are the newest of L cached positions: row sits at L - Nq + row
+    const int L = min(max(key_len[b], 0), Nk);
+    limit = min(L - Nq + row, L - 1);
   } else {
     limit = Nk - 1;
   }
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  const float inv = (nkeys > first && l > 0.f) ? 1.f / l : 0.f;
+  const float inv = (nkeys > first && l > 0.f) ? 1.f / l : 0.f;  // no allowed key: zeros
   float* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
 #pragma unroll
   for (int t = 0; t < kMaxD; ++t) {
