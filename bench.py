@@ -38,6 +38,7 @@ METRIC = "SDPA/MHA fwd TFLOP/s & % of GB300 bf16 tensor peak; MHA-layer tokens/s
 WORKLOAD = "big_long_b8_n4096"
 FFN_WORKLOAD = "ffn_big_b8_n4096"
 WINDOW = 256
+DECODE_B, DECODE_L = 64, 4096
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -107,6 +108,55 @@ def measure_window(lib, C, dev, stream, flush, steps, warmup, peak, window=WINDO
         "value": tf, "unit": "TFLOP/s (allowed pairs only)", "ms": t,
         "flops_per_launch": fl, "frac_of_peak": tf / peak,
         "speedup_vs_full_attention_time": None,
+    }
+
+
+def measure_decode(lib, C, dev, stream, flush, steps, warmup, hbm_peak, B=DECODE_B, Nq=1,
+                   L=DECODE_L):
+    """One generation step (Nq new queries per sequence) of the big model's heads against full
+    key/value caches of L positions for B sequences: bound by reading the caches from HBM."""
+    import torch
+
+    w = si.WORKLOADS[WORKLOAD]
+    H = w.H
+    g = torch.Generator(device=dev).manual_seed(20260011)
+    q = torch.randn(B, H, Nq, 64, device=dev, generator=g).to(torch.bfloat16)
+    kc = torch.randn(B, H, L, 64, device=dev, generator=g).to(torch.bfloat16)
+    vc = torch.randn(B, H, L, 64, device=dev, generator=g).to(torch.bfloat16)
+    cl = torch.full((B,), L, dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    n = ctypes.c_size_t(0)
+    C.check(lib.mha_decode_workspace_size(B, H, Nq, L, C.MHA_BF16, ctypes.byref(n)), "dec ws")
+    ws = torch.empty(n.value, dtype=torch.uint8, device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    args = (B, H, Nq, L, 64, 64, C.MHA_BF16, 1, vp(cl), 0.0, vp(q), vp(kc), vp(vc), vp(o), None,
+            vp(ws), n.value, sp)
+    for _ in range(warmup):
+        flush.zero_()
+        C.check(lib.mha_sdpa_decode_fwd(*args), "mha_sdpa_decode_fwd")
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        C.check(lib.mha_sdpa_decode_fwd(*args), "mha_sdpa_decode_fwd")
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    t = float(np.mean(ms))
+    cache_bytes = 2 * B * H * L * 64 * 2               # K and V caches read once
+    algo_bytes = cache_bytes + 2 * B * H * Nq * 64 * 2  # plus Q read and O written
+    gbs = algo_bytes / (t * 1e-3) / 1e9
+    return {
+        "workload": f"generation step: B={B} sequences, h={H}, Nq={Nq} new query per sequence, "
+                    f"{L} cached positions each (full caches), causal",
+        "value": B * Nq / (t * 1e-3), "unit": "new tokens/s (one layer's attention)",
+        "ms": t, "launches_per_step": 2,
+        "roofline": {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
+                     "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "algorithmic_bytes_per_step": algo_bytes},
     }
 
 
@@ -544,6 +594,8 @@ def run_ours(args):
     ffn = measure_ffn(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
     window = measure_window(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
     window["speedup_vs_full_attention_time"] = sdpa_ms / window["ms"]
+    decode = measure_decode(lib, C, dev, stream, flush, args.steps, args.warmup,
+                            float(peaks["hbm_gbs"]))
     encoder = measure_encoder(lib, C, dev, stream, flush, max(3, args.steps // 2), args.warmup)
 
     # end to end through the public API: pinned host x -> device, sublayer, y -> pinned host
@@ -608,6 +660,7 @@ def run_ours(args):
         "ffn": ffn,
         "encoder_layer": encoder,
         "window": window,
+        "decode": decode,
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, w, "none")

@@ -37,15 +37,19 @@ constexpr int kBoxBytes = kBox * kD * 2;  // 16 KB
 constexpr int kErrTimeout = -6;
 constexpr int kSiteDecode = 31;
 
-// shared memory: K chunk, V chunk (1024-aligned for the swizzle), Q, scores, partial O
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + 2 * kBoxBytes;
-constexpr int kOffQ = kOffV + 2 * kBoxBytes;                   // float [16][64]
-constexpr int kOffS = kOffQ + kDecodeMaxQ * kD * 4;            // float [16][256]
-constexpr int kOffO = kOffS + kDecodeMaxQ * kChunk * 4;        // float [warps][16][64]
-constexpr int kOffStat = kOffO + kWarps * kDecodeMaxQ * kD * 4;  // float [16][2]
-constexpr int kOffBar = kOffStat + kDecodeMaxQ * 2 * 4;
-constexpr int kSmemBytes = 1024 + kOffBar + 64;
+// shared memory for NQ query rows: K chunk, V chunk (1024-aligned for the swizzle), Q,
+// scores, the warps' partial O, per-query max and sum, the TMA barrier
+template <int NQ>
+struct DecodeSmem {
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + 2 * kBoxBytes;
+  static constexpr int kOffQ = kOffV + 2 * kBoxBytes;         // float [NQ][64]
+  static constexpr int kOffS = kOffQ + NQ * kD * 4;           // float [NQ][256]
+  static constexpr int kOffO = kOffS + NQ * kChunk * 4;       // float [warps][NQ][64]
+  static constexpr int kOffStat = kOffO + kWarps * NQ * kD * 4;  // float [NQ][2]
+  static constexpr int kOffBar = kOffStat + NQ * 2 * 4;
+  static constexpr int kBytes = 1024 + kOffBar + 64;  // two barriers: K landed, V landed
+};
 
 struct DecodeParams {
   int H, Nq, Lmax, causal, n_split;
@@ -61,9 +65,14 @@ struct DecodeParams {
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// NQ: compile-time bound on the query rows (1, 2, 4, 8 or 16); p.Nq <= NQ
+template <int NQ>
 __global__ void __launch_bounds__(kThreads)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+  using Sm = DecodeSmem<NQ>;
+  constexpr int kOffK = Sm::kOffK, kOffV = Sm::kOffV, kOffQ = Sm::kOffQ, kOffS = Sm::kOffS,
+                kOffO = Sm::kOffO, kOffStat = Sm::kOffStat, kOffBar = Sm::kOffBar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -90,49 +99,54 @@ __global__ void __launch_bounds__(kThreads)
   const int nk = min(kChunk, L - k0);  // cached keys in this chunk
   const int nbox = (nk + kBox - 1) / kBox;
 
+  const uint32_t barK = smem_u32(bar), barV = smem_u32(bar + 1);
   if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
+    mbar_init(barK, 1);
+    mbar_init(barV, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0) {  // K first: the scores start while V is still on its way
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
-    mbar_arrive_expect_tx(smem_u32(bar), 2 * nbox * kBoxBytes);
-    for (int x = 0; x < nbox; ++x) {
-      tma_load_4d(smem_u32(smem + kOffK + x * kBoxBytes), &tmK, smem_u32(bar), 0,
-                  k0 + x * kBox, h, b);
-      tma_load_4d(smem_u32(smem + kOffV + x * kBoxBytes), &tmV, smem_u32(bar), 0,
-                  k0 + x * kBox, h, b);
-    }
+    mbar_arrive_expect_tx(barK, nbox * kBoxBytes);
+    for (int x = 0; x < nbox; ++x)
+      tma_load_4d(smem_u32(smem + kOffK + x * kBoxBytes), &tmK, barK, 0, k0 + x * kBox, h, b);
+    mbar_arrive_expect_tx(barV, nbox * kBoxBytes);
+    for (int x = 0; x < nbox; ++x)
+      tma_load_4d(smem_u32(smem + kOffV + x * kBoxBytes), &tmV, barV, 0, k0 + x * kBox, h, b);
   }
   // queries to shared memory as fp32 while the cache chunk is in flight
   const __nv_bfloat16* qb = p.Q + b * p.sq_b + h * p.sq_h;
   for (int i = tid; i < Nq * kD; i += kThreads)
     sQ[i] = __bfloat162float(qb[(i / kD) * p.sq_n + (i % kD)]);
-  if (!mbar_wait(smem_u32(bar), 0, p.timeout_ns)) {
+  // a timed-out wait records the error, lets the copies land (bounded) and leaves
+  auto give_up = [&]() {
     if (tid == 0) record_error(p.status, kErrTimeout, kSiteDecode);
-    // the copies may still land: wait for them once more before the CTA may exit
-    (void)mbar_wait(smem_u32(bar), 0, p.timeout_ns);
+    (void)mbar_wait(barK, 0, p.timeout_ns);
+    (void)mbar_wait(barV, 0, p.timeout_ns);
+  };
+  // every thread waits (bounded); the block gives up together if any wait ran out
+  if (!__syncthreads_and(mbar_wait(barK, 0, p.timeout_ns))) {
+    give_up();
     return;
   }
-  __syncthreads();
 
   // ---- scores: thread t takes keys t and t + 128 of the chunk
   for (int kk = tid; kk < kChunk; kk += kThreads) {
     const int key = k0 + kk;
-    float s[kDecodeMaxQ];
+    float s[NQ];
     if (kk < nk) {
       const uint8_t* row = smem + kOffK + kk * 128;  // box rows are consecutive 128-byte rows
 #pragma unroll
-      for (int q = 0; q < kDecodeMaxQ; ++q) s[q] = 0.f;
+      for (int q = 0; q < NQ; ++q) s[q] = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of row kk sits at chunk c ^ (kk & 7)
         const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (kk & 7)) << 4));
         const float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
                              bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
 #pragma unroll
-        for (int q = 0; q < kDecodeMaxQ; ++q) {
+        for (int q = 0; q < NQ; ++q) {
           if (q < Nq) {
             const float* qr = sQ + q * kD + c * 8;
 #pragma unroll
@@ -142,7 +156,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
 #pragma unroll
-    for (int q = 0; q < kDecodeMaxQ; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       if (q < Nq) {
         const bool ok = kk < nk && (!p.causal || key <= L - Nq + q);
         sS[q * kChunk + kk] = ok ? s[q] : -INFINITY;
@@ -173,12 +187,15 @@ __global__ void __launch_bounds__(kThreads)
       sStat[2 * q + 1] = l;
     }
   }
-  __syncthreads();
+  if (!__syncthreads_and(mbar_wait(barV, 0, p.timeout_ns))) {
+    give_up();
+    return;
+  }
 
   // ---- unnormalised O: warp w sums keys [64 w, 64 w + 64), lane owns columns 2 lane, 2 lane + 1
-  float acc[kDecodeMaxQ][2];
+  float acc[NQ][2];
 #pragma unroll
-  for (int q = 0; q < kDecodeMaxQ; ++q) acc[q][0] = acc[q][1] = 0.f;
+  for (int q = 0; q < NQ; ++q) acc[q][0] = acc[q][1] = 0.f;
   const int kend = min(kChunk / kWarps * (warp + 1), nk);
   for (int kk = kChunk / kWarps * warp; kk < kend; ++kk) {
     const uint8_t* row = smem + kOffV + kk * 128;
@@ -187,7 +204,7 @@ __global__ void __launch_bounds__(kThreads)
         row + ((((lane >> 2) ^ (kk & 7)) << 4) | ((lane & 3) << 2)));
     const float v0 = bf16_lo(u), v1 = bf16_hi(u);
 #pragma unroll
-    for (int q = 0; q < kDecodeMaxQ; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       if (q < Nq) {
         const float pq = sS[q * kChunk + kk];
         acc[q][0] = fmaf(pq, v0, acc[q][0]);
@@ -196,10 +213,10 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
 #pragma unroll
-  for (int q = 0; q < kDecodeMaxQ; ++q) {
+  for (int q = 0; q < NQ; ++q) {
     if (q < Nq) {
-      sO[(warp * kDecodeMaxQ + q) * kD + 2 * lane] = acc[q][0];
-      sO[(warp * kDecodeMaxQ + q) * kD + 2 * lane + 1] = acc[q][1];
+      sO[(warp * NQ + q) * kD + 2 * lane] = acc[q][0];
+      sO[(warp * NQ + q) * kD + 2 * lane + 1] = acc[q][1];
     }
   }
   __syncthreads();
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(kThreads)
     const int q = i / kD, d = i % kD;
     float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) o += sO[(w * kDecodeMaxQ + q) * kD + d];
+    for (int w = 0; w < kWarps; ++w) o += sO[(w * NQ + q) * kD + d];
     out[q * (kD + 2) + d] = o;
   }
   if (tid < Nq) {
@@ -243,6 +260,18 @@ __global__ void __launch_bounds__(kDecodeMaxQ * kD)
   O[b * so_b + h * so_h + q * so_n + d] = __float2bfloat16_rn(y);
 }
 
+template <int NQ>
+cudaError_t launch_partial(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                           dim3 grid, cudaStream_t s) {
+  static_assert(NQ <= kDecodeMaxQ, "query rows beyond the decode limit");
+  auto kern = decode_partial_kernel<NQ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       DecodeSmem<NQ>::kBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, DecodeSmem<NQ>::kBytes, s>>>(tmK, tmV, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int decode_num_splits(int Lmax) { return (Lmax + kChunk - 1) / kChunk; }
@@ -265,11 +294,18 @@ cudaError_t launch_sdpa_decode_bf16(const CUtensorMap& tmK, const CUtensorMap& t
   p.part = part;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
-  cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  decode_partial_kernel<<<dim3(p.n_split, a.H, a.B), kThreads, kSmemBytes, s>>>(tmK, tmV, p);
-  e = cudaGetLastError();
+  const dim3 grid(p.n_split, a.H, a.B);
+  cudaError_t e;
+  if (a.Nq <= 1)
+    e = launch_partial<1>(tmK, tmV, p, grid, s);
+  else if (a.Nq <= 2)
+    e = launch_partial<2>(tmK, tmV, p, grid, s);
+  else if (a.Nq <= 4)
+    e = launch_partial<4>(tmK, tmV, p, grid, s);
+  else if (a.Nq <= 8)
+    e = launch_partial<8>(tmK, tmV, p, grid, s);
+  else
+    e = launch_partial<16>(tmK, tmV, p, grid, s);
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<dim3(a.H, a.B), kDecodeMaxQ * kD, 0, s>>>(
       part, a.H, a.Nq, p.n_split, a.scale, static_cast<__nv_bfloat16*>(a.O), a.so[0], a.so[1],
