@@ -7,8 +7,8 @@ path (the CUDA library and its Python binding) never calls it and shares no code
 with it.
 
 Every function computes in float64 with NumPy, following the definitions on the
-pages one step at a time.  See ``oracle.mha_ref`` and ``oracle.ffn`` for the
-citations.
+pages one step at a time (the backward: the chain rule through those steps).  See
+``oracle.mha_ref``, ``oracle.ffn`` and ``oracle.backward`` for the citations.
 """
 from .mha_ref import (  # noqa: F401
     allowed_keys,
@@ -24,4 +24,11 @@ from .ffn import (  # noqa: F401
     ffn_ref,
     ffn_layer_ref,
     encoder_layer_ref,
+)
+from .backward import (  # noqa: F401
+    layernorm_bwd_ref,
+    attention_bwd_ref,
+    sdpa_bwd_ref,
+    sdpa_lse_ref,
+    mha_layer_bwd_ref,
 )
