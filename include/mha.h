@@ -85,6 +85,46 @@ int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
                  const int64_t* strides, cudaStream_t stream);
 
 /*
+ * mha_sdpa_fwd_lse -- mha_sdpa_fwd that also writes, for every query row, the natural log of
+ * its softmax denominator: lse[b,h,i] = log sum_j exp(Q[b,h,i] . K[b,h,j] * scale) over the
+ * allowed keys (+inf for a row with none), fp32 [B, H, Nq] contiguous, 4-byte aligned.  The
+ * backward pass (mha_sdpa_bwd) rebuilds the softmax weights as exp(s - lse) from it.
+ * Same arguments, limits and errors as mha_sdpa_fwd; MHA_ERR_INVALID if lse is NULL.
+ */
+int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                     const int32_t* key_len, float scale, const void* Q, const void* K,
+                     const void* V, void* O, const int64_t* strides, float* lse,
+                     cudaStream_t stream);
+
+/*
+ * mha_sdpa_bwd_workspace_size -- bytes of device workspace mha_sdpa_bwd needs (one fp32 per
+ * query row: D_i = sum_d dO_id O_id).
+ */
+int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes);
+
+/*
+ * mha_sdpa_bwd -- backward of scaled dot-product attention ([JY] Transformer 训练样例 >
+ * 反向传播: the chain rule through the forward's steps; [LT] 3.2.1 for the forward).  With the
+ * weights rebuilt from the forward's log-sum-exp, P_ij = exp(Q_i . K_j * scale - lse_i)
+ * (0 for excluded keys), and D_i = sum_d dO_id O_id:
+ *     dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale * dS K,  dK = scale * dS^T Q
+ *   Q, O, dO, dQ [B,H,Nq,d]; K, V, dK, dV [B,H,Nk,d]; lse [B,H,Nq] fp32 from
+ *   mha_sdpa_fwd_lse (same Q, K, mask and scale); O is that call's output.  mask, key_len,
+ *   scale as for mha_sdpa_fwd (none / causal / key padding).  dQ, dK, dV are written
+ *   (keys no query may see get zero gradients); they may not alias the inputs.
+ *   strides: NULL for contiguous, or 32 element strides {Q, K, V, O, dO, dQ, dK, dV} x
+ *   {b, h, n, d} (d stride 1).  workspace: mha_sdpa_bwd_workspace_size() bytes, 256-byte
+ *   aligned.  dtype MHA_BF16: d_k == d_v == 64, other strides multiples of 8, 16-byte aligned
+ *   pointers; tensor-core kernels (one CTA per 128 query rows for dQ, one per 128 keys for
+ *   dK and dV; no atomics).  dtype MHA_F32: d <= 128, SIMT kernels.
+ */
+int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                 const int32_t* key_len, float scale, const void* Q, const void* K,
+                 const void* V, const void* O, const void* dO, const float* lse, void* dQ,
+                 void* dK, void* dV, const int64_t* strides, void* workspace, size_t ws_bytes,
+                 cudaStream_t stream);
+
+/*
  * mha_sdpa_window_fwd -- restricted self-attention ([JY] Self-Attention的优势, 总结): every
  * position attends only the neighbourhood of size r = 2*window + 1 centred on it,
  *     O[b,h,i] = softmax_j(Q[b,h,i] . K[b,h,j] * scale, |i - j| <= window) V[b,h,j]

@@ -277,3 +277,35 @@ def test_decode_workspace_and_validation(lib):
     assert dec(ws_bytes=64) == C.MHA_ERR_WORKSPACE
     assert dec(Q=ODD) == C.MHA_ERR_ALIGN
     assert dec(cl=ctypes.c_void_p(0x10002)) == C.MHA_ERR_ALIGN
+
+
+def test_sdpa_backward_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_sdpa_bwd_workspace_size(8, 16, 4096, 1, ctypes.byref(n)) == 0
+    assert n.value == 8 * 16 * 4096 * 4
+    assert lib.mha_sdpa_bwd_workspace_size(0, 16, 4096, 1, ctypes.byref(n)) == C.MHA_ERR_INVALID
+
+    def bwd(**kw):
+        a = dict(B=1, H=2, Nq=200, Nk=200, dk=64, dv=64, dt=1, mask=0, kl=None, lse=FAKE,
+                 dQ=FAKE, ws=FAKE, ws_bytes=1 << 20)
+        a.update(kw)
+        return lib.mha_sdpa_bwd(a["B"], a["H"], a["Nq"], a["Nk"], a["dk"], a["dv"], a["dt"],
+                                a["mask"], a["kl"], 0.0, FAKE, FAKE, FAKE, FAKE, FAKE, a["lse"],
+                                a["dQ"], FAKE, FAKE, None, a["ws"], a["ws_bytes"], None)
+
+    assert bwd(B=0) == C.MHA_ERR_INVALID
+    assert bwd(mask=3) == C.MHA_ERR_INVALID
+    assert bwd(mask=1, Nk=300) == C.MHA_ERR_INVALID     # causal needs Nq == Nk
+    assert bwd(mask=2) == C.MHA_ERR_INVALID             # key padding needs key_len
+    assert bwd(lse=None) == C.MHA_ERR_INVALID
+    assert bwd(dQ=None) == C.MHA_ERR_INVALID
+    assert bwd(dk=32) == C.MHA_ERR_UNSUPPORTED
+    assert bwd(ws=None) == C.MHA_ERR_WORKSPACE
+    assert bwd(ws_bytes=16) == C.MHA_ERR_WORKSPACE
+    assert bwd(dQ=ODD) == C.MHA_ERR_ALIGN
+    assert bwd(lse=ctypes.c_void_p(0x10002)) == C.MHA_ERR_ALIGN
+    f = lib.mha_sdpa_fwd_lse
+    assert f(1, 1, 8, 8, 64, 64, 1, 0, None, 0.0, FAKE, FAKE, FAKE, FAKE, None, None, None) == \
+        C.MHA_ERR_INVALID
+    assert f(1, 1, 8, 8, 64, 64, 1, 0, None, 0.0, FAKE, FAKE, FAKE, FAKE, None,
+             ctypes.c_void_p(0x10002), None) == C.MHA_ERR_ALIGN

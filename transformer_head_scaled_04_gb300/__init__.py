@@ -23,6 +23,8 @@ from .api import (  # noqa: F401
     mha_layer,
     residual_layernorm,
     sdpa,
+    sdpa_backward,
     sdpa_decode,
+    sdpa_with_lse,
     wait_selftest,
 )

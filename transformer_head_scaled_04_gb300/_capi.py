@@ -23,6 +23,9 @@ _i64, _size = ctypes.c_int64, ctypes.c_size_t
 
 PROTOTYPES = {
     "mha_sdpa_fwd": (_c_int, [_c_int] * 8 + [_vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mha_sdpa_fwd_lse": (_c_int, [_c_int] * 8 + [_vp, _c_float, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "mha_sdpa_bwd_workspace_size": (_c_int, [_c_int] * 4 + [ctypes.POINTER(_size)]),
+    "mha_sdpa_bwd": (_c_int, [_c_int] * 8 + [_vp, _c_float] + [_vp] * 9 + [_vp, _vp, _size, _vp]),
     "mha_sdpa_window_fwd": (_c_int, [_c_int] * 7 + [_c_float, _vp, _vp, _vp, _vp, _vp, _vp]),
     "mha_decode_workspace_size": (_c_int, [_c_int] * 5 + [ctypes.POINTER(_size)]),
     "mha_sdpa_decode_fwd": (_c_int, [_c_int] * 8 + [_vp, _c_float] + [_vp] * 5

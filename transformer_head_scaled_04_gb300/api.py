@@ -75,6 +75,52 @@ def sdpa(q, k, v, mask="none", key_len=None, scale=None, out=None, window=None):
     return out
 
 
+def _strides(*ts):
+    return (ctypes.c_int64 * (4 * len(ts)))(*[x for t in ts for x in t.stride()])
+
+
+def sdpa_with_lse(q, k, v, mask="none", key_len=None, scale=None, out=None):
+    """``sdpa`` via ``mha_sdpa_fwd_lse``: returns (O, lse) with lse [B,H,Nq] fp32, the natural
+    log of each row's softmax denominator (what ``sdpa_backward`` needs)."""
+    _cuda(q, k, v, key_len, out)
+    B, H, Nq, d_k = q.shape
+    Nk, d_v = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, d_v), dtype=q.dtype, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        code = C.load().mha_sdpa_fwd_lse(
+            B, H, Nq, Nk, d_k, d_v, _dt(q), _mask(mask), _ptr(key_len), float(scale or 0.0),
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), ctypes.cast(_strides(q, k, v, out),
+                                                              ctypes.c_void_p),
+            _ptr(lse), _stream(q.device))
+    C.check(code, "mha_sdpa_fwd_lse")
+    return out, lse
+
+
+def sdpa_backward(q, k, v, o, do, lse, mask="none", key_len=None, scale=None, workspace=None):
+    """dQ, dK, dV of attention via ``mha_sdpa_bwd`` (o, lse from ``sdpa_with_lse``)."""
+    _cuda(q, k, v, o, do, lse, key_len, workspace)
+    B, H, Nq, d_k = q.shape
+    Nk, d_v = k.shape[2], v.shape[3]
+    dq = torch.empty((B, H, Nq, d_k), dtype=q.dtype, device=q.device)
+    dk = torch.empty((B, H, Nk, d_k), dtype=q.dtype, device=q.device)
+    dv = torch.empty((B, H, Nk, d_v), dtype=q.dtype, device=q.device)
+    n = ctypes.c_size_t(0)
+    C.check(C.load().mha_sdpa_bwd_workspace_size(B, H, Nq, _dt(q), ctypes.byref(n)),
+            "mha_sdpa_bwd_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(n.value, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        code = C.load().mha_sdpa_bwd(
+            B, H, Nq, Nk, d_k, d_v, _dt(q), _mask(mask), _ptr(key_len), float(scale or 0.0),
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+            _ptr(dv), ctypes.cast(_strides(q, k, v, o, do, dq, dk, dv), ctypes.c_void_p),
+            _ptr(workspace), workspace.numel(), _stream(q.device))
+    C.check(code, "mha_sdpa_bwd")
+    return dq, dk, dv
+
+
 def decode_workspace_size(B, H, Nq, Lmax, dtype) -> int:
     n = ctypes.c_size_t(0)
     dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)

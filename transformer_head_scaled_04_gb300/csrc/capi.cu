@@ -289,7 +289,8 @@ namespace {
 // mask: an mha_mask value or mha::kMaskWindow (then `window` is the neighbourhood radius)
 int sdpa_entry(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
                const int32_t* key_len, int window, float scale, const void* Q, const void* K,
-               const void* V, void* O, const int64_t* strides, cudaStream_t stream) {
+               const void* V, void* O, const int64_t* strides, cudaStream_t stream,
+               float* lse = nullptr) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d_k < 1 || d_v < 1) return MHA_ERR_INVALID;
   if (!valid_dtype(dtype) || mask < MHA_MASK_NONE ||
       (mask > MHA_MASK_KEY_PADDING && mask != mha::kMaskWindow))
@@ -310,6 +311,8 @@ int sdpa_entry(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int ma
   // a radius of Nk or more already reaches every key
   a.window = (mask == mha::kMaskWindow) ? (window < Nk ? window : Nk) : 0;
   a.Q = Q; a.K = K; a.V = V; a.O = O;
+  a.lse = lse;
+  if (lse != nullptr && !aligned(lse, 4)) return MHA_ERR_ALIGN;
   const int64_t cont[4][4] = {
       {static_cast<int64_t>(H) * Nq * d_k, static_cast<int64_t>(Nq) * d_k, d_k, 1},
       {static_cast<int64_t>(H) * Nk * d_k, static_cast<int64_t>(Nk) * d_k, d_k, 1},
@@ -439,6 +442,98 @@ int mha_sdpa_decode_fwd(int B, int H, int Nq, int Lmax, int d_k, int d_v, int dt
   for (int t = 0; t < 4; ++t)
     for (int i = 0; i < 4; ++i) dst[t][i] = str[t][i];
   return run_sdpa(a, dtype, ctx, stream);
+}
+
+int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                     const int32_t* key_len, float scale, const void* Q, const void* K,
+                     const void* V, void* O, const int64_t* strides, float* lse,
+                     cudaStream_t stream) {
+  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING || lse == nullptr)
+    return MHA_ERR_INVALID;
+  return sdpa_entry(B, H, Nq, Nk, d_k, d_v, dtype, mask, key_len, 0, scale, Q, K, V, O, strides,
+                    stream, lse);
+}
+
+int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes) {
+  if (bytes == nullptr || B < 1 || H < 1 || Nq < 1 || !valid_dtype(dtype))
+    return MHA_ERR_INVALID;
+  *bytes = round_up(static_cast<size_t>(B) * H * Nq * sizeof(float), 256);  // D = rowsum(dO O)
+  return MHA_OK;
+}
+
+int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
+                 const int32_t* key_len, float scale, const void* Q, const void* K,
+                 const void* V, const void* O, const void* dO, const float* lse, void* dQ,
+                 void* dK, void* dV, const int64_t* strides, void* workspace, size_t ws_bytes,
+                 cudaStream_t stream) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d_k < 1 || d_v < 1 || !valid_dtype(dtype))
+    return MHA_ERR_INVALID;
+  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
+  if (mask == MHA_MASK_CAUSAL && Nq != Nk) return MHA_ERR_INVALID;
+  if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
+  const void* ptrs[8] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (q == nullptr) return MHA_ERR_INVALID;
+  if (lse == nullptr || std::isnan(scale) || std::isinf(scale)) return MHA_ERR_INVALID;
+  if (!aligned(lse, 4) || (key_len != nullptr && !aligned(key_len, 4))) return MHA_ERR_ALIGN;
+  if (B > 65535 || H > 65535 || (Nq + 127) / 128 > 65535 || (Nk + 127) / 128 > 65535)
+    return MHA_ERR_UNSUPPORTED;
+  size_t need = 0;
+  int st = mha_sdpa_bwd_workspace_size(B, H, Nq, dtype, &need);
+  if (st != MHA_OK) return st;
+  if (workspace == nullptr || ws_bytes < need) return MHA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  mha::SdpaBwdArgs a;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nk = Nk; a.d_k = d_k; a.d_v = d_v;
+  a.mask = mask;
+  a.window = 0;
+  a.key_len = (mask == MHA_MASK_KEY_PADDING) ? key_len : nullptr;
+  a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+  a.Q = Q; a.K = K; a.V = V; a.O = O; a.dO = dO;
+  a.lse = lse;
+  a.Dv = static_cast<float*>(workspace);
+  a.dQ = dQ; a.dK = dK; a.dV = dV;
+  // contiguous [B, H, N, d] unless strides are given: Q, K, V, O, dO, dQ, dK, dV
+  const int rows[8] = {Nq, Nk, Nk, Nq, Nq, Nq, Nk, Nk};
+  const int dims[8] = {d_k, d_k, d_v, d_v, d_v, d_k, d_k, d_v};
+  for (int t = 0; t < 8; ++t) {
+    const int64_t cont[4] = {static_cast<int64_t>(H) * rows[t] * dims[t],
+                             static_cast<int64_t>(rows[t]) * dims[t], dims[t], 1};
+    for (int i = 0; i < 4; ++i) {
+      a.st[t][i] = strides ? strides[4 * t + i] : cont[i];
+      if (a.st[t][i] < 0) return MHA_ERR_INVALID;
+    }
+  }
+  if (dtype == MHA_BF16) {
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    for (int t = 0; t < 8; ++t) {
+      if (a.st[t][3] != 1) return MHA_ERR_UNSUPPORTED;
+      for (int i = 0; i < 3; ++i)
+        if (a.st[t][i] == 0 || a.st[t][i] % 8 != 0) return MHA_ERR_ALIGN;
+      if (!aligned(ptrs[t], 16)) return MHA_ERR_ALIGN;
+    }
+  } else {
+    if (d_k > 128 || d_v > 128) return MHA_ERR_UNSUPPORTED;
+    for (int t = 0; t < 8; ++t) {
+      if (a.st[t][3] != 1) return MHA_ERR_UNSUPPORTED;
+      if (!aligned(ptrs[t], 4)) return MHA_ERR_ALIGN;
+    }
+  }
+  DevCtx ctx;
+  st = device_ctx(&ctx);
+  if (st != MHA_OK) return st;
+  cudaError_t e = mha::launch_sdpa_bwd_rowdot(a, dtype, stream);
+  if (e != cudaSuccess) return MHA_ERR_CUDA;
+  if (dtype == MHA_BF16) {
+    CUtensorMap tq, tk, tv, tg;
+    if (!map_bhnd_bf16(&tq, Q, B, H, Nq, a.st[0]) || !map_bhnd_bf16(&tk, K, B, H, Nk, a.st[1]) ||
+        !map_bhnd_bf16(&tv, V, B, H, Nk, a.st[2]) || !map_bhnd_bf16(&tg, dO, B, H, Nq, a.st[4]))
+      return MHA_ERR_CUDA;
+    e = mha::launch_sdpa_bwd_bf16(tq, tk, tv, tg, a, ctx, stream);
+  } else {
+    e = mha::launch_sdpa_bwd_f32(a, stream);
+  }
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,

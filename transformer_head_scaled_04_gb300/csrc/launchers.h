@@ -43,6 +43,9 @@ struct SdpaArgs {
   const void* V;
   void* O;
   int64_t sq[4], sk[4], sv[4], so[4];  // element strides b, h, n, d
+  // optional: natural log of each row's softmax denominator, log sum_j exp(q.k_j * scale)
+  // over the allowed keys (+inf for a row with none), fp32 [B, H, Nq] contiguous
+  float* lse = nullptr;
 };
 // bf16: Q/K/V through 4-D TMA maps {d, n, h, b} with box {64, 128, 1, 1}, 128-byte swizzle.
 cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
@@ -67,6 +70,25 @@ int decode_num_splits(int Lmax);  // 256-key chunks per (batch, head)
 cudaError_t launch_sdpa_decode_bf16(const CUtensorMap& tmK, const CUtensorMap& tmV,
                                     const DecodeArgs& a, float* part, const DevCtx& ctx,
                                     cudaStream_t s);
+
+// ---- attention backward (dQ, dK, dV) from Q, K, V, O, dO and the forward's log-sum-exp
+struct SdpaBwdArgs {
+  int B, H, Nq, Nk, d_k, d_v;
+  int mask, window;          // as in SdpaArgs
+  const int32_t* key_len;
+  float scale;
+  const void *Q, *K, *V, *O, *dO;
+  const float* lse;          // [B, H, Nq] natural-log softmax denominators
+  float* Dv;                 // [B, H, Nq] scratch: rowsum(dO * O)
+  void *dQ, *dK, *dV;
+  int64_t st[8][4];          // element strides b, h, n, d of Q, K, V, O, dO, dQ, dK, dV
+};
+cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_sdpa_bwd_f32(const SdpaBwdArgs& a, cudaStream_t s);
+// bf16 (d = 64): Q, K, V, dO through 4-D TMA maps {64, n, h, b}, box {64, 128, 1, 1}
+cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmG,
+                                 const SdpaBwdArgs& a, const DevCtx& ctx, cudaStream_t s);
 
 // ---- residual + LayerNorm: y = LN(x + a) * gamma + beta
 cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,

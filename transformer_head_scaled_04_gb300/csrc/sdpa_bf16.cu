@@ -101,6 +101,7 @@ struct Params {
   float scale_log2;  // scale * log2(e)
   __nv_bfloat16* O;
   int64_t so_b, so_h, so_n;
+  float* lse;  // optional [B, H, Nq]: (m_used * c + log2 l) * ln 2
   int* status;
   uint64_t timeout_ns;
 };
@@ -512,6 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (p.lse != nullptr && row < p.Nq)
+      p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + row] =
+          (ok && l > 0.f) ? (m_used * c + log2f(l)) * 0.6931471805599453f : INFINITY;
     if (row < p.Nq) {
       __nv_bfloat16* dst = p.O + static_cast<int64_t>(b) * p.so_b +
                            static_cast<int64_t>(h) * p.so_h + static_cast<int64_t>(row) * p.so_n;
@@ -555,6 +559,7 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.so_b = a.so[0];
   p.so_h = a.so[1];
   p.so_n = a.so[2];
+  p.lse = a.lse;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
   cudaError_t e = cudaFuncSetAttribute(sdpa_fwd_bf16_kernel,

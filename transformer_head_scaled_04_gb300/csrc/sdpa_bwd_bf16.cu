@@ -1,0 +1,603 @@
+// sdpa_bwd_bf16.cu -- backward of scaled dot-product attention on the sm_103a tensor cores.
+//
+// The chain rule through O = softmax(Q K^T * scale, masked) V ("Transformer：抛弃循环与卷积的
+// 序列建模", Transformer 训练样例 > 反向传播; "Attention Is All You Need", lettle.cn
+// translation, 3.2.1 缩放点积注意力).  The softmax weights are rebuilt tile by tile from the
+// forward's log-sum-exp (P = 2^(s*c - lse2), c = scale*log2 e, lse2 = lse*log2 e), so the
+// n x n matrices never leave the SM:
+//   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_d dO_id O_id   (D from a small prior launch)
+//   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO
+// Two kernels, neither with atomics:
+//   dq   -- one CTA per 128-row query tile; K/V tiles stream through a TMA ring.
+//           tcgen05.mma: S = Q K^T and dP = dO V^T (128x128x16, fp32 in TMEM); four math
+//           warps (one query row per thread) turn a 64-key half at a time into bf16 dS in
+//           TMEM; dQ += dS K (128x64x16, A = dS from TMEM, B = K as an MN-major operand).
+//   dkdv -- one CTA per 128-key tile; Q/dO tiles (and their lse, D) stream through a ring.
+//           S^T = K Q^T and dP^T = V dO^T; the math warps (one key row per thread) write bf16
+//           P^T and dS^T into TMEM; dV += P^T dO and dK += dS^T Q accumulate in TMEM
+//           (all 512 columns: S^T, dP^T, P^T, dS^T, dV, dK).
+// Warps: 0-3 math, 4 TMA producer, 5 TMEM owner and MMA issuer.  Every wait is bounded; a
+// timeout records MHA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM.
+// Masks: none, causal (j <= i) and key padding (j < key_len[b]); fully masked tiles are
+// skipped, and the d = 64 heads of the forward kernel are assumed.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "device_common.cuh"
+#include "launchers.h"
+
+namespace mha {
+namespace {
+
+constexpr int kT = 128;                    // rows per tile (queries or keys)
+constexpr int kHD = 64;                    // head dim
+constexpr int kTileBytes = kT * kHD * 2;   // 16 KB
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kErrTimeout = -6;
+enum : int { kSiteBwdProducer = 41, kSiteBwdMma = 42, kSiteBwdMath = 43, kSiteBwdEpi = 44 };
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  int H, Nq, Nk, mask;
+  const int32_t* key_len;
+  float scale;       // multiplies q.k
+  const float* lse;  // [B, H, Nq]
+  const float* Dv;   // [B, H, Nq]
+  __nv_bfloat16* out0;  // dq: dQ; dkdv: dK
+  __nv_bfloat16* out1;  // dkdv: dV
+  int64_t o0_b, o0_h, o0_n, o1_b, o1_h, o1_n;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// number of keys query row i may see through key tile boundaries: L (key padding) or Nk
+__device__ __forceinline__ int key_limit(const BwdParams& p, int b) {
+  return (p.mask == 2) ? min(max(__ldg(p.key_len + b), 0), p.Nk) : p.Nk;
+}
+
+// store 64 fp32 values (times mul) of one row as bf16
+__device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t* r0,
+                                          const uint32_t* r1, float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint32_t* r = u < 4 ? r0 + 8 * u : r1 + 8 * (u - 4);
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul);
+    v.y = pack_bf16x2(__uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
+    v.z = pack_bf16x2(__uint_as_float(r[4]) * mul, __uint_as_float(r[5]) * mul);
+    v.w = pack_bf16x2(__uint_as_float(r[6]) * mul, __uint_as_float(r[7]) * mul);
+    d4[u] = v;
+  }
+}
+
+// ============================================================================ dq kernel
+// smem: Q, dO (once), K ring, V ring, barriers
+constexpr int kQOffQ = 0;
+constexpr int kQOffG = kQOffQ + kTileBytes;
+constexpr int kQOffK = kQOffG + kTileBytes;
+constexpr int kQOffV = kQOffK + kStages * kTileBytes;
+constexpr int kQOffBar = kQOffV + kStages * kTileBytes;
+constexpr int kQSmem = 1024 + kQOffBar + 256;
+// TMEM: S [0,128) dP [128,256) dS (bf16 pairs) [256,320) dQ [320,384)
+constexpr uint32_t kQColS = 0, kQColP = 128, kQColDS = 256, kQColDQ = 320;
+// barriers
+constexpr int kQBarIn = 0;                     // Q, dO landed
+constexpr int kQBarKV = 1;                     // [kStages] K_j, V_j landed
+constexpr int kQBarKVEmpty = kQBarKV + kStages;  // [kStages] MMAs done with K_j, V_j
+constexpr int kQBarSFull = kQBarKVEmpty + kStages;
+constexpr int kQBarSFree = kQBarSFull + 1;   // math warps read S, dP (count 4)
+constexpr int kQBarDSFull = kQBarSFree + 1;  // math warps wrote dS (count 4)
+constexpr int kQBarDQDone = kQBarDSFull + 1; // dQ MMA done with dS
+constexpr int kQBarDrain = kQBarDQDone + 1;
+constexpr int kQNumBars = kQBarDrain + 1;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kQNumBars);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int q0 = qt * kT;
+  const int L = key_limit(p, b);
+  // key tiles this query tile needs: causal stops at the diagonal tile
+  int nk = (L + kT - 1) / kT;
+  if (p.mask == 1) nk = min(nk, (min(q0 + kT, p.Nq) - 1) / kT + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQBarIn), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kQBarKV + s), 1);
+      mbar_init(bar(kQBarKVEmpty + s), 1);
+    }
+    mbar_init(bar(kQBarSFull), 1);
+    mbar_init(bar(kQBarSFree), 4);
+    mbar_init(bar(kQBarDSFull), 4);
+    mbar_init(bar(kQBarDQDone), 1);
+    mbar_init(bar(kQBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && nk > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(bar(kQBarIn), 2 * kTileBytes);
+      tma_load_4d(smem_u32(smem + kQOffQ), &tmQ, bar(kQBarIn), 0, q0, h, b);
+      tma_load_4d(smem_u32(smem + kQOffG), &tmG, bar(kQBarIn), 0, q0, h, b);
+      bool ok = true;
+      int issued = 0;
+      for (int j = 0; j < nk; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait_backoff(bar(kQBarKVEmpty + s), ((j / kStages) & 1) ^ 1, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kQBarKV + s), 2 * kTileBytes);
+        tma_load_4d(smem_u32(smem + kQOffK + s * kTileBytes), &tmK, bar(kQBarKV + s), 0, j * kT,
+                    h, b);
+        tma_load_4d(smem_u32(smem + kQOffV + s * kTileBytes), &tmV, bar(kQBarKV + s), 0, j * kT,
+                    h, b);
+        issued = j + 1;
+      }
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdProducer);
+      (void)mbar_wait(bar(kQBarIn), 0, p.timeout_ns);
+      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        (void)mbar_wait(bar(kQBarKV + i % kStages), (i / kStages) & 1, p.timeout_ns);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nk > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
+      constexpr uint32_t idQ = idesc_bf16_f32(kT, kHD, false, true);
+      const uint64_t dQd = smem_desc_sw128(smem_u32(smem + kQOffQ), 1024, 1024);
+      const uint64_t dGd = smem_desc_sw128(smem_u32(smem + kQOffG), 1024, 1024);
+      bool ok = mbar_wait(bar(kQBarIn), 0, p.timeout_ns);
+      for (int j = 0; ok && j < nk; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(bar(kQBarKV + s), (j / kStages) & 1, p.timeout_ns) ||
+            (j > 0 && !mbar_wait(bar(kQBarSFree), (j - 1) & 1, p.timeout_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t dK = smem_desc_sw128(smem_u32(smem + kQOffK + s * kTileBytes), 1024, 1024);
+        const uint64_t dV = smem_desc_sw128(smem_u32(smem + kQOffV + s * kTileBytes), 1024, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {  // 16 of d per MMA = 32 B in the swizzle row
+          mma_bf16_ss(tmem + kQColS, dQd + kk * 2, dK + kk * 2, idS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + kQColP, dGd + kk * 2, dV + kk * 2, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kQBarSFull));
+        if (!mbar_wait(bar(kQBarDSFull), j & 1, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dQ += dS K_j: 16 keys (8 TMEM columns of dS, 16 K rows) per MMA
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_bf16_ts(tmem + kQColDQ, tmem + kQColDS + kk * 8, dK + kk * ((16 * 128) >> 4), idQ,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kQBarDQDone));
+        mma_commit(bar(kQBarKVEmpty + s));
+      }
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
+      mma_commit(bar(kQBarDrain));
+      (void)mbar_wait(bar(kQBarDrain), 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ math warps
+    const int r_local = warp * 32 + lane;
+    const int row = q0 + r_local;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t stat = (static_cast<int64_t>(b) * p.H + h) * p.Nq + row;
+    const bool live = row < p.Nq;
+    const float lse2 = live ? __ldg(p.lse + stat) * kLog2e : INFINITY;
+    const float Dr = live ? __ldg(p.Dv + stat) : 0.f;
+    const float c = p.scale * kLog2e;
+    const int limit = (p.mask == 1) ? min(row, L - 1) : L - 1;  // keys j <= limit
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!warp_all(mbar_wait(bar(kQBarSFull), j & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int half = 0; half < 2; ++half) {
+        uint32_t s0[32], s1[32], g0[32], g1[32];
+        tmem_ld32(tmem + kQColS + lane_off + half * 64, s0);
+        tmem_ld32(tmem + kQColS + lane_off + half * 64 + 32, s1);
+        tmem_ld32(tmem + kQColP + lane_off + half * 64, g0);
+        tmem_ld32(tmem + kQColP + lane_off + half * 64 + 32, g1);
+        tmem_wait_ld();
+        reg_fence(s0);
+        reg_fence(s1);
+        reg_fence(g0);
+        reg_fence(g1);
+        if (half == 1) {  // S and dP of this tile are in registers: the next products may run
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kQBarSFree));
+        }
+        const int col0 = j * kT + half * 64;
+        uint32_t ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
+          float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
+          const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
+          const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
+          const float pa = (col0 + 2 * i <= limit) ? ex2_approx(fmaf(sa, c, -lse2)) : 0.f;
+          const float pb = (col0 + 2 * i + 1 <= limit) ? ex2_approx(fmaf(sb, c, -lse2)) : 0.f;
+          ds[i] = pack_bf16x2(pa * (ga - Dr), pb * (gb - Dr));
+        }
+        // the previous dQ product must have read dS before it is overwritten
+        if (half == 0 && j > 0 &&
+            !warp_all(mbar_wait(bar(kQBarDQDone), (j - 1) & 1, p.timeout_ns))) {
+          record_error(p.status, kErrTimeout, kSiteBwdMath);
+          ok = false;
+          break;
+        }
+        tmem_st32(tmem + kQColDS + lane_off + half * 32, ds);
+      }
+      if (!ok) break;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQBarDSFull));
+    }
+    // ---- epilogue: dQ * scale -> bf16
+    if (ok && nk > 0 && warp_all(mbar_wait(bar(kQBarDQDone), (nk - 1) & 1, p.timeout_ns))) {
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + kQColDQ + lane_off, r0);
+      tmem_ld32(tmem + kQColDQ + lane_off + 32, r1);
+      tmem_wait_ld();
+      reg_fence(r0);
+      reg_fence(r1);
+      if (live)
+        store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(row) * p.o0_n, r0, r1,
+                  p.scale);
+    } else if (live) {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      if (ok && nk > 0) record_error(p.status, kErrTimeout, kSiteBwdEpi);
+      store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(row) * p.o0_n, z, z,
+                0.f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================ dkdv kernel
+// smem: K, V (once), Q ring, dO ring, lse2/D ring (2 x 128 floats per stage), barriers
+constexpr int kKOffK = 0;
+constexpr int kKOffV = kKOffK + kTileBytes;
+constexpr int kKOffQ = kKOffV + kTileBytes;
+constexpr int kKOffG = kKOffQ + kStages * kTileBytes;
+constexpr int kKOffStat = kKOffG + kStages * kTileBytes;  // float [kStages][2][128]
+constexpr int kKOffBar = kKOffStat + kStages * 2 * kT * 4;
+constexpr int kKSmem = 1024 + kKOffBar + 256;
+// TMEM: S^T [0,128) dP^T [128,256) P^T [256,320) dS^T [320,384) dV [384,448) dK [448,512)
+constexpr uint32_t kKColS = 0, kKColP = 128, kKColPT = 256, kKColDS = 320, kKColDV = 384,
+                   kKColDK = 448;
+constexpr int kKBarIn = 0;                        // K, V landed
+constexpr int kKBarQ = 1;                         // [kStages] Q_i, dO_i, lse, D landed
+constexpr int kKBarQEmpty = kKBarQ + kStages;     // [kStages] MMAs done with Q_i, dO_i
+constexpr int kKBarSFull = kKBarQEmpty + kStages;
+constexpr int kKBarSFree = kKBarSFull + 1;        // count 4
+constexpr int kKBarPFull = kKBarSFree + 1;        // count 4
+constexpr int kKBarPVDone = kKBarPFull + 1;
+constexpr int kKBarDrain = kKBarPVDone + 1;
+constexpr int kKNumBars = kKBarDrain + 1;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
+                         const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKNumBars);
+  float* sstat = reinterpret_cast<float*>(smem + kKOffStat);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int k0 = kt * kT;
+  const int L = key_limit(p, b);
+  const int nqt = (p.Nq + kT - 1) / kT;
+  // query tiles that can see any key of this tile: causal starts at the diagonal tile; a tile
+  // past key_len is seen by none
+  const int i0 = (p.mask == 1) ? kt : 0;
+  const int ni = (k0 < L) ? max(nqt - i0, 0) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kKBarIn), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kKBarQ + s), 1);
+      mbar_init(bar(kKBarQEmpty + s), 1);
+    }
+    mbar_init(bar(kKBarSFull), 1);
+    mbar_init(bar(kKBarSFree), 4);
+    mbar_init(bar(kKBarPFull), 4);
+    mbar_init(bar(kKBarPVDone), 1);
+    mbar_init(bar(kKBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int64_t stat0 = (static_cast<int64_t>(b) * p.H + h) * p.Nq;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer (TMA + stats)
+    bool ok = true;
+    int issued = 0;
+    if (ni > 0) {
+      if (lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+        mbar_arrive_expect_tx(bar(kKBarIn), 2 * kTileBytes);
+        tma_load_4d(smem_u32(smem + kKOffK), &tmK, bar(kKBarIn), 0, k0, h, b);
+        tma_load_4d(smem_u32(smem + kKOffV), &tmV, bar(kKBarIn), 0, k0, h, b);
+      }
+      for (int t = 0; t < ni; ++t) {
+        const int s = t % kStages;
+        const int q0 = (i0 + t) * kT;
+        if (!warp_all(mbar_wait_backoff(bar(kKBarQEmpty + s), ((t / kStages) & 1) ^ 1,
+                                        p.timeout_ns))) {
+          ok = false;
+          break;
+        }
+        // this tile's lse (in log2 units) and D; rows past Nq see nothing (lse2 = +inf)
+        float* st = sstat + s * 2 * kT;
+        for (int r = lane; r < kT; r += 32) {
+          const bool live = q0 + r < p.Nq;
+          st[r] = live ? __ldg(p.lse + stat0 + q0 + r) * kLog2e : INFINITY;
+          st[kT + r] = live ? __ldg(p.Dv + stat0 + q0 + r) : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes);
+          tma_load_4d(smem_u32(smem + kKOffQ + s * kTileBytes), &tmQ, bar(kKBarQ + s), 0, q0, h,
+                      b);
+          tma_load_4d(smem_u32(smem + kKOffG + s * kTileBytes), &tmG, bar(kKBarQ + s), 0, q0, h,
+                      b);
+        }
+        issued = t + 1;
+      }
+      if (lane == 0) {
+        if (!ok) record_error(p.status, kErrTimeout, kSiteBwdProducer);
+        (void)mbar_wait(bar(kKBarIn), 0, p.timeout_ns);
+        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+          (void)mbar_wait(bar(kKBarQ + i % kStages), (i / kStages) & 1, p.timeout_ns);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ni > 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
+      constexpr uint32_t idO = idesc_bf16_f32(kT, kHD, false, true);
+      const uint64_t dKd = smem_desc_sw128(smem_u32(smem + kKOffK), 1024, 1024);
+      const uint64_t dVd = smem_desc_sw128(smem_u32(smem + kKOffV), 1024, 1024);
+      bool ok = mbar_wait(bar(kKBarIn), 0, p.timeout_ns);
+      for (int t = 0; ok && t < ni; ++t) {
+        const int s = t % kStages;
+        if (!mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns) ||
+            (t > 0 && !mbar_wait(bar(kKBarSFree), (t - 1) & 1, p.timeout_ns))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kKOffQ + s * kTileBytes), 1024, 1024);
+        const uint64_t dG = smem_desc_sw128(smem_u32(smem + kKOffG + s * kTileBytes), 1024, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {
+          mma_bf16_ss(tmem + kKColS, dKd + kk * 2, dQ + kk * 2, idS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + kKColP, dVd + kk * 2, dG + kk * 2, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kKBarSFull));
+        if (!mbar_wait(bar(kKBarPFull), t & 1, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dV += P^T dO_i and dK += dS^T Q_i: 16 queries (8 TMEM columns, 16 smem rows) per MMA
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          mma_bf16_ts(tmem + kKColDV, tmem + kKColPT + kk * 8, dG + kk * ((16 * 128) >> 4), idO,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kKColDK, tmem + kKColDS + kk * 8, dQ + kk * ((16 * 128) >> 4), idO,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kKBarPVDone));
+        mma_commit(bar(kKBarQEmpty + s));
+      }
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
+      mma_commit(bar(kKBarDrain));
+      (void)mbar_wait(bar(kKBarDrain), 0, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ math warps (one key row each)
+    const int r_local = warp * 32 + lane;
+    const int key = k0 + r_local;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.scale * kLog2e;
+    bool ok = true;
+    for (int t = 0; t < ni; ++t) {
+      const int s = t % kStages;
+      const int q0 = (i0 + t) * kT;
+      if (!warp_all(mbar_wait(bar(kKBarSFull), t & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* st = sstat + s * 2 * kT;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t s0[32], s1[32], g0[32], g1[32];
+        tmem_ld32(tmem + kKColS + lane_off + half * 64, s0);
+        tmem_ld32(tmem + kKColS + lane_off + half * 64 + 32, s1);
+        tmem_ld32(tmem + kKColP + lane_off + half * 64, g0);
+        tmem_ld32(tmem + kKColP + lane_off + half * 64 + 32, g1);
+        tmem_wait_ld();
+        reg_fence(s0);
+        reg_fence(s1);
+        reg_fence(g0);
+        reg_fence(g1);
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kKBarSFree));
+        }
+        uint32_t pp[32], ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int ca = half * 64 + 2 * i;  // query column within the tile
+          const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
+          const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
+          const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
+          const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
+          // key j = key may be seen by query q0 + ca: j < L, and j <= q for the causal mask
+          const bool oka = key < L && (p.mask != 1 || key <= q0 + ca);
+          const bool okb = key < L && (p.mask != 1 || key <= q0 + ca + 1);
+          const float pa = oka ? ex2_approx(fmaf(sa, c, -st[ca])) : 0.f;
+          const float pb = okb ? ex2_approx(fmaf(sb, c, -st[ca + 1])) : 0.f;
+          pp[i] = pack_bf16x2(pa, pb);
+          ds[i] = pack_bf16x2(pa * (ga - st[kT + ca]), pb * (gb - st[kT + ca + 1]));
+        }
+        // the previous dV/dK products must have read P^T and dS^T before they change
+        if (half == 0 && t > 0 &&
+            !warp_all(mbar_wait(bar(kKBarPVDone), (t - 1) & 1, p.timeout_ns))) {
+          record_error(p.status, kErrTimeout, kSiteBwdMath);
+          ok = false;
+          break;
+        }
+        tmem_st32(tmem + kKColPT + lane_off + half * 32, pp);
+        tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
+      }
+      if (!ok) break;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kKBarPFull));
+    }
+    // ---- epilogue: dK * scale, dV -> bf16 (zeros for keys no query sees)
+    const bool live = key < p.Nk;
+    uint32_t a0[32], a1[32], v0[32], v1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a0[i] = a1[i] = v0[i] = v1[i] = 0u;
+    if (ok && ni > 0) {
+      if (warp_all(mbar_wait(bar(kKBarPVDone), (ni - 1) & 1, p.timeout_ns))) {
+        tc_fence_after();
+        tmem_ld32(tmem + kKColDK + lane_off, a0);
+        tmem_ld32(tmem + kKColDK + lane_off + 32, a1);
+        tmem_ld32(tmem + kKColDV + lane_off, v0);
+        tmem_ld32(tmem + kKColDV + lane_off + 32, v1);
+        tmem_wait_ld();
+        reg_fence(a0);
+        reg_fence(a1);
+        reg_fence(v0);
+        reg_fence(v1);
+      } else {
+        record_error(p.status, kErrTimeout, kSiteBwdEpi);
+      }
+    }
+    if (live) {
+      store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(key) * p.o0_n, a0, a1,
+                p.scale);
+      store_row(p.out1 + b * p.o1_b + h * p.o1_h + static_cast<int64_t>(key) * p.o1_n, v0, v1,
+                1.f);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                                 const CUtensorMap& tmV, const CUtensorMap& tmG,
+                                 const SdpaBwdArgs& a, const DevCtx& ctx, cudaStream_t s) {
+  BwdParams p;
+  p.H = a.H;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.mask = a.mask;
+  p.key_len = a.key_len;
+  p.scale = a.scale;
+  p.lse = a.lse;
+  p.Dv = a.Dv;
+  p.status = ctx.status;
+  p.timeout_ns = ctx.timeout_ns;
+  cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_dq_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sdpa_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kKSmem);
+  if (e != cudaSuccess) return e;
+  p.out0 = static_cast<__nv_bfloat16*>(a.dQ);
+  p.o0_b = a.st[5][0];
+  p.o0_h = a.st[5][1];
+  p.o0_n = a.st[5][2];
+  sdpa_bwd_dq_kernel<<<dim3((a.Nq + kT - 1) / kT, a.H, a.B), kThreads, kQSmem, s>>>(
+      tmQ, tmK, tmV, tmG, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  p.out0 = static_cast<__nv_bfloat16*>(a.dK);
+  p.o0_b = a.st[6][0];
+  p.o0_h = a.st[6][1];
+  p.o0_n = a.st[6][2];
+  p.out1 = static_cast<__nv_bfloat16*>(a.dV);
+  p.o1_b = a.st[7][0];
+  p.o1_h = a.st[7][1];
+  p.o1_n = a.st[7][2];
+  sdpa_bwd_dkdv_kernel<<<dim3((a.Nk + kT - 1) / kT, a.H, a.B), kThreads, kKSmem, s>>>(
+      tmQ, tmK, tmV, tmG, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mha

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     sdpa_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                     const float* __restrict__ V, float* __restrict__ O, int Nq, int Nk, int d_k,
                     int d_v, int mask, int window, const int32_t* __restrict__ key_len,
-                    float scale,
+                    float scale, float* __restrict__ lse,
                     int64_t qb, int64_t qh, int64_t qn, int64_t qd, int64_t kb, int64_t kh,
                     int64_t kn, int64_t kd, int64_t vb, int64_t vh, int64_t vn, int64_t vd,
                     int64_t ob, int64_t oh, int64_t on, int64_t od) {
@@ -87,6 +87,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   const float inv = (nkeys > first && l > 0.f) ? 1.f / l : 0.f;  // no allowed key: zeros
+  if (lse != nullptr && lane == 0)
+    lse[(static_cast<int64_t>(b) * gridDim.y + h) * Nq + row] =
+        (nkeys > first && l > 0.f) ? m + logf(l) : INFINITY;
   float* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
 #pragma unroll
   for (int t = 0; t < kMaxD; ++t) {
@@ -106,7 +109,7 @@ cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s) {
   sdpa_f32_kernel<<<grid, kWarps * 32, 0, s>>>(
       static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
       static_cast<const float*>(a.V), static_cast<float*>(a.O), a.Nq, a.Nk, a.d_k, a.d_v,
-      a.mask, a.window, a.key_len, a.scale, a.sq[0], a.sq[1], a.sq[2], a.sq[3], a.sk[0], a.sk[1], a.sk[2],
+      a.mask, a.window, a.key_len, a.scale, a.lse, a.sq[0], a.sq[1], a.sq[2], a.sq[3], a.sk[0], a.sk[1], a.sk[2],
       a.sk[3], a.sv[0], a.sv[1], a.sv[2], a.sv[3], a.so[0], a.so[1], a.so[2], a.so[3]);
   return cudaGetLastError();
 }
