@@ -263,6 +263,89 @@ def measure_encoder(lib, C, dev, stream, flush, steps, warmup):
     }
 
 
+def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
+    """Backward of the big model's self-attention sublayer on the headline workload: the
+    attention backward alone (mha_sdpa_bwd from the forward's O and log-sum-exp) and the whole
+    sublayer's gradients (mha_layer_bwd, which recomputes the forward first)."""
+    import torch
+
+    w = si.WORKLOADS[WORKLOAD]
+    inp = si.draw_layer(w, affine=True)
+    bf = torch.bfloat16
+    t = {k: torch.from_numpy(v).to(dev, bf) for k, v in inp.items()
+         if v is not None and k != "key_len"}
+    g = np.random.Generator(np.random.PCG64(w.seed + 200))
+    dy = torch.from_numpy(si.round_bf16(g.standard_normal((w.B, w.Nq, w.D)))).to(dev, bf)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+
+    def timed(fn, what):
+        for _ in range(warmup):
+            flush.zero_()
+            C.check(fn(), what)
+        torch.cuda.synchronize(dev)
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            C.check(fn(), what)
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return float(np.mean(ms))
+
+    # attention alone, on per-head tensors [B, H, n, 64]
+    shp = (w.B, w.H, w.Nq, w.d_k)
+    q, k, v, do = (torch.from_numpy(si.round_bf16(g.standard_normal(shp))).to(dev, bf)
+                   for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    n = ctypes.c_size_t(0)
+    C.check(lib.mha_sdpa_bwd_workspace_size(w.B, w.H, w.Nq, C.MHA_BF16, ctypes.byref(n)), "ws")
+    ws_a = torch.empty(max(n.value, 256), dtype=torch.uint8, device=dev)
+    C.check(lib.mha_sdpa_fwd_lse(w.B, w.H, w.Nq, w.Nk, w.d_k, w.d_v, C.MHA_BF16, 0, None, 0.0,
+                                 vp(q), vp(k), vp(v), vp(o), None, vp(lse), sp), "fwd lse")
+    attn_ms = timed(lambda: lib.mha_sdpa_bwd(
+        w.B, w.H, w.Nq, w.Nk, w.d_k, w.d_v, C.MHA_BF16, 0, None, 0.0, vp(q), vp(k), vp(v),
+        vp(o), vp(do), vp(lse), vp(dq), vp(dk), vp(dv), None, vp(ws_a), ws_a.numel(), sp),
+        "mha_sdpa_bwd")
+    attn_fl = 2.5 * sdpa_flops(w, "none")
+    del q, k, v, do, o, lse, dq, dk, dv, ws_a
+
+    # the whole sublayer
+    C.check(lib.mha_layer_bwd_workspace_size(w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v,
+                                             C.MHA_BF16, 1, ctypes.byref(n)), "layer bwd ws")
+    ws = torch.empty(n.value, dtype=torch.uint8, device=dev)
+    e = lambda x: torch.empty_like(x)  # noqa: E731
+    out = dict(dx_q=e(t["x_q"]), dW_qkv=e(t["W_qkv"]), db_qkv=e(t["b_qkv"]), dW_o=e(t["W_o"]),
+               db_o=e(t["b_o"]), dgamma=e(t["gamma"]), dbeta=e(t["beta"]))
+    layer_ms = timed(lambda: lib.mha_layer_bwd(
+        w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16, 0, None, 1e-5, vp(t["x_q"]), None,
+        vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]), vp(t["b_o"]), vp(t["gamma"]),
+        vp(t["beta"]), vp(dy), vp(out["dx_q"]), None, vp(out["dW_qkv"]), vp(out["db_qkv"]),
+        vp(out["dW_o"]), vp(out["db_o"]), vp(out["dgamma"]), vp(out["dbeta"]), vp(ws),
+        ws.numel(), sp), "mha_layer_bwd")
+    fwd = layer_flops(w, "none")
+    gemm = fwd - sdpa_flops(w, "none")
+    layer_fl = fwd + 2.0 * gemm + attn_fl
+    return {
+        "workload": f"self-attention sublayer backward of the big model, B={w.B}, n={w.Nq}, "
+                    f"d_model={w.D}, h={w.H}, no mask, bf16",
+        "attention": {"value": attn_fl / (attn_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": attn_ms, "flops_per_step": attn_fl,
+                      "frac_of_peak": attn_fl / (attn_ms * 1e-3) / 1e12 / peak,
+                      "flops_model": "2.5x the forward's: S recomputed, dP, dV, dQ, dK"},
+        "layer": {"value": layer_fl / (layer_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "ms_per_step": layer_ms, "flops_per_step": layer_fl,
+                  "tokens_per_s": w.B * w.Nq / (layer_ms * 1e-3),
+                  "flops_model": "forward recomputed + data and weight gradients of the four "
+                                 "projections + the attention backward"},
+        "gpu_launches_per_step": {"attention": 3, "layer": 24},
+    }
+
+
 def recorded_traffic(kernel: str, sources: list[str]):
     """Per-launch DRAM bytes from the committed ncu record, or None once the kernel's sources
     no longer match the ones the counters were taken on."""
@@ -597,6 +680,8 @@ def run_ours(args):
     decode = measure_decode(lib, C, dev, stream, flush, args.steps, args.warmup,
                             float(peaks["hbm_gbs"]))
     encoder = measure_encoder(lib, C, dev, stream, flush, max(3, args.steps // 2), args.warmup)
+    backward = measure_backward(lib, C, dev, stream, flush, max(3, args.steps // 2),
+                                args.warmup, peak)
 
     # end to end through the public API: pinned host x -> device, sublayer, y -> pinned host
     x_host = t["x_q"].cpu().pin_memory()
@@ -659,6 +744,7 @@ def run_ours(args):
         "clocks": clocks,
         "ffn": ffn,
         "encoder_layer": encoder,
+        "backward": backward,
         "window": window,
         "decode": decode,
     })

@@ -224,6 +224,45 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         const cudaEvent_t* events, int n_events);
 
 /*
+ * mha_layer_bwd_workspace_size -- bytes of device workspace mha_layer_bwd needs for these
+ * sizes (self_attention != 0: x_kv is NULL and Nk == Nq).  It holds the recomputed forward
+ * intermediates, the gradients between the steps and the transposed operands of the
+ * weight-gradient products.
+ */
+int mha_layer_bwd_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d_v,
+                                 int dtype, int self_attention, size_t* bytes);
+
+/*
+ * mha_layer_bwd -- gradients of one post-norm multi-head attention sublayer ([JY] Transformer
+ * 训练样例 > 反向传播: the chain rule back through every step of mha_layer_fwd's forward).
+ * Given dy = dL/dy for y = mha_layer_fwd(...), it recomputes the forward (keeping the
+ * attention's log-sum-exp) and writes, with r = x_q + A and rhat = LayerNorm(r) unscaled:
+ *     dgamma = sum_rows dy * rhat,  dbeta = sum_rows dy,  dr = LayerNorm'(r)^T (dy * gamma)
+ *     db_o = sum_rows dr,  dW_o = dr^T C,  dC = dr W_o          (C: head concat)
+ *     dQ, dK, dV = mha_sdpa_bwd(...) per head, from dC split by heads
+ *     dW_qkv = [dQ|dK|dV]^T [x_q|x_kv|x_kv],  db_qkv = column sums of [dQ|dK|dV]
+ *     dx_q = dr + dQ W^Q (+ dK W^K + dV W^V for self-attention),  dx_kv = dK W^K + dV W^V
+ *   Inputs as for mha_layer_fwd (same arguments, same values; beta does not enter any
+ *   gradient and may be NULL); dy [B,Nq,D].  mask: none, causal or key padding.
+ *   Outputs (all `dtype`, written, none may alias an input, another output or the workspace):
+ *   dx_q [B,Nq,D]; dx_kv [B,Nk,D] for cross-attention (ignored, may be NULL, for self);
+ *   dW_qkv like W_qkv; db_qkv [H*(2*d_k+d_v)]; dW_o like W_o; db_o, dgamma, dbeta [D]
+ *   (always written, also when the forward passed NULL for the bias, gamma or beta).
+ *   Sums over rows run per chunk of 256 rows and then over the chunks in a fixed order:
+ *   results are deterministic.  workspace: mha_layer_bwd_workspace_size() bytes, 256-byte
+ *   aligned.  Limits and errors as for mha_layer_fwd; MHA_ERR_INVALID for a NULL output.
+ * Launches (all on `stream`): the forward's GEMMs, attention and W^O GEMM again, the
+ * LayerNorm backward, the attention backward, the data- and weight-gradient GEMMs on the
+ * same tensor-core kernel as the forward, transposes and column-sum reductions.
+ */
+int mha_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                  const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                  const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                  const void* gamma, const void* beta, const void* dy, void* dx_q, void* dx_kv,
+                  void* dW_qkv, void* db_qkv, void* dW_o, void* db_o, void* dgamma, void* dbeta,
+                  void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * mha_layer_fwd_noalloc -- mha_layer_fwd for callers that cannot supply a workspace.
  * The pages have no counterpart: this is a packaging variant, not part of the method.
  *

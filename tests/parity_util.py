@@ -16,6 +16,22 @@ Tolerances (stated for the sublayer's outputs):
   its magnitude grows with the sequence (a key seen by 200 queries sums 200 rows of dO); the
   stored bf16 value alone is off by up to 2^-9 |ref|, and the bf16 rounding of the softmax
   weights and dS inside the products adds a few times that.
+* bf16 gradients of the whole sublayer (mha_layer_bwd): these pass through about k = 8
+  bf16 stores on the way from dy (dr, dC, the projected Q/K/V, the head concat O, the
+  softmax weights and dS inside the attention products, the projection gradients, the
+  result).  One bf16 rounding moves a value by 2^-8/sqrt(12) times its size on average over
+  the significand (about 1.7e-3 rms, relative); k independent ones give sqrt(k) * 1.7e-3 =
+  4.7e-3.  Relative L2 <= 1e-2 is twice that.  Elementwise:
+  - per-token gradients (dx_q, dx_kv): |gpu - ref| <= 2e-2 * max(1, rms of the token's row
+    of ref) + 2^-7 |ref|.  A key/value row sums over the queries that see it, so rows differ
+    in size by the number of those queries (5 against 200 in the ragged cases); each row is
+    held to the per-token bound at its own scale.
+  - parameter gradients (dW, db, dgamma, dbeta: sums over all B*N tokens): |gpu - ref| <=
+    5e-2 * max(1, rms(ref)) + 2^-7 |ref|.  An entry's error is a random walk over the tokens
+    with steps of 4.7e-3 of each term, about 4.7e-3 of the entry's own scale; over a million
+    entries the largest is about 5 sigma, and entry scales run to about twice rms(ref)
+    (LayerNorm's gamma scales the rows of dW_o, the heads' output sizes its columns):
+    5 * 4.7e-3 * 2 = 4.7e-2.
 """
 import numpy as np
 
@@ -67,4 +83,39 @@ def assert_bf16_grad_close(got, ref, what=""):
     worst = float((np.abs(got - ref) / bound).max()) if got.size else 0.0
     assert worst <= 1.0 and rel <= BF16_REL_L2, \
         f"{what}: worst |d| / (2e-2 + 2^-7 |ref|) = {worst:.3f}, relL2={rel:.3e}"
+    return worst, rel
+
+
+BF16_LAYER_GRAD_REL_L2 = 1e-2
+BF16_PARAM_GRAD_ABS = 5e-2
+
+
+def assert_bf16_token_grad_close(got, ref, what=""):
+    """Per-token gradient of the sublayer: each row (token) at its own scale."""
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    _, rel = errors(got, ref)
+    r2 = ref.reshape(-1, ref.shape[-1])
+    row_rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
+    bound = BF16_GRAD_ABS * np.maximum(1.0, row_rms) + BF16_GRAD_REL * np.abs(r2)
+    worst = float((np.abs(got.reshape(r2.shape) - r2) / bound).max()) if got.size else 0.0
+    assert worst <= 1.0 and rel <= BF16_LAYER_GRAD_REL_L2, \
+        f"{what}: worst |d| / (2e-2 max(1, row rms) + 2^-7 |ref|) = {worst:.3f}, " \
+        f"relL2={rel:.3e}"
+    return worst, rel
+
+
+def assert_bf16_param_grad_close(got, ref, what=""):
+    """Parameter gradient of the sublayer (a sum over every token)."""
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    _, rel = errors(got, ref)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    bound = BF16_PARAM_GRAD_ABS * max(1.0, rms) + BF16_GRAD_REL * np.abs(ref)
+    worst = float((np.abs(got - ref) / bound).max()) if got.size else 0.0
+    assert worst <= 1.0 and rel <= BF16_LAYER_GRAD_REL_L2, \
+        f"{what}: worst |d| / (5e-2 max(1, rms) + 2^-7 |ref|) = {worst:.3f} (rms {rms:.3g}), " \
+        f"relL2={rel:.3e}"
     return worst, rel

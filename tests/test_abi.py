@@ -309,3 +309,43 @@ def test_sdpa_backward_validation(lib):
         C.MHA_ERR_INVALID
     assert f(1, 1, 8, 8, 64, 64, 1, 0, None, 0.0, FAKE, FAKE, FAKE, FAKE, None,
              ctypes.c_void_p(0x10002), None) == C.MHA_ERR_ALIGN
+
+
+def test_layer_backward_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 1, 1,
+                                            ctypes.byref(n)) == 0
+    self_bytes = n.value
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 1, 0,
+                                            ctypes.byref(n)) == 0
+    assert n.value > self_bytes          # cross-attention keeps separate key/value buffers
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 90, 128, 64, 64, 1, 1,
+                                            ctypes.byref(n)) == C.MHA_ERR_INVALID
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 96, 64, 64, 1, 1,
+                                            ctypes.byref(n)) == C.MHA_ERR_UNSUPPORTED
+
+    def bwd(**kw):
+        a = dict(B=2, H=2, Nq=100, Nk=100, D=128, dk=64, dv=64, dt=1, mask=0, kl=None, eps=1e-5,
+                 x_kv=None, dy=FAKE, dx_q=FAKE, dx_kv=None, dW_qkv=FAKE, dgamma=FAKE,
+                 ws=FAKE, ws_bytes=self_bytes)
+        a.update(kw)
+        return lib.mha_layer_bwd(a["B"], a["H"], a["Nq"], a["Nk"], a["D"], a["dk"], a["dv"],
+                                 a["dt"], a["mask"], a["kl"], a["eps"], FAKE, a["x_kv"], FAKE,
+                                 None, FAKE, None, None, None, a["dy"], a["dx_q"], a["dx_kv"],
+                                 a["dW_qkv"], FAKE, FAKE, FAKE, a["dgamma"], FAKE, a["ws"],
+                                 a["ws_bytes"], None)
+
+    assert bwd(B=0) == C.MHA_ERR_INVALID
+    assert bwd(mask=3) == C.MHA_ERR_INVALID              # no window mask in the sublayer
+    assert bwd(Nk=90) == C.MHA_ERR_INVALID               # self-attention needs Nq == Nk
+    assert bwd(mask=2) == C.MHA_ERR_INVALID              # key padding needs key_len
+    assert bwd(dy=None) == C.MHA_ERR_INVALID
+    assert bwd(dW_qkv=None) == C.MHA_ERR_INVALID
+    assert bwd(dgamma=None) == C.MHA_ERR_INVALID
+    assert bwd(x_kv=FAKE, Nk=90) == C.MHA_ERR_INVALID     # cross-attention needs dx_kv
+    assert bwd(eps=-1.0) == C.MHA_ERR_INVALID
+    assert bwd(D=96) == C.MHA_ERR_UNSUPPORTED
+    assert bwd(ws=None) == C.MHA_ERR_WORKSPACE
+    assert bwd(ws_bytes=self_bytes - 1) == C.MHA_ERR_WORKSPACE
+    assert bwd(dx_q=ODD) == C.MHA_ERR_ALIGN
+    assert bwd(ws=ctypes.c_void_p(0x10010)) == C.MHA_ERR_ALIGN

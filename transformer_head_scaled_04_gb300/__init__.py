@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) multi-head attention sublayer forward, with the position-wise
+"""GB300 (sm_103a) multi-head attention sublayer forward and backward, with the position-wise
 feed-forward sublayer and the encoder layer they form: a C-ABI CUDA library (libmha.so,
 declared in include/mha.h) and a thin torch binding of it.
 
@@ -18,9 +18,11 @@ from .api import (  # noqa: F401
     encoder_layer_workspace_size,
     ffn,
     ffn_workspace_size,
+    layer_bwd_workspace_size,
     layer_workspace_size,
     linear,
     mha_layer,
+    mha_layer_backward,
     residual_layernorm,
     sdpa,
     sdpa_backward,

@@ -196,6 +196,49 @@ def mha_layer(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, mask="none", ke
     return out
 
 
+def layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype, self_attention) -> int:
+    n = ctypes.c_size_t(0)
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    C.check(C.load().mha_layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dt,
+                                                  int(bool(self_attention)), ctypes.byref(n)),
+            "mha_layer_bwd_workspace_size")
+    return n.value
+
+
+def mha_layer_backward(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, dy, mask="none",
+                       key_len=None, eps=1e-5, d_k=None, d_v=None, workspace=None):
+    """Gradients of ``mha_layer`` with respect to every input and parameter, given dy = dL/dy,
+    via ``mha_layer_bwd``.  Returns a dict with dx_q, dx_kv (None for self-attention), dW_qkv,
+    db_qkv, dW_o, db_o, dgamma, dbeta -- each shaped like its tensor (the bias, gamma and beta
+    gradients are [D] / [H*(2d_k+d_v)] even where the forward passed None).
+    """
+    _cuda(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, dy, key_len, workspace)
+    _contiguous("mha_layer_backward", x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, dy)
+    B, Nq, D = x_q.shape
+    Nk = Nq if x_kv is None else x_kv.shape[1]
+    d_k = D // H if d_k is None else d_k
+    d_v = D // H if d_v is None else d_v
+    if tuple(dy.shape) != (B, Nq, D):
+        raise ValueError(f"dy must be [{B},{Nq},{D}]")
+    ws = layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, x_q.dtype, x_kv is None)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x_q.device)
+    e = lambda *shape: torch.empty(shape, dtype=x_q.dtype, device=x_q.device)  # noqa: E731
+    g = {"dx_q": torch.empty_like(x_q),
+         "dx_kv": None if x_kv is None else torch.empty_like(x_kv),
+         "dW_qkv": torch.empty_like(W_qkv), "db_qkv": e(W_qkv.shape[0]),
+         "dW_o": torch.empty_like(W_o), "db_o": e(D), "dgamma": e(D), "dbeta": e(D)}
+    with torch.cuda.device(x_q.device):
+        code = C.load().mha_layer_bwd(
+            B, H, Nq, Nk, D, d_k, d_v, _dt(x_q), _mask(mask), _ptr(key_len), float(eps),
+            _ptr(x_q), _ptr(x_kv), _ptr(W_qkv), _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma),
+            _ptr(beta), _ptr(dy), _ptr(g["dx_q"]), _ptr(g["dx_kv"]), _ptr(g["dW_qkv"]),
+            _ptr(g["db_qkv"]), _ptr(g["dW_o"]), _ptr(g["db_o"]), _ptr(g["dgamma"]),
+            _ptr(g["dbeta"]), _ptr(workspace), workspace.numel(), _stream(x_q.device))
+    C.check(code, "mha_layer_bwd")
+    return g
+
+
 def linear(x, W, bias=None, out=None, relu=False):
     """Y = x W^T + bias via ``mha_linear_fwd`` (``mha_linear_relu_fwd``: max(0, .) when relu);
     x [M,K] (row pitch = x.stride(0)), W [N,K]."""

@@ -1,0 +1,246 @@
+// bwd_util.cu -- the memory-bound steps of the sublayer's backward pass ("Transformer：抛弃
+// 循环与卷积的序列建模", Transformer 训练样例 > 反向传播: the chain rule back through the
+// residual + LayerNorm step of "Attention Is All You Need", lettle.cn translation, 3.1).
+//
+//   layernorm_bwd: with r = x + a, rhat = (r - mean) * rstd, g = dy * gamma:
+//                  dr = (g - mean(g) - rhat * mean(g * rhat)) * rstd   (one warp per row;
+//                  also keeps each row's mean and rstd for the parameter gradients)
+//   ln_param_partials + reduce_partials: dgamma = sum dy * rhat, dbeta = sum dy and
+//                  db_o = sum dr over all rows, summed per chunk of rows and then over the
+//                  chunks in a fixed order (deterministic)
+//   colsum_partials + reduce_partials: a bias gradient, the column sums of a gradient matrix
+//   transpose: Y = X^T with the reduced dimension padded by zero rows to a whole number of
+//                  64-wide K slices, so the weight-gradient products run on the same GEMM
+#include <cuda_bf16.h>
+
+#include "launchers.h"
+
+namespace mha {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p) {
+  if constexpr (sizeof(T) == 2)
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(p));
+  else
+    return static_cast<float>(*p);
+}
+template <typename T>
+__device__ __forceinline__ T stf(float v) {
+  if constexpr (sizeof(T) == 2)
+    return __float2bfloat16_rn(v);
+  else
+    return v;
+}
+
+constexpr int kRows = 8;  // rows (warps) per block in the row kernels
+
+// one warp per row, D <= 32 * NIT
+template <typename T, int NIT>
+__global__ void __launch_bounds__(kRows * 32)
+    layernorm_bwd_kernel(const T* __restrict__ x, const T* __restrict__ a,
+                         const T* __restrict__ gamma, const T* __restrict__ dy,
+                         T* __restrict__ dr, float2* __restrict__ stats, int M, int D,
+                         float eps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRows + warp;
+  if (row >= M) return;
+  const int64_t base = static_cast<int64_t>(row) * D;
+  float r[NIT], g[NIT];
+  float sum = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int col = it * 32 + lane;
+    r[it] = 0.f;
+    g[it] = 0.f;
+    if (col < D) {
+      r[it] = ldf(x + base + col) + ldf(a + base + col);
+      g[it] = ldf(dy + base + col) * (gamma ? ldf(gamma + col) : 1.f);
+      sum += r[it];
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float mean = sum / static_cast<float>(D);
+  float sq = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it)
+    if (it * 32 + lane < D) sq = fmaf(r[it] - mean, r[it] - mean, sq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  const float rstd = 1.0f / sqrtf(sq / static_cast<float>(D) + eps);
+  float sg = 0.f, sgr = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    if (it * 32 + lane < D) {
+      r[it] = (r[it] - mean) * rstd;  // rhat
+      sg += g[it];
+      sgr = fmaf(g[it], r[it], sgr);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sg += __shfl_xor_sync(0xffffffffu, sg, off);
+    sgr += __shfl_xor_sync(0xffffffffu, sgr, off);
+  }
+  const float mg = sg / static_cast<float>(D), mgr = sgr / static_cast<float>(D);
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int col = it * 32 + lane;
+    if (col < D) dr[base + col] = stf<T>((g[it] - mg - r[it] * mgr) * rstd);
+  }
+  if (lane == 0) stats[row] = make_float2(mean, rstd);
+}
+
+// rows [chunk * rows_per_chunk, ...) of columns [blockIdx.x * 256 + threadIdx.x]: partial
+// sums of dy * rhat, dy and dr, written to part[(chunk * 3 + k) * D + col]
+template <typename T>
+__global__ void __launch_bounds__(256)
+    ln_param_partials_kernel(const T* __restrict__ x, const T* __restrict__ a,
+                             const T* __restrict__ dy, const T* __restrict__ dr,
+                             const float2* __restrict__ stats, float* __restrict__ part, int M,
+                             int D, int rows_per_chunk) {
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  const int chunk = blockIdx.y;
+  if (col >= D) return;
+  const int r0 = chunk * rows_per_chunk, r1 = min(r0 + rows_per_chunk, M);
+  float sg = 0.f, sb = 0.f, sd = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const int64_t i = static_cast<int64_t>(r) * D + col;
+    const float2 st = stats[r];
+    const float rhat = (ldf(x + i) + ldf(a + i) - st.x) * st.y;
+    const float d = ldf(dy + i);
+    sg = fmaf(d, rhat, sg);
+    sb += d;
+    sd += ldf(dr + i);
+  }
+  float* p = part + static_cast<int64_t>(chunk) * 3 * D + col;
+  p[0] = sg;
+  p[D] = sb;
+  p[2 * D] = sd;
+}
+
+// column sums of X [M, N] (row pitch ld) over chunks of rows: part[chunk * N + col]
+template <typename T>
+__global__ void __launch_bounds__(256)
+    colsum_partials_kernel(const T* __restrict__ X, int64_t ld, int M, int N,
+                           int rows_per_chunk, float* __restrict__ part) {
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  const int chunk = blockIdx.y;
+  if (col >= N) return;
+  const int r0 = chunk * rows_per_chunk, r1 = min(r0 + rows_per_chunk, M);
+  float s = 0.f;
+  for (int r = r0; r < r1; ++r) s += ldf(X + static_cast<int64_t>(r) * ld + col);
+  part[static_cast<int64_t>(chunk) * N + col] = s;
+}
+
+// out[col] = sum over chunks, in chunk order, of part[chunk * chunk_stride + col]
+template <typename T>
+__global__ void __launch_bounds__(256)
+    reduce_partials_kernel(const float* __restrict__ part, int nchunk, int64_t chunk_stride,
+                           int N, T* __restrict__ out) {
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  if (col >= N) return;
+  float s = 0.f;
+  for (int c = 0; c < nchunk; ++c) s += part[static_cast<int64_t>(c) * chunk_stride + col];
+  out[col] = stf<T>(s);
+}
+
+// Y[c * ldy + r] = X[r * ldx + c] for r < R, c < C; rows R <= r < R_pad of Y's columns are 0
+template <typename T>
+__global__ void __launch_bounds__(256)
+    transpose_kernel(const T* __restrict__ X, int64_t ldx, int R, int C, T* __restrict__ Y,
+                     int64_t ldy, int R_pad) {
+  __shared__ T tile[32][33];
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int k = ty; k < 32; k += 8) {
+    const int r = r0 + k, c = c0 + tx;
+    tile[k][tx] = (r < R && c < C) ? X[static_cast<int64_t>(r) * ldx + c] : stf<T>(0.f);
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int c = c0 + k, r = r0 + tx;
+    if (c < C && r < R_pad) Y[static_cast<int64_t>(c) * ldy + r] = tile[tx][k];
+  }
+}
+
+constexpr int kChunkRows = 256;
+
+}  // namespace
+
+int bwd_row_chunks(int M) { return (M + kChunkRows - 1) / kChunkRows; }
+
+cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void* x,
+                                 const void* a, const void* gamma, const void* dy, void* dr,
+                                 float2* stats, float* part, cudaStream_t s) {
+  const dim3 grid_rows((M + kRows - 1) / kRows);
+  const int nit = (D + 31) / 32;
+  const dim3 grid_cols((D + 255) / 256, bwd_row_chunks(M));
+#define MHA_LN_BWD(T, N)                                                                    \
+  layernorm_bwd_kernel<T, N><<<grid_rows, kRows * 32, 0, s>>>(                              \
+      static_cast<const T*>(x), static_cast<const T*>(a), static_cast<const T*>(gamma),     \
+      static_cast<const T*>(dy), static_cast<T*>(dr), stats, M, D, eps)
+  if (dtype == 1) {
+    if (nit <= 16) MHA_LN_BWD(__nv_bfloat16, 16);
+    else if (nit <= 32) MHA_LN_BWD(__nv_bfloat16, 32);
+    else MHA_LN_BWD(__nv_bfloat16, 64);
+  } else {
+    if (nit <= 16) MHA_LN_BWD(float, 16);
+    else if (nit <= 32) MHA_LN_BWD(float, 32);
+    else MHA_LN_BWD(float, 64);
+  }
+#undef MHA_LN_BWD
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dtype == 1)
+    ln_param_partials_kernel<__nv_bfloat16><<<grid_cols, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
+        static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(dr), stats,
+        part, M, D, kChunkRows);
+  else
+    ln_param_partials_kernel<float><<<grid_cols, 256, 0, s>>>(
+        static_cast<const float*>(x), static_cast<const float*>(a),
+        static_cast<const float*>(dy), static_cast<const float*>(dr), stats, part, M, D,
+        kChunkRows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, int N,
+                                   float* part, cudaStream_t s) {
+  const dim3 grid((N + 255) / 256, bwd_row_chunks(M));
+  if (dtype == 1)
+    colsum_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(X), ld, M, N, kChunkRows, part);
+  else
+    colsum_partials_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), ld, M, N,
+                                                       kChunkRows, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
+                                   int64_t chunk_stride, int N, void* out, cudaStream_t s) {
+  const dim3 grid((N + 255) / 256);
+  if (dtype == 1)
+    reduce_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        part, nchunk, chunk_stride, N, static_cast<__nv_bfloat16*>(out));
+  else
+    reduce_partials_kernel<float><<<grid, 256, 0, s>>>(part, nchunk, chunk_stride, N,
+                                                       static_cast<float*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C, void* Y,
+                             int64_t ldy, int R_pad, cudaStream_t s) {
+  const dim3 grid((R_pad + 31) / 32, (C + 31) / 32);
+  if (dtype == 1)
+    transpose_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(X), ldx, R, C, static_cast<__nv_bfloat16*>(Y), ldy,
+        R_pad);
+  else
+    transpose_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), ldx, R, C,
+                                                 static_cast<float*>(Y), ldy, R_pad);
+  return cudaGetLastError();
+}
+
+}  // namespace mha

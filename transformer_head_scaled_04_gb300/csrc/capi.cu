@@ -134,7 +134,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------------ step launchers
 int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
                const void* bias, void* Y, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
-               bool relu = false) {
+               bool relu = false, const void* residual = nullptr) {
   cudaError_t e;
   if (dtype == MHA_BF16) {
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);
@@ -142,11 +142,11 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
     CUtensorMap tmX, tmW;
     if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, bn))
       return MHA_ERR_CUDA;
-    e = mha::launch_gemm_bf16(tmX, tmW, bn, relu, bias, Y, M, N, K, ldy, ctx, s);
+    e = mha::launch_gemm_bf16(tmX, tmW, bn, relu, bias, Y, M, N, K, ldy, ctx, s, residual);
   } else {
     e = mha::launch_gemm_f32(static_cast<const float*>(X), ldx, static_cast<const float*>(W),
                              static_cast<const float*>(bias), relu, static_cast<float*>(Y), ldy,
-                             M, N, K, s);
+                             M, N, K, s, static_cast<const float*>(residual));
   }
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -162,6 +162,24 @@ int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t 
     e = mha::launch_sdpa_bf16(tq, tk, tv, a, ctx, s);
   } else {
     e = mha::launch_sdpa_f32(a, s);
+  }
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// rowdot (D) and the gradient kernels of one attention backward; a.Dv is the caller's scratch
+int run_sdpa_bwd(const mha::SdpaBwdArgs& a, int dtype, const DevCtx& ctx, cudaStream_t s) {
+  cudaError_t e = mha::launch_sdpa_bwd_rowdot(a, dtype, s);
+  if (e != cudaSuccess) return MHA_ERR_CUDA;
+  if (dtype == MHA_BF16) {
+    CUtensorMap tq, tk, tv, tg;
+    if (!map_bhnd_bf16(&tq, a.Q, a.B, a.H, a.Nq, a.st[0]) ||
+        !map_bhnd_bf16(&tk, a.K, a.B, a.H, a.Nk, a.st[1]) ||
+        !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.st[2]) ||
+        !map_bhnd_bf16(&tg, a.dO, a.B, a.H, a.Nq, a.st[4]))
+      return MHA_ERR_CUDA;
+    e = mha::launch_sdpa_bwd_bf16(tq, tk, tv, tg, a, ctx, s);
+  } else {
+    e = mha::launch_sdpa_bwd_f32(a, s);
   }
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -522,18 +540,7 @@ int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
   DevCtx ctx;
   st = device_ctx(&ctx);
   if (st != MHA_OK) return st;
-  cudaError_t e = mha::launch_sdpa_bwd_rowdot(a, dtype, stream);
-  if (e != cudaSuccess) return MHA_ERR_CUDA;
-  if (dtype == MHA_BF16) {
-    CUtensorMap tq, tk, tv, tg;
-    if (!map_bhnd_bf16(&tq, Q, B, H, Nq, a.st[0]) || !map_bhnd_bf16(&tk, K, B, H, Nk, a.st[1]) ||
-        !map_bhnd_bf16(&tv, V, B, H, Nk, a.st[2]) || !map_bhnd_bf16(&tg, dO, B, H, Nq, a.st[4]))
-      return MHA_ERR_CUDA;
-    e = mha::launch_sdpa_bwd_bf16(tq, tk, tv, tg, a, ctx, stream);
-  } else {
-    e = mha::launch_sdpa_bwd_f32(a, stream);
-  }
-  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  return run_sdpa_bwd(a, dtype, ctx, stream);
 }
 
 int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
@@ -875,6 +882,266 @@ int mha_debug_wait_selftest(int64_t timeout_ns, cudaStream_t stream) {
   if (timeout_ns > 1000000000) timeout_ns = 1000000000;
   ctx.timeout_ns = static_cast<uint64_t>(timeout_ns);
   return mha::launch_wait_selftest(ctx, stream) == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ==================================================================== sublayer backward
+namespace {
+
+// Scratch of one sublayer backward (offsets into the caller's workspace, 256-byte aligned).
+// Forward intermediates: the projections (self: Q|K|V interleaved per token; cross: Q, then
+// K|V), the head-concat C, the W^O output A, the log-sum-exp; then the gradients dr, dC and
+// the projections' gradients (same layouts), the transposed operands of the weight-gradient
+// GEMMs (token axis padded to a multiple of 64) and the fp32 partial column sums.
+struct LayerBwdPlan {
+  int Mq, Mk, Mq_pad, Mk_pad, nqk, nv, ld_q, ld_kv;  // ld_q: row pitch of the Q projection
+  size_t off_q, off_kv, off_c, off_a, off_lse, off_dvec, off_stats, off_part, off_dr, off_dc,
+      off_dq, off_dkv, off_wot, off_wqt, off_wkvt, off_drt, off_ct, off_dqt, off_dkvt, off_xqt,
+      off_xkvt, total;
+};
+
+LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                            bool self) {
+  const size_t es = elem_size(dtype);
+  LayerBwdPlan p;
+  p.Mq = B * Nq;
+  p.Mk = B * Nk;
+  p.Mq_pad = (p.Mq + 63) / 64 * 64;
+  p.Mk_pad = (p.Mk + 63) / 64 * 64;
+  p.nqk = H * d_k;
+  p.nv = H * d_v;
+  p.ld_q = self ? 2 * p.nqk + p.nv : p.nqk;
+  p.ld_kv = self ? 2 * p.nqk + p.nv : p.nqk + p.nv;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += round_up(bytes, 256);
+    return at;
+  };
+  const int nchunk = mha::bwd_row_chunks(p.Mq > p.Mk ? p.Mq : p.Mk);
+  const int part_cols = (3 * D > 2 * p.nqk + p.nv) ? 3 * D : 2 * p.nqk + p.nv;
+  p.off_q = take(static_cast<size_t>(p.Mq) * p.ld_q * es);
+  p.off_kv = self ? p.off_q : take(static_cast<size_t>(p.Mk) * p.ld_kv * es);
+  p.off_c = take(static_cast<size_t>(p.Mq) * p.nv * es);
+  p.off_a = take(static_cast<size_t>(p.Mq) * D * es);
+  p.off_lse = take(static_cast<size_t>(B) * H * Nq * 4);
+  p.off_dvec = take(static_cast<size_t>(B) * H * Nq * 4);
+  p.off_stats = take(static_cast<size_t>(p.Mq) * 8);
+  p.off_part = take(static_cast<size_t>(nchunk) * part_cols * 4);
+  p.off_dr = take(static_cast<size_t>(p.Mq) * D * es);
+  p.off_dc = take(static_cast<size_t>(p.Mq) * p.nv * es);
+  p.off_dq = take(static_cast<size_t>(p.Mq) * p.ld_q * es);
+  p.off_dkv = self ? p.off_dq : take(static_cast<size_t>(p.Mk) * p.ld_kv * es);
+  p.off_wot = take(static_cast<size_t>(p.nv) * D * es);
+  p.off_wqt = take(static_cast<size_t>(D) * p.ld_q * es);
+  p.off_wkvt = self ? p.off_wqt : take(static_cast<size_t>(D) * p.ld_kv * es);
+  p.off_drt = take(static_cast<size_t>(D) * p.Mq_pad * es);
+  p.off_ct = take(static_cast<size_t>(p.nv) * p.Mq_pad * es);
+  p.off_dqt = take(static_cast<size_t>(p.ld_q) * p.Mq_pad * es);
+  p.off_dkvt = self ? p.off_dqt : take(static_cast<size_t>(p.ld_kv) * p.Mk_pad * es);
+  p.off_xqt = take(static_cast<size_t>(D) * p.Mq_pad * es);
+  p.off_xkvt = self ? p.off_xqt : take(static_cast<size_t>(D) * p.Mk_pad * es);
+  p.total = o;
+  return p;
+}
+
+int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                   const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                   const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                   const void* gamma, const void* dy, void* dx_q, void* dx_kv, void* dW_qkv,
+                   void* db_qkv, void* dW_o, void* db_o, void* dgamma, void* dbeta,
+                   void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
+  if (st != MHA_OK) return st;
+  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
+  const bool self = (x_kv == nullptr);
+  if ((self || mask == MHA_MASK_CAUSAL) && Nq != Nk) return MHA_ERR_INVALID;
+  if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
+  const void* need[] = {x_q, W_qkv, W_o, dy, dx_q, dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta};
+  for (const void* q : need)
+    if (q == nullptr) return MHA_ERR_INVALID;
+  if (!self && dx_kv == nullptr) return MHA_ERR_INVALID;
+  if (std::isnan(ln_eps) || ln_eps < 0.f) return MHA_ERR_INVALID;
+  const LayerBwdPlan pl = plan_layer_bwd(B, H, Nq, Nk, D, d_k, d_v, dtype, self);
+  if (workspace == nullptr || ws_bytes < pl.total) return MHA_ERR_WORKSPACE;
+  const void* all[] = {x_q,  x_kv,  W_qkv, b_qkv, W_o,    b_o,  gamma,  dy,   dx_q,
+                       dx_kv, dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta, workspace};
+  for (const void* q : all)
+    if (q != nullptr && !aligned(q, 16)) return MHA_ERR_ALIGN;
+  if (key_len != nullptr && !aligned(key_len, 4)) return MHA_ERR_ALIGN;
+  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  DevCtx ctx;
+  st = device_ctx(&ctx);
+  if (st != MHA_OK) return st;
+
+  const size_t es = elem_size(dtype);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
+  const uint8_t* Wb = static_cast<const uint8_t*>(W_qkv);
+  const uint8_t* bq = static_cast<const uint8_t*>(b_qkv);
+  const int Mq = pl.Mq, Mk = pl.Mk, nqk = pl.nqk, nv = pl.nv;
+  const void* src_kv = self ? x_q : x_kv;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; };
+#define MHA_TRY(call)          \
+  do {                         \
+    const int s_ = (call);     \
+    if (s_ != MHA_OK) return s_; \
+  } while (0)
+
+  // ---- forward again, keeping what the backward needs
+  mha::SdpaArgs a;
+  a.B = B; a.H = H; a.Nq = Nq; a.Nk = Nk; a.d_k = d_k; a.d_v = d_v;
+  a.mask = mask;
+  a.key_len = (mask == MHA_MASK_KEY_PADDING) ? key_len : nullptr;
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+  uint8_t* qbuf = ws + pl.off_q;
+  uint8_t* kvbuf = ws + pl.off_kv;
+  if (self) {
+    MHA_TRY(run_linear(Mq, pl.ld_q, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, pl.ld_q, ctx, stream));
+    a.Q = qbuf;
+    a.K = qbuf + nqk * es;
+    a.V = qbuf + 2 * nqk * es;
+  } else {
+    MHA_TRY(run_linear(Mq, nqk, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, nqk, ctx, stream));
+    MHA_TRY(run_linear(Mk, pl.ld_kv, D, dtype, x_kv, D, Wb + static_cast<size_t>(nqk) * D * es,
+                       bq ? bq + nqk * es : nullptr, kvbuf, pl.ld_kv, ctx, stream));
+    a.Q = qbuf;
+    a.K = kvbuf;
+    a.V = kvbuf + nqk * es;
+  }
+  const int64_t sq[4] = {static_cast<int64_t>(Nq) * pl.ld_q, d_k, pl.ld_q, 1};
+  const int64_t sk[4] = {static_cast<int64_t>(Nk) * pl.ld_kv, d_k, pl.ld_kv, 1};
+  const int64_t sv[4] = {static_cast<int64_t>(Nk) * pl.ld_kv, d_v, pl.ld_kv, 1};
+  const int64_t so[4] = {static_cast<int64_t>(Nq) * nv, d_v, nv, 1};
+  for (int i = 0; i < 4; ++i) {
+    a.sq[i] = sq[i];
+    a.sk[i] = sk[i];
+    a.sv[i] = sv[i];
+    a.so[i] = so[i];
+  }
+  a.O = W(pl.off_c);
+  a.lse = static_cast<float*>(W(pl.off_lse));
+  MHA_TRY(run_sdpa(a, dtype, ctx, stream));
+  MHA_TRY(run_linear(Mq, D, nv, dtype, W(pl.off_c), nv, W_o, b_o, W(pl.off_a), D, ctx, stream));
+
+  // ---- residual + LayerNorm backward: dr; dgamma, dbeta, db_o from per-chunk partials
+  float* part = static_cast<float*>(W(pl.off_part));
+  MHA_TRY(ok(mha::launch_layernorm_bwd(dtype, Mq, D, ln_eps, x_q, W(pl.off_a), gamma, dy,
+                                       W(pl.off_dr), static_cast<float2*>(W(pl.off_stats)),
+                                       part, stream)));
+  const int nch_q = mha::bwd_row_chunks(Mq);
+  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, 3 * D, D, dgamma, stream)));
+  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part + D, nch_q, 3 * D, D, dbeta, stream)));
+  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part + 2 * D, nch_q, 3 * D, D, db_o, stream)));
+
+  // ---- W^O: dC = dr W^O (via W^O^T), dW^O = dr^T C
+  MHA_TRY(ok(mha::launch_transpose(dtype, W_o, nv, D, nv, W(pl.off_wot), D, D, stream)));
+  MHA_TRY(run_linear(Mq, nv, D, dtype, W(pl.off_dr), D, W(pl.off_wot), nullptr, W(pl.off_dc),
+                     nv, ctx, stream));
+  MHA_TRY(ok(mha::launch_transpose(dtype, W(pl.off_dr), D, Mq, D, W(pl.off_drt), pl.Mq_pad,
+                                   pl.Mq_pad, stream)));
+  MHA_TRY(ok(mha::launch_transpose(dtype, W(pl.off_c), nv, Mq, nv, W(pl.off_ct), pl.Mq_pad,
+                                   pl.Mq_pad, stream)));
+  MHA_TRY(run_linear(D, nv, pl.Mq_pad, dtype, W(pl.off_drt), pl.Mq_pad, W(pl.off_ct), nullptr,
+                     dW_o, nv, ctx, stream));
+
+  // ---- attention backward: dQ, dK, dV into buffers laid out like the projections
+  mha::SdpaBwdArgs g;
+  g.B = B; g.H = H; g.Nq = Nq; g.Nk = Nk; g.d_k = d_k; g.d_v = d_v;
+  g.mask = mask;
+  g.window = 0;
+  g.key_len = a.key_len;
+  g.scale = a.scale;
+  g.Q = a.Q; g.K = a.K; g.V = a.V; g.O = a.O; g.dO = W(pl.off_dc);
+  g.lse = a.lse;
+  g.Dv = static_cast<float*>(W(pl.off_dvec));
+  uint8_t* dqbuf = ws + pl.off_dq;
+  uint8_t* dkvbuf = ws + pl.off_dkv;
+  g.dQ = dqbuf;
+  g.dK = self ? dqbuf + nqk * es : dkvbuf;
+  g.dV = self ? dqbuf + 2 * nqk * es : dkvbuf + nqk * es;
+  const int64_t* strs[8] = {sq, sk, sv, so, so, sq, sk, sv};
+  for (int t = 0; t < 8; ++t)
+    for (int i = 0; i < 4; ++i) g.st[t][i] = strs[t][i];
+  MHA_TRY(run_sdpa_bwd(g, dtype, ctx, stream));
+
+  // ---- projections: dx = dProj W (+ dr on the query side), dW = dProj^T x, db = colsum
+  if (self) {
+    MHA_TRY(ok(mha::launch_transpose(dtype, W_qkv, D, pl.ld_q, D, W(pl.off_wqt), pl.ld_q,
+                                     pl.ld_q, stream)));
+    MHA_TRY(run_linear(Mq, D, pl.ld_q, dtype, dqbuf, pl.ld_q, W(pl.off_wqt), nullptr, dx_q, D,
+                       ctx, stream, false, W(pl.off_dr)));
+    MHA_TRY(ok(mha::launch_transpose(dtype, dqbuf, pl.ld_q, Mq, pl.ld_q, W(pl.off_dqt),
+                                     pl.Mq_pad, pl.Mq_pad, stream)));
+    MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
+                                     stream)));
+    MHA_TRY(run_linear(pl.ld_q, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
+                       nullptr, dW_qkv, D, ctx, stream));
+    MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, pl.ld_q, Mq, pl.ld_q, part, stream)));
+    MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, pl.ld_q, pl.ld_q, db_qkv,
+                                           stream)));
+  } else {
+    uint8_t* dWb = static_cast<uint8_t*>(dW_qkv);
+    uint8_t* dbb = static_cast<uint8_t*>(db_qkv);
+    // query side
+    MHA_TRY(ok(mha::launch_transpose(dtype, W_qkv, D, nqk, D, W(pl.off_wqt), nqk, nqk,
+                                     stream)));
+    MHA_TRY(run_linear(Mq, D, nqk, dtype, dqbuf, nqk, W(pl.off_wqt), nullptr, dx_q, D, ctx,
+                       stream, false, W(pl.off_dr)));
+    MHA_TRY(ok(mha::launch_transpose(dtype, dqbuf, nqk, Mq, nqk, W(pl.off_dqt), pl.Mq_pad,
+                                     pl.Mq_pad, stream)));
+    MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
+                                     stream)));
+    MHA_TRY(run_linear(nqk, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
+                       nullptr, dWb, D, ctx, stream));
+    MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, nqk, Mq, nqk, part, stream)));
+    MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, nqk, nqk, dbb, stream)));
+    // key/value side
+    const int nch_k = mha::bwd_row_chunks(Mk);
+    MHA_TRY(ok(mha::launch_transpose(dtype, Wb + static_cast<size_t>(nqk) * D * es, D,
+                                     pl.ld_kv, D, W(pl.off_wkvt), pl.ld_kv, pl.ld_kv, stream)));
+    MHA_TRY(run_linear(Mk, D, pl.ld_kv, dtype, dkvbuf, pl.ld_kv, W(pl.off_wkvt), nullptr, dx_kv,
+                       D, ctx, stream));
+    MHA_TRY(ok(mha::launch_transpose(dtype, dkvbuf, pl.ld_kv, Mk, pl.ld_kv, W(pl.off_dkvt),
+                                     pl.Mk_pad, pl.Mk_pad, stream)));
+    MHA_TRY(ok(mha::launch_transpose(dtype, src_kv, D, Mk, D, W(pl.off_xkvt), pl.Mk_pad,
+                                     pl.Mk_pad, stream)));
+    MHA_TRY(run_linear(pl.ld_kv, D, pl.Mk_pad, dtype, W(pl.off_dkvt), pl.Mk_pad, W(pl.off_xkvt),
+                       nullptr, dWb + static_cast<size_t>(nqk) * D * es, D, ctx, stream));
+    MHA_TRY(ok(mha::launch_colsum_partials(dtype, dkvbuf, pl.ld_kv, Mk, pl.ld_kv, part,
+                                           stream)));
+    MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_k, pl.ld_kv, pl.ld_kv,
+                                           dbb + nqk * es, stream)));
+  }
+#undef MHA_TRY
+  return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mha_layer_bwd_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d_v,
+                                 int dtype, int self_attention, size_t* bytes) {
+  if (bytes == nullptr) return MHA_ERR_INVALID;
+  const int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
+  if (st != MHA_OK) return st;
+  if (self_attention && Nq != Nk) return MHA_ERR_INVALID;
+  *bytes = plan_layer_bwd(B, H, Nq, Nk, D, d_k, d_v, dtype, self_attention != 0).total;
+  return MHA_OK;
+}
+
+int mha_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                  const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                  const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                  const void* gamma, const void* beta, const void* dy, void* dx_q, void* dx_kv,
+                  void* dW_qkv, void* db_qkv, void* dW_o, void* db_o, void* dgamma, void* dbeta,
+                  void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  (void)beta;  // the output shift does not enter any gradient
+  return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
+                        W_qkv, b_qkv, W_o, b_o, gamma, dy, dx_q, dx_kv, dW_qkv, db_qkv, dW_o,
+                        db_o, dgamma, dbeta, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

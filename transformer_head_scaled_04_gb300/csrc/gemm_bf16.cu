@@ -50,7 +50,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
                           const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ Y,
-                          int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns) {
+                          int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns,
+                          const __nv_bfloat16* __restrict__ R) {
   using S = GemmShape<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -195,6 +196,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) bv[i] = 0.f;
           }
+          if (R != nullptr) {  // a residual matrix with Y's layout joins the bias
+            const uint4* rp = reinterpret_cast<const uint4*>(R + static_cast<int64_t>(row) * ldy + col);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 u = rp[v];
+              const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float2 f = __bfloat1622float2(hv[e]);
+                bv[v * 8 + e * 2] += f.x;
+                bv[v * 8 + e * 2 + 1] += f.y;
+              }
+            }
+          }
           uint4 out[4];
           uint32_t* o32 = reinterpret_cast<uint32_t*>(out);
 #pragma unroll
@@ -229,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool kRelu>
 cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void* bias, void* Y,
-                      int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+                      int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
+                      const void* R) {
   using S = GemmShape<BN>;
   auto kern = gemm_bias_bf16_kernel<BN, kRelu>;
   cudaError_t e =
@@ -239,7 +255,8 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
   kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW, static_cast<const __nv_bfloat16*>(bias),
                                              static_cast<__nv_bfloat16*>(Y), M, N, K, ldy,
-                                             ctx.status, ctx.timeout_ns);
+                                             ctx.status, ctx.timeout_ns,
+                                             static_cast<const __nv_bfloat16*>(R));
   return cudaGetLastError();
 }
 
@@ -247,13 +264,13 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
 
 cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
-                             int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+                             int64_t ldy, const DevCtx& ctx, cudaStream_t s, const void* R) {
   if (relu) {
-    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
-    return launch_bn<128, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
+    return launch_bn<128, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
   }
-  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
-  return launch_bn<128, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s);
+  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
+  return launch_bn<128, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
 }
 
 }  // namespace mha

@@ -15,7 +15,7 @@ constexpr int kKT = 16;
 __global__ void __launch_bounds__(256)
     gemm_f32_kernel(const float* __restrict__ X, int64_t ldx, const float* __restrict__ W,
                     const float* __restrict__ bias, bool relu, float* __restrict__ Y,
-                    int64_t ldy, int M, int N, int K) {
+                    int64_t ldy, int M, int N, int K, const float* __restrict__ R) {
   __shared__ float sx[kKT][kT + 4];
   __shared__ float sw[kKT][kT + 4];
   const int tx = threadIdx.x & 15;  // column group
@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(256)
     for (int jn = 0; jn < 4; ++jn) {
       const int gn = n0 + tx * 4 + jn;
       if (gn >= N) continue;
-      const float v = acc[i][jn] + (bias ? bias[gn] : 0.f);
+      const float v = acc[i][jn] + (bias ? bias[gn] : 0.f) +
+                      (R ? R[static_cast<int64_t>(gm) * ldy + gn] : 0.f);
       Y[static_cast<int64_t>(gm) * ldy + gn] = relu ? fmaxf(v, 0.f) : v;
     }
   }
@@ -65,9 +66,9 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
                             bool relu, float* Y, int64_t ldy, int M, int N, int K,
-                            cudaStream_t s) {
+                            cudaStream_t s, const float* R) {
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
-  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, W, bias, relu, Y, ldy, M, N, K);
+  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, W, bias, relu, Y, ldy, M, N, K, R);
   return cudaGetLastError();
 }
 

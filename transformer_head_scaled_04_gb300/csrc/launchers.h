@@ -18,12 +18,14 @@ struct DevCtx {
 // ---- projections: Y[M,N] = act(X[M,K] W[N,K]^T + bias), act = identity or ReLU (relu)
 // bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W
 // {K, N}, box {64, block_n}; both 128-byte swizzled.  block_n is 128 or 256.
+// residual: optional R [M, N] with Y's row pitch, added in the epilogue (Y = XW^T + b + R)
 cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
-                             int64_t ldy, const DevCtx& ctx, cudaStream_t s);
+                             int64_t ldy, const DevCtx& ctx, cudaStream_t s,
+                             const void* residual = nullptr);
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
                             bool relu, float* Y, int64_t ldy, int M, int N, int K,
-                            cudaStream_t s);
+                            cudaStream_t s, const float* residual = nullptr);
 
 // ---- attention
 // Mask kinds beyond the public mha_mask values: restricted self-attention, where query i
@@ -89,6 +91,23 @@ cudaError_t launch_sdpa_bwd_f32(const SdpaBwdArgs& a, cudaStream_t s);
 cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmG,
                                  const SdpaBwdArgs& a, const DevCtx& ctx, cudaStream_t s);
+
+// ---- memory-bound steps of the sublayer backward (bwd_util.cu)
+int bwd_row_chunks(int M);  // chunks of rows the partial column sums use
+// dr = LayerNorm backward at r = x + a (one warp per row; stats[row] = (mean, rstd)), then
+// part[(chunk * 3 + k) * D + col] = per-chunk sums of dy * rhat, dy, dr
+cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void* x,
+                                 const void* a, const void* gamma, const void* dy, void* dr,
+                                 float2* stats, float* part, cudaStream_t s);
+// part[chunk * N + col] = per-chunk column sums of X [M, N] (row pitch ld)
+cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, int N,
+                                   float* part, cudaStream_t s);
+// out[col] = sum over chunks of part[chunk * chunk_stride + col], in chunk order
+cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
+                                   int64_t chunk_stride, int N, void* out, cudaStream_t s);
+// Y [C, R_pad] (row pitch ldy) = X [R, C]^T (row pitch ldx), zero for rows R..R_pad
+cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C, void* Y,
+                             int64_t ldy, int R_pad, cudaStream_t s);
 
 // ---- residual + LayerNorm: y = LN(x + a) * gamma + beta
 cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,
