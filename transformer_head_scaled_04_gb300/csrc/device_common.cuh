@@ -33,6 +33,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// The dynamic shared-memory window rounded up to a 1024-byte boundary (the 128-byte swizzle
+// atoms of the TMA tiles and MMA operands).  Offsetting the __shared__ array itself, rather
+// than going through an integer, keeps the pointer in the shared state space for the
+// compiler, so C++ loads and stores through it become plain shared-memory accesses.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -75,6 +75,56 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t* r0
   }
 }
 
+// dS of one 64-key half of a query row: p = 2^(s*c - lse2) (0 past the row's last key when
+// kMask), dS = p * (dP - D), packed to bf16 pairs
+template <bool kMask>
+__device__ __forceinline__ void dq_half(const uint32_t* s0, const uint32_t* s1,
+                                        const uint32_t* g0, const uint32_t* g1, int col0,
+                                        int limit, float c, float lse2, float Dr, uint32_t* ds) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
+    const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
+    const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
+    const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
+    float pa = ex2_approx(fmaf(sa, c, -lse2));
+    float pb = ex2_approx(fmaf(sb, c, -lse2));
+    if (kMask) {
+      if (col0 + 2 * i > limit) pa = 0.f;
+      if (col0 + 2 * i + 1 > limit) pb = 0.f;
+    }
+    ds[i] = pack_bf16x2(pa * (ga - Dr), pb * (gb - Dr));
+  }
+}
+
+// P^T and dS^T of one 64-query half of a key row; st: this query tile's lse2 [128] then
+// D [128] in shared memory, ca0 the half's first query column.  kMask: query q0 + ca sees
+// this key only when ca >= first_ok (causal) and the key is below the key limit (row_ok).
+template <bool kMask>
+__device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1,
+                                          const uint32_t* g0, const uint32_t* g1,
+                                          const float* st, int ca0, bool row_ok, int first_ok,
+                                          float c, uint32_t* pp, uint32_t* ds) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int ca = ca0 + 2 * i;  // query column within the tile
+    const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
+    const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
+    const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
+    const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
+    const float2 l2 = *reinterpret_cast<const float2*>(st + ca);
+    const float2 dd = *reinterpret_cast<const float2*>(st + kT + ca);
+    float pa = ex2_approx(fmaf(sa, c, -l2.x));
+    float pb = ex2_approx(fmaf(sb, c, -l2.y));
+    if (kMask) {
+      if (!row_ok || ca < first_ok) pa = 0.f;
+      if (!row_ok || ca + 1 < first_ok) pb = 0.f;
+    }
+    pp[i] = pack_bf16x2(pa, pb);
+    ds[i] = pack_bf16x2(pa * (ga - dd.x), pb * (gb - dd.y));
+  }
+}
+
 // ============================================================================ dq kernel
 // smem: Q, dO (once), K ring, V ring, barriers
 constexpr int kQOffQ = 0;
@@ -102,8 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kQNumBars);
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -174,14 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idQ = idesc_bf16_f32(kT, kHD, false, true);
       const uint64_t dQd = smem_desc_sw128(smem_u32(smem + kQOffQ), 1024, 1024);
       const uint64_t dGd = smem_desc_sw128(smem_u32(smem + kQOffG), 1024, 1024);
-      bool ok = mbar_wait(bar(kQBarIn), 0, p.timeout_ns);
-      for (int j = 0; ok && j < nk; ++j) {
+      // S_j = Q K_j^T and dP_j = dO V_j^T into the single S/dP buffer
+      auto issue_s = [&](int j) -> bool {
         const int s = j % kStages;
-        if (!mbar_wait(bar(kQBarKV + s), (j / kStages) & 1, p.timeout_ns) ||
-            (j > 0 && !mbar_wait(bar(kQBarSFree), (j - 1) & 1, p.timeout_ns))) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(bar(kQBarKV + s), (j / kStages) & 1, p.timeout_ns)) return false;
         tc_fence_after();
         const uint64_t dK = smem_desc_sw128(smem_u32(smem + kQOffK + s * kTileBytes), 1024, 1024);
         const uint64_t dV = smem_desc_sw128(smem_u32(smem + kQOffV + s * kTileBytes), 1024, 1024);
@@ -191,11 +236,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kQColP, dGd + kk * 2, dV + kk * 2, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kQBarSFull));
+        return true;
+      };
+      bool ok = mbar_wait(bar(kQBarIn), 0, p.timeout_ns) && issue_s(0);
+      for (int j = 0; ok && j < nk; ++j) {
+        const int s = j % kStages;
+        // once the math warps hold S_j and dP_j in registers the next tile's products run
+        // while they turn them into dS_j
+        if (j + 1 < nk &&
+            (!mbar_wait(bar(kQBarSFree), j & 1, p.timeout_ns) || !issue_s(j + 1))) {
+          ok = false;
+          break;
+        }
         if (!mbar_wait(bar(kQBarDSFull), j & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint64_t dK = smem_desc_sw128(smem_u32(smem + kQOffK + s * kTileBytes), 1024, 1024);
         // dQ += dS K_j: 16 keys (8 TMEM columns of dS, 16 K rows) per MMA
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
@@ -245,16 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int col0 = j * kT + half * 64;
         uint32_t ds[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
-          float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
-          const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
-          const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
-          const float pa = (col0 + 2 * i <= limit) ? ex2_approx(fmaf(sa, c, -lse2)) : 0.f;
-          const float pb = (col0 + 2 * i + 1 <= limit) ? ex2_approx(fmaf(sb, c, -lse2)) : 0.f;
-          ds[i] = pack_bf16x2(pa * (ga - Dr), pb * (gb - Dr));
-        }
+        if (warp_all(col0 + 63 <= limit))  // no key of this half is masked for any row here
+          dq_half<false>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
+        else
+          dq_half<true>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
         // the previous dQ product must have read dS before it is overwritten
         if (half == 0 && j > 0 &&
             !warp_all(mbar_wait(bar(kQBarDQDone), (j - 1) & 1, p.timeout_ns))) {
@@ -327,8 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKNumBars);
   float* sstat = reinterpret_cast<float*>(smem + kKOffStat);
@@ -419,14 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idO = idesc_bf16_f32(kT, kHD, false, true);
       const uint64_t dKd = smem_desc_sw128(smem_u32(smem + kKOffK), 1024, 1024);
       const uint64_t dVd = smem_desc_sw128(smem_u32(smem + kKOffV), 1024, 1024);
-      bool ok = mbar_wait(bar(kKBarIn), 0, p.timeout_ns);
-      for (int t = 0; ok && t < ni; ++t) {
+      // S^T_t = K Q_t^T and dP^T_t = V dO_t^T into the single S/dP buffer
+      auto issue_s = [&](int t) -> bool {
         const int s = t % kStages;
-        if (!mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns) ||
-            (t > 0 && !mbar_wait(bar(kKBarSFree), (t - 1) & 1, p.timeout_ns))) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns)) return false;
         tc_fence_after();
         const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kKOffQ + s * kTileBytes), 1024, 1024);
         const uint64_t dG = smem_desc_sw128(smem_u32(smem + kKOffG + s * kTileBytes), 1024, 1024);
@@ -436,12 +483,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kKColP, dVd + kk * 2, dG + kk * 2, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kKBarSFull));
+        return true;
+      };
+      bool ok = mbar_wait(bar(kKBarIn), 0, p.timeout_ns) && issue_s(0);
+      for (int t = 0; ok && t < ni; ++t) {
+        const int s = t % kStages;
+        // once the math warps hold S^T_t and dP^T_t in registers the next tile's products run
+        // while they turn them into P^T_t and dS^T_t
+        if (t + 1 < ni &&
+            (!mbar_wait(bar(kKBarSFree), t & 1, p.timeout_ns) || !issue_s(t + 1))) {
+          ok = false;
+          break;
+        }
         if (!mbar_wait(bar(kKBarPFull), t & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // dV += P^T dO_i and dK += dS^T Q_i: 16 queries (8 TMEM columns, 16 smem rows) per MMA
+        const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kKOffQ + s * kTileBytes), 1024, 1024);
+        const uint64_t dG = smem_desc_sw128(smem_u32(smem + kKOffG + s * kTileBytes), 1024, 1024);
+        // dV += P^T dO_t and dK += dS^T Q_t: 16 queries (8 TMEM columns, 16 smem rows) per MMA
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk) {
           mma_bf16_ts(tmem + kKColDV, tmem + kKColPT + kk * 8, dG + kk * ((16 * 128) >> 4), idO,
@@ -490,21 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar(kKBarSFree));
         }
         uint32_t pp[32], ds[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int ca = half * 64 + 2 * i;  // query column within the tile
-          const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
-          const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
-          const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
-          const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
-          // key j = key may be seen by query q0 + ca: j < L, and j <= q for the causal mask
-          const bool oka = key < L && (p.mask != 1 || key <= q0 + ca);
-          const bool okb = key < L && (p.mask != 1 || key <= q0 + ca + 1);
-          const float pa = oka ? ex2_approx(fmaf(sa, c, -st[ca])) : 0.f;
-          const float pb = okb ? ex2_approx(fmaf(sb, c, -st[ca + 1])) : 0.f;
-          pp[i] = pack_bf16x2(pa, pb);
-          ds[i] = pack_bf16x2(pa * (ga - st[kT + ca]), pb * (gb - st[kT + ca + 1]));
-        }
+        // key j = key is seen by query q0 + ca when j < L and, for the causal mask, j <= q
+        const bool row_ok = key < L;
+        const int first_ok = (p.mask == 1) ? key - q0 : -kT;
+        if (warp_all(row_ok && first_ok <= half * 64))  // every pair of this half is allowed
+          dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
+        else
+          dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
         // the previous dV/dK products must have read P^T and dS^T before they change
         if (half == 0 && t > 0 &&
             !warp_all(mbar_wait(bar(kKBarPVDone), (t - 1) & 1, p.timeout_ns))) {
