@@ -475,7 +475,7 @@ int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, 
 int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes) {
   if (bytes == nullptr || B < 1 || H < 1 || Nq < 1 || !valid_dtype(dtype))
     return MHA_ERR_INVALID;
-  *bytes = round_up(static_cast<size_t>(B) * H * Nq * sizeof(float), 256);  // D = rowsum(dO O)
+  *bytes = round_up(mha::sdpa_bwd_scratch_bytes(B, H, Nq, dtype), 256);  // D (and lse) per row
   return MHA_OK;
 }
 
@@ -926,7 +926,7 @@ LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_
   p.off_c = take(static_cast<size_t>(p.Mq) * p.nv * es);
   p.off_a = take(static_cast<size_t>(p.Mq) * D * es);
   p.off_lse = take(static_cast<size_t>(B) * H * Nq * 4);
-  p.off_dvec = take(static_cast<size_t>(B) * H * Nq * 4);
+  p.off_dvec = take(mha::sdpa_bwd_scratch_bytes(B, H, Nq, dtype));
   p.off_stats = take(static_cast<size_t>(p.Mq) * 8);
   p.off_part = take(static_cast<size_t>(nchunk) * part_cols * 4);
   p.off_dr = take(static_cast<size_t>(p.Mq) * D * es);

@@ -81,11 +81,20 @@ struct SdpaBwdArgs {
   float scale;
   const void *Q, *K, *V, *O, *dO;
   const float* lse;          // [B, H, Nq] natural-log softmax denominators
-  float* Dv;                 // [B, H, Nq] scratch: rowsum(dO * O)
+  // scratch written by launch_sdpa_bwd_rowdot from O, dO and lse: fp32 path, D_i =
+  // rowsum(dO * O) as [B, H, Nq]; bf16 path, per 128-row query tile of every (b, h) the
+  // tile's lse * log2(e) [128] then its D [128] (rows past Nq: +inf and 0), so one 1 KB bulk
+  // copy brings a tile's statistics into shared memory
+  float* Dv;
   void *dQ, *dK, *dV;
   int64_t st[8][4];          // element strides b, h, n, d of Q, K, V, O, dO, dQ, dK, dV
 };
 cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s);
+// bytes of the Dv scratch above
+inline size_t sdpa_bwd_scratch_bytes(int B, int H, int Nq, int dtype) {
+  return dtype == 1 ? static_cast<size_t>(B) * H * ((Nq + 127) / 128) * 1024
+                    : static_cast<size_t>(B) * H * Nq * 4;
+}
 cudaError_t launch_sdpa_bwd_f32(const SdpaBwdArgs& a, cudaStream_t s);
 // bf16 (d = 64): Q, K, V, dO through 4-D TMA maps {64, n, h, b}, box {64, 128, 1, 1}
 cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,

@@ -5,7 +5,8 @@
 // translation, 3.2.1 缩放点积注意力).  The softmax weights are rebuilt tile by tile from the
 // forward's log-sum-exp (P = 2^(s*c - lse2), c = scale*log2 e, lse2 = lse*log2 e), so the
 // n x n matrices never leave the SM:
-//   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_d dO_id O_id   (D from a small prior launch)
+//   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_d dO_id O_id
+// (a small prior launch writes D and lse * log2 e per 128-row query tile, 1 KB per tile)
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO
 // Two kernels, neither with atomics:
 //   dq   -- one CTA per 128-row query tile; K/V tiles stream through a TMA ring.
@@ -16,7 +17,8 @@
 //           S^T = K Q^T and dP^T = V dO^T; the math warps (one key row per thread) write bf16
 //           P^T and dS^T into TMEM; dV += P^T dO and dK += dS^T Q accumulate in TMEM
 //           (all 512 columns: S^T, dP^T, P^T, dS^T, dV, dK).
-// Warps: 0-3 math, 4 TMA producer, 5 TMEM owner and MMA issuer.  Every wait is bounded; a
+// Warps: 0-7 math (two per sub-partition: warps w and w+4 share TMEM lanes 32*(w%4).. and
+// take the two 64-column halves of every tile), 8 TMA producer, 9 TMEM owner and MMA issuer.  Every wait is bounded; a
 // timeout records MHA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM.
 // Masks: none, causal (j <= i) and key padding (j < key_len[b]); fully masked tiles are
 // skipped, and the d = 64 heads of the forward kernel are assumed.
@@ -34,7 +36,10 @@ constexpr int kT = 128;                    // rows per tile (queries or keys)
 constexpr int kHD = 64;                    // head dim
 constexpr int kTileBytes = kT * kHD * 2;   // 16 KB
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kMathWarps = 8;               // warp w: rows 32*(w%4).. of the tile, column half w/4
+constexpr int kWarpProducer = kMathWarps;   // TMA
+constexpr int kWarpMma = kMathWarps + 1;    // TMEM owner and MMA issuer
+constexpr int kThreads = (kMathWarps + 2) * 32;
 constexpr int kErrTimeout = -6;
 enum : int { kSiteBwdProducer = 41, kSiteBwdMma = 42, kSiteBwdMath = 43, kSiteBwdEpi = 44 };
 constexpr float kLog2e = 1.4426950408889634f;
@@ -43,8 +48,7 @@ struct BwdParams {
   int H, Nq, Nk, mask;
   const int32_t* key_len;
   float scale;       // multiplies q.k
-  const float* lse;  // [B, H, Nq]
-  const float* Dv;   // [B, H, Nq]
+  const float* stats;  // per (b, h, 128-row query tile): lse * log2 e [128], then D [128]
   __nv_bfloat16* out0;  // dq: dQ; dkdv: dK
   __nv_bfloat16* out1;  // dkdv: dV
   int64_t o0_b, o0_h, o0_n, o1_b, o1_h, o1_n;
@@ -125,6 +129,22 @@ __device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1
   }
 }
 
+// store 32 fp32 values (times mul) of half a row as bf16
+__device__ __forceinline__ void store_half_row(__nv_bfloat16* dst, const uint32_t* r,
+                                               float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t* q = r + 8 * u;
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(q[0]) * mul, __uint_as_float(q[1]) * mul);
+    v.y = pack_bf16x2(__uint_as_float(q[2]) * mul, __uint_as_float(q[3]) * mul);
+    v.z = pack_bf16x2(__uint_as_float(q[4]) * mul, __uint_as_float(q[5]) * mul);
+    v.w = pack_bf16x2(__uint_as_float(q[6]) * mul, __uint_as_float(q[7]) * mul);
+    d4[u] = v;
+  }
+}
+
 // ============================================================================ dq kernel
 // smem: Q, dO (once), K ring, V ring, barriers
 constexpr int kQOffQ = 0;
@@ -140,8 +160,8 @@ constexpr int kQBarIn = 0;                     // Q, dO landed
 constexpr int kQBarKV = 1;                     // [kStages] K_j, V_j landed
 constexpr int kQBarKVEmpty = kQBarKV + kStages;  // [kStages] MMAs done with K_j, V_j
 constexpr int kQBarSFull = kQBarKVEmpty + kStages;
-constexpr int kQBarSFree = kQBarSFull + 1;   // math warps read S, dP (count 4)
-constexpr int kQBarDSFull = kQBarSFree + 1;  // math warps wrote dS (count 4)
+constexpr int kQBarSFree = kQBarSFull + 1;   // every math warp holds its S, dP half
+constexpr int kQBarDSFull = kQBarSFree + 1;  // every math warp wrote its dS half
 constexpr int kQBarDQDone = kQBarDSFull + 1; // dQ MMA done with dS
 constexpr int kQBarDrain = kQBarDQDone + 1;
 constexpr int kQNumBars = kQBarDrain + 1;
@@ -171,13 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kQBarKVEmpty + s), 1);
     }
     mbar_init(bar(kQBarSFull), 1);
-    mbar_init(bar(kQBarSFree), 4);
-    mbar_init(bar(kQBarDSFull), 4);
+    mbar_init(bar(kQBarSFree), kMathWarps);
+    mbar_init(bar(kQBarDSFull), kMathWarps);
     mbar_init(bar(kQBarDQDone), 1);
     mbar_init(bar(kQBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -186,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && nk > 0) {
       prefetch_tmap(&tmQ);
@@ -216,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
         (void)mbar_wait(bar(kQBarKV + i % kStages), (i / kStages) & 1, p.timeout_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nk > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
@@ -268,13 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ math warps
-    const int r_local = warp * 32 + lane;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r_local = quarter * 32 + lane;
     const int row = q0 + r_local;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int64_t stat = (static_cast<int64_t>(b) * p.H + h) * p.Nq + row;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool live = row < p.Nq;
-    const float lse2 = live ? __ldg(p.lse + stat) * kLog2e : INFINITY;
-    const float Dr = live ? __ldg(p.Dv + stat) : 0.f;
+    const float* tile_st =
+        p.stats + ((static_cast<int64_t>(b) * p.H + h) * gridDim.x + qt) * (2 * kT);
+    const float lse2 = __ldg(tile_st + r_local);  // +inf past Nq
+    const float Dr = __ldg(tile_st + kT + r_local);
     const float c = p.scale * kLog2e;
     const int limit = (p.mask == 1) ? min(row, L - 1) : L - 1;  // keys j <= limit
     bool ok = true;
@@ -285,67 +307,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s0[32], s1[32], g0[32], g1[32];
-        tmem_ld32(tmem + kQColS + lane_off + half * 64, s0);
-        tmem_ld32(tmem + kQColS + lane_off + half * 64 + 32, s1);
-        tmem_ld32(tmem + kQColP + lane_off + half * 64, g0);
-        tmem_ld32(tmem + kQColP + lane_off + half * 64 + 32, g1);
-        tmem_wait_ld();
-        reg_fence(s0);
-        reg_fence(s1);
-        reg_fence(g0);
-        reg_fence(g1);
-        if (half == 1) {  // S and dP of this tile are in registers: the next products may run
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kQBarSFree));
-        }
-        const int col0 = j * kT + half * 64;
-        uint32_t ds[32];
-        if (warp_all(col0 + 63 <= limit))  // no key of this half is masked for any row here
-          dq_half<false>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
-        else
-          dq_half<true>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
-        // the previous dQ product must have read dS before it is overwritten
-        if (half == 0 && j > 0 &&
-            !warp_all(mbar_wait(bar(kQBarDQDone), (j - 1) & 1, p.timeout_ns))) {
-          record_error(p.status, kErrTimeout, kSiteBwdMath);
-          ok = false;
-          break;
-        }
-        tmem_st32(tmem + kQColDS + lane_off + half * 32, ds);
+      uint32_t s0[32], s1[32], g0[32], g1[32];
+      tmem_ld32(tmem + kQColS + lane_off + half * 64, s0);
+      tmem_ld32(tmem + kQColS + lane_off + half * 64 + 32, s1);
+      tmem_ld32(tmem + kQColP + lane_off + half * 64, g0);
+      tmem_ld32(tmem + kQColP + lane_off + half * 64 + 32, g1);
+      tmem_wait_ld();
+      reg_fence(s0);
+      reg_fence(s1);
+      reg_fence(g0);
+      reg_fence(g1);
+      // S and dP of this half are in registers: the next tile's products may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQBarSFree));
+      const int col0 = j * kT + half * 64;
+      uint32_t ds[32];
+      if (warp_all(col0 + 63 <= limit))  // no key of this half is masked for any row here
+        dq_half<false>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
+      else
+        dq_half<true>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
+      // the previous dQ product must have read dS before it is overwritten
+      if (j > 0 && !warp_all(mbar_wait(bar(kQBarDQDone), (j - 1) & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
       }
-      if (!ok) break;
+      tmem_st32(tmem + kQColDS + lane_off + half * 32, ds);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kQBarDSFull));
     }
-    // ---- epilogue: dQ * scale -> bf16
-    if (ok && nk > 0 && warp_all(mbar_wait(bar(kQBarDQDone), (nk - 1) & 1, p.timeout_ns))) {
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + kQColDQ + lane_off, r0);
-      tmem_ld32(tmem + kQColDQ + lane_off + 32, r1);
-      tmem_wait_ld();
-      reg_fence(r0);
-      reg_fence(r1);
-      if (live)
-        store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(row) * p.o0_n, r0, r1,
-                  p.scale);
-    } else if (live) {
-      uint32_t z[32];
+    // ---- epilogue: dQ * scale -> bf16, 32 of the 64 columns per warp
+    __nv_bfloat16* dst =
+        p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(row) * p.o0_n + half * 32;
+    uint32_t r0[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = 0u;
-      if (ok && nk > 0) record_error(p.status, kErrTimeout, kSiteBwdEpi);
-      store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(row) * p.o0_n, z, z,
-                0.f);
+    for (int i = 0; i < 32; ++i) r0[i] = 0u;
+    if (ok && nk > 0) {
+      if (warp_all(mbar_wait(bar(kQBarDQDone), (nk - 1) & 1, p.timeout_ns))) {
+        tc_fence_after();
+        tmem_ld32(tmem + kQColDQ + lane_off + half * 32, r0);
+        tmem_wait_ld();
+        reg_fence(r0);
+      } else {
+        record_error(p.status, kErrTimeout, kSiteBwdEpi);
+      }
     }
+    if (live) store_half_row(dst, r0, p.scale);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -367,8 +381,8 @@ constexpr int kKBarIn = 0;                        // K, V landed
 constexpr int kKBarQ = 1;                         // [kStages] Q_i, dO_i, lse, D landed
 constexpr int kKBarQEmpty = kKBarQ + kStages;     // [kStages] MMAs done with Q_i, dO_i
 constexpr int kKBarSFull = kKBarQEmpty + kStages;
-constexpr int kKBarSFree = kKBarSFull + 1;        // count 4
-constexpr int kKBarPFull = kKBarSFree + 1;        // count 4
+constexpr int kKBarSFree = kKBarSFull + 1;        // every math warp holds its S^T, dP^T half
+constexpr int kKBarPFull = kKBarSFree + 1;        // every math warp wrote its P^T, dS^T half
 constexpr int kKBarPVDone = kKBarPFull + 1;
 constexpr int kKBarDrain = kKBarPVDone + 1;
 constexpr int kKNumBars = kKBarDrain + 1;
@@ -401,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kKBarQEmpty + s), 1);
     }
     mbar_init(bar(kKBarSFull), 1);
-    mbar_init(bar(kKBarSFree), 4);
-    mbar_init(bar(kKBarPFull), 4);
+    mbar_init(bar(kKBarSFree), kMathWarps);
+    mbar_init(bar(kKBarPFull), kMathWarps);
     mbar_init(bar(kKBarPVDone), 1);
     mbar_init(bar(kKBarDrain), 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -415,55 +429,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int64_t stat0 = (static_cast<int64_t>(b) * p.H + h) * p.Nq;
 
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer (TMA + stats)
-    bool ok = true;
-    int issued = 0;
-    if (ni > 0) {
-      if (lane == 0) {
-        prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
-        prefetch_tmap(&tmG);
-        mbar_arrive_expect_tx(bar(kKBarIn), 2 * kTileBytes);
-        tma_load_4d(smem_u32(smem + kKOffK), &tmK, bar(kKBarIn), 0, k0, h, b);
-        tma_load_4d(smem_u32(smem + kKOffV), &tmV, bar(kKBarIn), 0, k0, h, b);
-      }
+    if (lane == 0 && ni > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmG);
+      mbar_arrive_expect_tx(bar(kKBarIn), 2 * kTileBytes);
+      tma_load_4d(smem_u32(smem + kKOffK), &tmK, bar(kKBarIn), 0, k0, h, b);
+      tma_load_4d(smem_u32(smem + kKOffV), &tmV, bar(kKBarIn), 0, k0, h, b);
+      const float* st_bh = p.stats + (static_cast<int64_t>(b) * p.H + h) * nqt * (2 * kT);
+      bool ok = true;
+      int issued = 0;
       for (int t = 0; t < ni; ++t) {
         const int s = t % kStages;
-        const int q0 = (i0 + t) * kT;
-        if (!warp_all(mbar_wait_backoff(bar(kKBarQEmpty + s), ((t / kStages) & 1) ^ 1,
-                                        p.timeout_ns))) {
+        const int qt = i0 + t;
+        if (!mbar_wait_backoff(bar(kKBarQEmpty + s), ((t / kStages) & 1) ^ 1, p.timeout_ns)) {
           ok = false;
           break;
         }
-        // this tile's lse (in log2 units) and D; rows past Nq see nothing (lse2 = +inf)
-        float* st = sstat + s * 2 * kT;
-        for (int r = lane; r < kT; r += 32) {
-          const bool live = q0 + r < p.Nq;
-          st[r] = live ? __ldg(p.lse + stat0 + q0 + r) * kLog2e : INFINITY;
-          st[kT + r] = live ? __ldg(p.Dv + stat0 + q0 + r) : 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes);
-          tma_load_4d(smem_u32(smem + kKOffQ + s * kTileBytes), &tmQ, bar(kKBarQ + s), 0, q0, h,
-                      b);
-          tma_load_4d(smem_u32(smem + kKOffG + s * kTileBytes), &tmG, bar(kKBarQ + s), 0, q0, h,
-                      b);
-        }
+        // Q_t, dO_t and the tile's statistics (lse2 and D, 1 KB) on one barrier
+        mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes + 2 * kT * 4);
+        tma_load_4d(smem_u32(smem + kKOffQ + s * kTileBytes), &tmQ, bar(kKBarQ + s), 0, qt * kT,
+                    h, b);
+        tma_load_4d(smem_u32(smem + kKOffG + s * kTileBytes), &tmG, bar(kKBarQ + s), 0, qt * kT,
+                    h, b);
+        bulk_load(smem_u32(sstat + s * 2 * kT), st_bh + qt * (2 * kT), 2 * kT * 4,
+                  bar(kKBarQ + s));
         issued = t + 1;
       }
-      if (lane == 0) {
-        if (!ok) record_error(p.status, kErrTimeout, kSiteBwdProducer);
-        (void)mbar_wait(bar(kKBarIn), 0, p.timeout_ns);
-        for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-          (void)mbar_wait(bar(kKBarQ + i % kStages), (i / kStages) & 1, p.timeout_ns);
-      }
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdProducer);
+      (void)mbar_wait(bar(kKBarIn), 0, p.timeout_ns);
+      for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        (void)mbar_wait(bar(kKBarQ + i % kStages), (i / kStages) & 1, p.timeout_ns);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && ni > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
@@ -519,9 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ math warps (one key row each)
-    const int r_local = warp * 32 + lane;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r_local = quarter * 32 + lane;
     const int key = k0 + r_local;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale * kLog2e;
     bool ok = true;
     for (int t = 0; t < ni; ++t) {
@@ -533,78 +536,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float* st = sstat + s * 2 * kT;
-      for (int half = 0; half < 2; ++half) {
-        uint32_t s0[32], s1[32], g0[32], g1[32];
-        tmem_ld32(tmem + kKColS + lane_off + half * 64, s0);
-        tmem_ld32(tmem + kKColS + lane_off + half * 64 + 32, s1);
-        tmem_ld32(tmem + kKColP + lane_off + half * 64, g0);
-        tmem_ld32(tmem + kKColP + lane_off + half * 64 + 32, g1);
-        tmem_wait_ld();
-        reg_fence(s0);
-        reg_fence(s1);
-        reg_fence(g0);
-        reg_fence(g1);
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kKBarSFree));
-        }
-        uint32_t pp[32], ds[32];
-        // key j = key is seen by query q0 + ca when j < L and, for the causal mask, j <= q
-        const bool row_ok = key < L;
-        const int first_ok = (p.mask == 1) ? key - q0 : -kT;
-        if (warp_all(row_ok && first_ok <= half * 64))  // every pair of this half is allowed
-          dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
-        else
-          dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
-        // the previous dV/dK products must have read P^T and dS^T before they change
-        if (half == 0 && t > 0 &&
-            !warp_all(mbar_wait(bar(kKBarPVDone), (t - 1) & 1, p.timeout_ns))) {
-          record_error(p.status, kErrTimeout, kSiteBwdMath);
-          ok = false;
-          break;
-        }
-        tmem_st32(tmem + kKColPT + lane_off + half * 32, pp);
-        tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
+      // the statistics came by bulk copy on the Q_t barrier: observe its completion here too
+      // (it completed before S^T_t was issued) so their bytes are visible to these threads
+      if (!warp_all(mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
       }
-      if (!ok) break;
+      const float* st = sstat + s * 2 * kT;
+      uint32_t s0[32], s1[32], g0[32], g1[32];
+      tmem_ld32(tmem + kKColS + lane_off + half * 64, s0);
+      tmem_ld32(tmem + kKColS + lane_off + half * 64 + 32, s1);
+      tmem_ld32(tmem + kKColP + lane_off + half * 64, g0);
+      tmem_ld32(tmem + kKColP + lane_off + half * 64 + 32, g1);
+      tmem_wait_ld();
+      reg_fence(s0);
+      reg_fence(s1);
+      reg_fence(g0);
+      reg_fence(g1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kKBarSFree));
+      uint32_t pp[32], ds[32];
+      // key j = key is seen by query q0 + ca when j < L and, for the causal mask, j <= q
+      const bool row_ok = key < L;
+      const int first_ok = (p.mask == 1) ? key - q0 : -kT;
+      if (warp_all(row_ok && first_ok <= half * 64))  // every pair of this half is allowed
+        dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
+      else
+        dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
+      // the previous dV/dK products must have read P^T and dS^T before they change
+      if (t > 0 && !warp_all(mbar_wait(bar(kKBarPVDone), (t - 1) & 1, p.timeout_ns))) {
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
+      }
+      tmem_st32(tmem + kKColPT + lane_off + half * 32, pp);
+      tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kKBarPFull));
     }
-    // ---- epilogue: dK * scale, dV -> bf16 (zeros for keys no query sees)
+    // ---- epilogue: warps of half 0 write dK * scale, those of half 1 dV, as bf16 (zeros for
+    // keys no query sees)
     const bool live = key < p.Nk;
-    uint32_t a0[32], a1[32], v0[32], v1[32];
+    uint32_t a0[32], a1[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) a0[i] = a1[i] = v0[i] = v1[i] = 0u;
+    for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0u;
+    const uint32_t col = half == 0 ? kKColDK : kKColDV;
     if (ok && ni > 0) {
       if (warp_all(mbar_wait(bar(kKBarPVDone), (ni - 1) & 1, p.timeout_ns))) {
         tc_fence_after();
-        tmem_ld32(tmem + kKColDK + lane_off, a0);
-        tmem_ld32(tmem + kKColDK + lane_off + 32, a1);
-        tmem_ld32(tmem + kKColDV + lane_off, v0);
-        tmem_ld32(tmem + kKColDV + lane_off + 32, v1);
+        tmem_ld32(tmem + col + lane_off, a0);
+        tmem_ld32(tmem + col + lane_off + 32, a1);
         tmem_wait_ld();
         reg_fence(a0);
         reg_fence(a1);
-        reg_fence(v0);
-        reg_fence(v1);
       } else {
         record_error(p.status, kErrTimeout, kSiteBwdEpi);
       }
     }
     if (live) {
-      store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(key) * p.o0_n, a0, a1,
-                p.scale);
-      store_row(p.out1 + b * p.o1_b + h * p.o1_h + static_cast<int64_t>(key) * p.o1_n, v0, v1,
-                1.f);
+      if (half == 0)
+        store_row(p.out0 + b * p.o0_b + h * p.o0_h + static_cast<int64_t>(key) * p.o0_n, a0,
+                  a1, p.scale);
+      else
+        store_row(p.out1 + b * p.o1_b + h * p.o1_h + static_cast<int64_t>(key) * p.o1_n, a0,
+                  a1, 1.f);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -622,8 +626,7 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.mask = a.mask;
   p.key_len = a.key_len;
   p.scale = a.scale;
-  p.lse = a.lse;
-  p.Dv = a.Dv;
+  p.stats = a.Dv;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
   cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_dq_kernel,

@@ -50,18 +50,31 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
     sdpa_bwd_rowdot_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
-                           int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn) {
+                           int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
+                           const float* __restrict__ lse, int rows) {
+  // lse != null: the per-tile layout {lse * log2 e [128], D [128]} over rows up to a whole
+  // number of 128-row tiles; otherwise D alone as [B, H, Nq]
   const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
-  if (row >= Nq) return;
-  const T* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
-  const T* g = dO + b * gb + h * gh + static_cast<int64_t>(row) * gn;
+  if (row >= rows) return;
   float acc = 0.f;
-  for (int t = lane; t < d_v; t += 32) acc = fmaf(ld(o + t), ld(g + t), acc);
+  if (row < Nq) {
+    const T* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
+    const T* g = dO + b * gb + h * gh + static_cast<int64_t>(row) * gn;
+    for (int t = lane; t < d_v; t += 32) acc = fmaf(ld(o + t), ld(g + t), acc);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) Dv[(static_cast<int64_t>(b) * H + h) * Nq + row] = acc;
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  }
+  if (lane != 0) return;
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
+  if (lse == nullptr) {
+    Dv[bh * Nq + row] = acc;
+  } else {
+    float* tile = Dv + (bh * (rows / 128) + row / 128) * 256;
+    tile[row % 128] = row < Nq ? __ldg(lse + bh * Nq + row) * 1.4426950408889634f : INFINITY;
+    tile[128 + row % 128] = acc;
+  }
 }
 
 struct BwdF32 {
@@ -173,16 +186,18 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_bwd_dkdv_f32_kernel(const Bw
 }  // namespace
 
 cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s) {
-  dim3 grid((a.Nq + kWarps - 1) / kWarps, a.H, a.B);
+  const int rows = dtype == 1 ? (a.Nq + 127) / 128 * 128 : a.Nq;
+  dim3 grid((rows + kWarps - 1) / kWarps, a.H, a.B);
   if (dtype == 1)
     sdpa_bwd_rowdot_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.Dv,
         a.H, a.Nq, a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1],
-        a.st[4][2]);
+        a.st[4][2], a.lse, rows);
   else
     sdpa_bwd_rowdot_kernel<float><<<grid, kWarps * 32, 0, s>>>(
         static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
-        a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2]);
+        a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], nullptr,
+        rows);
   return cudaGetLastError();
 }
 
