@@ -113,8 +113,9 @@ bool map_2d_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [B, H, N, 64] bf16 tensor with element strides st = {b, h, n, d=1}; box {64, 128, 1, 1}.
-bool map_bhnd_bf16(CUtensorMap* m, const void* base, int B, int H, int N, const int64_t* st) {
+// [B, H, N, 64] bf16 tensor with element strides st = {b, h, n, d=1}; box {64, box_rows, 1, 1}.
+bool map_bhnd_bf16(CUtensorMap* m, const void* base, int B, int H, int N, const int64_t* st,
+                   uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
@@ -122,7 +123,7 @@ bool map_bhnd_bf16(CUtensorMap* m, const void* base, int B, int H, int N, const 
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2,
                            static_cast<cuuint64_t>(st[1]) * 2,
                            static_cast<cuuint64_t>(st[0]) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -154,12 +155,13 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
 int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t s) {
   cudaError_t e;
   if (dtype == MHA_BF16) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!map_bhnd_bf16(&tq, a.Q, a.B, a.H, a.Nq, a.sq) ||
         !map_bhnd_bf16(&tk, a.K, a.B, a.H, a.Nk, a.sk) ||
-        !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.sv))
+        !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.sv) ||
+        !map_bhnd_bf16(&to, a.O, a.B, a.H, a.Nq, a.so, 32))
       return MHA_ERR_CUDA;
-    e = mha::launch_sdpa_bf16(tq, tk, tv, a, ctx, s);
+    e = mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
   } else {
     e = mha::launch_sdpa_f32(a, s);
   }

@@ -49,10 +49,11 @@ struct SdpaArgs {
   // over the allowed keys (+inf for a row with none), fp32 [B, H, Nq] contiguous
   float* lse = nullptr;
 };
-// bf16: Q/K/V through 4-D TMA maps {d, n, h, b} with box {64, 128, 1, 1}, 128-byte swizzle.
+// bf16: Q/K/V through 4-D TMA maps {d, n, h, b} with box {64, 128, 1, 1}, 128-byte swizzle;
+// O written through the same kind of map with box {64, 32, 1, 1} (one 32-row box per warp).
 cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, const SdpaArgs& a, const DevCtx& ctx,
-                             cudaStream_t s);
+                             const CUtensorMap& tmV, const CUtensorMap& tmO, const SdpaArgs& a,
+                             const DevCtx& ctx, cudaStream_t s);
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s);
 
 // ---- one generation step against a key/value cache (split-K over the cached keys)

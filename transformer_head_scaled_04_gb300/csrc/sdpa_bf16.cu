@@ -27,8 +27,9 @@
 //              2^64 is redone from TMEM with its true max after rescaling O and l.  The
 //              exponentials run before the wait for the previous P.V product, and tile 1
 //              starts its first exponentials only when tile 0 has finished its own, so the
-//              two warpgroups' MUFU-heavy phases interleave instead of colliding.  At the end: O / l -> bf16 -> global, in any strided layout
-//              (the head-concat layout [B, Nq, H*64] in the sublayer).
+//              two warpgroups' MUFU-heavy phases interleave instead of colliding.  At the end: O / l -> bf16 ->
+//              a shared-memory staging tile -> one bulk tensor store per warp, into any
+//              strided layout (the head-concat layout [B, Nq, H*64] in the sublayer).
 // Whole K/V tiles past the causal diagonal or past key_len[b] are never loaded.  The query
 // blocks of one (b, h) are adjacent in the grid, so they run together and share K/V in L2.
 // Every wait is bounded (see device_common.cuh); a timeout records MHA_ERR_DEVICE_TIMEOUT.
@@ -63,7 +64,8 @@ constexpr int kOffQ = 0;
 constexpr int kOffK0 = kOffQ + 2 * kTileBytes;
 constexpr int kOffK = kOffK0 + kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+constexpr int kOffO = kOffV + kVStages * kTileBytes;  // O staging: two 128 x 64 bf16 tiles
+constexpr int kOffBar = kOffO + 2 * kTileBytes;
 constexpr int kSmemBytes = 1024 + kOffBar + 256;
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384) P0 [384,448) P1 [448,512)
 // (P holds 128 bf16 per row, two per 32-bit column)
@@ -99,8 +101,6 @@ struct Params {
   int window;  // kMaskWindow: query i attends keys j with |i - j| <= window
   const int32_t* key_len;
   float scale_log2;  // scale * log2(e)
-  __nv_bfloat16* O;
-  int64_t so_b, so_h, so_n;
   float* lse;  // optional [B, H, Nq]: (m_used * c + log2 l) * ln 2
   int* status;
   uint64_t timeout_ns;
@@ -111,7 +111,8 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const Params p) {
+                         const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK0 = smem_u32(smem + kOffK0);
   const uint32_t sK = smem_u32(smem + kOffK);
   const uint32_t sV = smem_u32(smem + kOffV);
+  const uint32_t sO = smem_u32(smem + kOffO);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -516,19 +518,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.lse != nullptr && row < p.Nq)
       p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + row] =
           (ok && l > 0.f) ? (m_used * c + log2f(l)) * 0.6931471805599453f : INFINITY;
-    if (row < p.Nq) {
-      __nv_bfloat16* dst = p.O + static_cast<int64_t>(b) * p.so_b +
-                           static_cast<int64_t>(h) * p.so_h + static_cast<int64_t>(row) * p.so_n;
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
+    // O / l in bf16 -> this warp's 32 rows of the staging tile (128-byte swizzle: 16-byte
+    // chunk c of row r at chunk c ^ (r % 8), conflict-free) -> one bulk tensor store per warp,
+    // which writes only the rows below Nq
+    const uint32_t sOw = sO + t * kTileBytes + quarter * (32 * 128);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint4 v;
-        v.x = pack_bf16x2(o[u * 8 + 0], o[u * 8 + 1]);
-        v.y = pack_bf16x2(o[u * 8 + 2], o[u * 8 + 3]);
-        v.z = pack_bf16x2(o[u * 8 + 4], o[u * 8 + 5]);
-        v.w = pack_bf16x2(o[u * 8 + 6], o[u * 8 + 7]);
-        d4[u] = v;
-      }
+    for (int cidx = 0; cidx < 8; ++cidx) {
+      uint4 v;
+      v.x = pack_bf16x2(o[cidx * 8 + 0], o[cidx * 8 + 1]);
+      v.y = pack_bf16x2(o[cidx * 8 + 2], o[cidx * 8 + 3]);
+      v.z = pack_bf16x2(o[cidx * 8 + 4], o[cidx * 8 + 5]);
+      v.w = pack_bf16x2(o[cidx * 8 + 6], o[cidx * 8 + 7]);
+      st_shared_v4(sOw + lane * 128 + ((cidx ^ (lane & 7)) << 4), v);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    const int wrow0 = q0 + t * kBQ + quarter * 32;
+    if (lane == 0 && wrow0 < p.Nq) {
+      tma_store_4d(&tmO, sOw, 0, wrow0, h, b);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the staging tile stays until the copy has read it
     }
   }
 
@@ -543,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                             const CUtensorMap& tmV, const SdpaArgs& a, const DevCtx& ctx,
-                             cudaStream_t s) {
+                             const CUtensorMap& tmV, const CUtensorMap& tmO, const SdpaArgs& a,
+                             const DevCtx& ctx, cudaStream_t s) {
   Params p;
   p.B = a.B;
   p.H = a.H;
@@ -555,10 +564,6 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.key_len = a.key_len;
   const double c = static_cast<double>(a.scale) * 1.4426950408889634;  // log2(e)
   p.scale_log2 = static_cast<float>(c);
-  p.O = static_cast<__nv_bfloat16*>(a.O);
-  p.so_b = a.so[0];
-  p.so_h = a.so[1];
-  p.so_n = a.so[2];
   p.lse = a.lse;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
@@ -573,7 +578,7 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (fa.numRegs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
     return cudaErrorInvalidConfiguration;
   dim3 grid((a.Nq + 2 * kBQ - 1) / (2 * kBQ), a.H, a.B);
-  sdpa_fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQ, tmK, tmV, p);
+  sdpa_fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQ, tmK, tmV, tmO, p);
   return cudaGetLastError();
 }
 
