@@ -140,10 +140,11 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
   if (dtype == MHA_BF16) {
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);
     const int bn = (tiles256 >= ctx.num_sms) ? 256 : 128;
-    CUtensorMap tmX, tmW;
-    if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, bn))
+    CUtensorMap tmX, tmW, tmY;
+    if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, bn) ||
+        !map_2d_bf16(&tmY, Y, N, M, ldy, 32))
       return MHA_ERR_CUDA;
-    e = mha::launch_gemm_bf16(tmX, tmW, bn, relu, bias, Y, M, N, K, ldy, ctx, s, residual);
+    e = mha::launch_gemm_bf16(tmX, tmW, tmY, bn, relu, bias, Y, M, N, K, ldy, ctx, s, residual);
   } else {
     e = mha::launch_gemm_f32(static_cast<const float*>(X), ldx, static_cast<const float*>(W),
                              static_cast<const float*>(bias), relu, static_cast<float*>(Y), ldy,

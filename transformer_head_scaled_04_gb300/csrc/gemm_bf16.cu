@@ -15,8 +15,9 @@
 //   warp 1     TMEM owner + MMA issuer: tcgen05.mma kind::f16 128xBNx16 into one of two TMEM
 //              accumulators, so the epilogue of tile i overlaps the MMAs of tile i+1
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (one TMEM lane quarter per warp), add
-//              bias, ReLU if asked, round to bf16 (nearest even), store, hand the
-//              accumulator back.
+//              bias, ReLU if asked, round to bf16 (nearest even), hand the accumulator back;
+//              each warp writes its 32 rows 64 columns at a time into one of two swizzled
+//              shared-memory staging boxes and issues one bulk tensor store per box.
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -41,7 +42,9 @@ struct GemmShape {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kOutBoxBytes = 32 * 64 * 2;        // 32 rows x 64 bf16 columns
+  static constexpr int kOutBytes = 4 * 2 * kOutBoxBytes;  // two boxes per epilogue warp
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
@@ -49,6 +52,7 @@ template <int BN, bool kRelu>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
+                          const __grid_constant__ CUtensorMap tmY,
                           const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ Y,
                           int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns,
                           const __nv_bfloat16* __restrict__ R) {
@@ -58,7 +62,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + S::kStages * S::kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
+  const uint32_t sOut = smem_u32(smem + S::kStages * S::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes + S::kOutBytes);
   // [0,ST) full, [ST,2ST) empty, then acc_full[2], acc_empty[2], drain; tmem slot after
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 5);
 
@@ -159,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     int tcount = 0;
+    int box = 0;  // staging boxes used so far (alternating)
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
       const int buf = tcount & 1;
       const int m0 = (tile / tiles_n) * kBM;
@@ -170,68 +176,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tbase = tmem + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const int wrow0 = m0 + quarter * 32;  // this warp's first output row
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tbase + c * 32, r);
-        tmem_wait_ld();
-        reg_fence(r);
-        const int col = n0 + c * 32;
-        if (row < M && col < N) {
-          float bv[32];
-          if (bias != nullptr) {
-            const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
+      for (int c = 0; c < BN / 64; ++c, ++box) {
+        uint32_t r[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tbase + c * 64, r0);
+          tmem_ld32(tbase + c * 64 + 32, r1);
+          tmem_wait_ld();
+          reg_fence(r0);
+          reg_fence(r1);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 u = __ldg(bp + v);
-              const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float2 f = __bfloat1622float2(hv[e]);
-                bv[v * 8 + e * 2] = f.x;
-                bv[v * 8 + e * 2 + 1] = f.y;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) bv[i] = 0.f;
+          for (int i = 0; i < 32; ++i) {
+            r[i] = r0[i];
+            r[32 + i] = r1[i];
           }
-          if (R != nullptr) {  // a residual matrix with Y's layout joins the bias
-            const uint4* rp = reinterpret_cast<const uint4*>(R + static_cast<int64_t>(row) * ldy + col);
+        }
+        if (c == BN / 64 - 1) {  // accumulator read: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(buf));
+        }
+        const int col = n0 + c * 64;
+        if (wrow0 >= M || col >= N) continue;  // nothing of this box is inside Y
+        float bv[64];
+        if (bias != nullptr) {
+          const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 u = rp[v];
-              const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+          for (int v = 0; v < 8; ++v) {
+            uint4 u = __ldg(bp + v);
+            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float2 f = __bfloat1622float2(hv[e]);
-                bv[v * 8 + e * 2] += f.x;
-                bv[v * 8 + e * 2 + 1] += f.y;
-              }
+            for (int e = 0; e < 4; ++e) {
+              float2 f = __bfloat1622float2(hv[e]);
+              bv[v * 8 + e * 2] = f.x;
+              bv[v * 8 + e * 2 + 1] = f.y;
             }
           }
-          uint4 out[4];
-          uint32_t* o32 = reinterpret_cast<uint32_t*>(out);
+        } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = __uint_as_float(r[2 * i]) + bv[2 * i];
-            float v1 = __uint_as_float(r[2 * i + 1]) + bv[2 * i + 1];
+          for (int i = 0; i < 64; ++i) bv[i] = 0.f;
+        }
+        if (R != nullptr && row < M) {  // a residual matrix with Y's layout joins the bias
+          const uint4* rp = reinterpret_cast<const uint4*>(R + static_cast<int64_t>(row) * ldy + col);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint4 u = rp[v];
+            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float2 f = __bfloat1622float2(hv[e]);
+              bv[v * 8 + e * 2] += f.x;
+              bv[v * 8 + e * 2 + 1] += f.y;
+            }
+          }
+        }
+        // the store issued from this staging box two boxes ago must have read it
+        const uint32_t sb = sOut + (quarter * 2 + (box & 1)) * S::kOutBoxBytes;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        // row `lane` of the box, 128-byte swizzle: 16-byte chunk q at chunk q ^ (lane % 8)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v0 = __uint_as_float(r[q * 8 + 2 * e]) + bv[q * 8 + 2 * e];
+            float v1 = __uint_as_float(r[q * 8 + 2 * e + 1]) + bv[q * 8 + 2 * e + 1];
             if (kRelu) {
               v0 = fmaxf(v0, 0.f);
               v1 = fmaxf(v1, 0.f);
             }
-            o32[i] = pack_bf16x2(v0, v1);
+            o[e] = pack_bf16x2(v0, v1);
           }
-          uint4* dst = reinterpret_cast<uint4*>(Y + static_cast<int64_t>(row) * ldy + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = out[v];
+          st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {  // rows past M are not written
+          tma_store_2d(&tmY, sb, col, wrow0);
+          bulk_commit_group();
         }
       }
-      // accumulator read: hand it back to the MMA issuer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(buf));
     }
+    if (lane == 0) bulk_wait_group_read<0>();  // staging stays until every store has read it
   }
 
   tc_fence_before();
@@ -243,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, bool kRelu>
-cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void* bias, void* Y,
+cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
+                      const void* bias, void* Y,
                       int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                       const void* R) {
   using S = GemmShape<BN>;
@@ -253,7 +283,7 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM);
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW, static_cast<const __nv_bfloat16*>(bias),
+  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW, tmY, static_cast<const __nv_bfloat16*>(bias),
                                              static_cast<__nv_bfloat16*>(Y), M, N, K, ldy,
                                              ctx.status, ctx.timeout_ns,
                                              static_cast<const __nv_bfloat16*>(R));
@@ -262,15 +292,16 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const void
 
 }  // namespace
 
-cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
+cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             const CUtensorMap& tmY, int block_n,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s, const void* R) {
   if (relu) {
-    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
-    return launch_bn<128, true>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
+    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
+    return launch_bn<128, true>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
   }
-  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
-  return launch_bn<128, false>(tmX, tmW, bias, Y, M, N, K, ldy, ctx, s, R);
+  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
+  return launch_bn<128, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
 }
 
 }  // namespace mha

@@ -17,9 +17,11 @@ struct DevCtx {
 
 // ---- projections: Y[M,N] = act(X[M,K] W[N,K]^T + bias), act = identity or ReLU (relu)
 // bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W
-// {K, N}, box {64, block_n}; both 128-byte swizzled.  block_n is 128 or 256.
+// {K, N}, box {64, block_n}; tmY: 2-D map over Y {N, M}, box {64, 32}; all 128-byte swizzled.
+// block_n is 128 or 256.
 // residual: optional R [M, N] with Y's row pitch, added in the epilogue (Y = XW^T + b + R)
-cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW, int block_n,
+cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             const CUtensorMap& tmY, int block_n,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                              const void* residual = nullptr);
