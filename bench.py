@@ -761,8 +761,8 @@ def run_ours(args):
 def run_profile_case(args):
     """One kernel family on the big model's heads with a reduced batch, for ncu captures:
     no L2 flush, no other legs, a short JSON line with the mean launch time.  Batch 4 keeps
-    the attention inputs (Q, K, V, O: 134 MB) above the 129 MB L2 while the whole device
-    footprint stays well under a few GB."""
+    the attention inputs (Q, K, V, O: 134 MB) and the QKV projection's X and Y (134 MB) above
+    the 129 MB L2 while the whole device footprint stays well under a few GB."""
     import torch
 
     from transformer_head_scaled_04_gb300 import _capi as C
@@ -796,8 +796,18 @@ def run_profile_case(args):
                                  vp(v), vp(o), vp(do), vp(lse), vp(dq), vp(dk), vp(dv), None,
                                  vp(ws), ws.numel(), sp), "mha_sdpa_bwd")
 
+    # the QKV projection of the same rows: X [B*n, d_model] -> [B*n, 3 d_model]
+    Dm = w.H * d
+    x = torch.randn((B * N, Dm), device=dev, generator=g).to(bf)
+    wq = (torch.randn((3 * Dm, Dm), device=dev, generator=g) * 0.03).to(bf)
+    y = torch.empty((B * N, 3 * Dm), dtype=bf, device=dev)
+
+    def qkv():
+        C.check(lib.mha_linear_fwd(B * N, 3 * Dm, Dm, C.MHA_BF16, vp(x), Dm, vp(wq), None, vp(y),
+                                   3 * Dm, sp), "mha_linear_fwd")
+
     fwd()
-    fn = fwd if args.profile_case == "sdpa_fwd" else bwd
+    fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv}[args.profile_case]
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -822,7 +832,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
-    ap.add_argument("--profile-case", choices=["sdpa_fwd", "sdpa_bwd"], default=None,
+    ap.add_argument("--profile-case", choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv"], default=None,
                     help="run only this kernel family (for ncu captures), no bench line")
     ap.add_argument("--batch", type=int, default=4, help="batch of --profile-case")
     args = ap.parse_args()
