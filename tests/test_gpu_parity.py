@@ -280,7 +280,8 @@ def test_linear_f32():
 # ------------------------------------------------------------------------ residual LayerNorm
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("M,D", [(1, 8), (333, 512), (65, 1024), (10, 200), (7, 2048)])
+@pytest.mark.parametrize("M,D", [(1, 8), (333, 512), (65, 1024), (10, 200), (7, 2048),
+                                 (4099, 1024)])
 def test_residual_layernorm(dtype, M, D):
     g = np.random.Generator(np.random.PCG64(M * D))
     rnd = si.round_bf16 if dtype == torch.bfloat16 else (lambda a: a.astype(np.float32))
