@@ -18,8 +18,12 @@
 //           P^T and dS^T into TMEM; dV += P^T dO and dK += dS^T Q accumulate in TMEM
 //           (all 512 columns: S^T, dP^T, P^T, dS^T, dV, dK).
 // Warps: 0-7 math (two per sub-partition: warps w and w+4 share TMEM lanes 32*(w%4).. and
-// take the two 64-column halves of every tile), 8 TMA producer, 9 TMEM owner and MMA issuer.  Every wait is bounded; a
-// timeout records MHA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land, frees TMEM.
+// take the two 64-column halves of every tile), 8 TMA producer, 9 TMEM owner and issuer of S
+// and dP (S^T and dP^T), then the gradient issuers: dq kernel warp 10 (dQ, with dS double-
+// buffered in TMEM so the math warps write dS_{j+1} while dQ still reads dS_j), dkdv kernel
+// warps 10 (dV) and 11 (dK; its math warps run at 200 registers through setmaxnreg).  Every
+// wait is bounded; a timeout records MHA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs
+// land, frees TMEM.
 // Masks: none, causal (j <= i) and key padding (j < key_len[b]); fully masked tiles are
 // skipped, and the d = 64 heads of the forward kernel are assumed.
 #include <cuda_bf16.h>
@@ -38,8 +42,19 @@ constexpr int kTileBytes = kT * kHD * 2;   // 16 KB
 constexpr int kStages = 3;
 constexpr int kMathWarps = 8;               // warp w: rows 32*(w%4).. of the tile, column half w/4
 constexpr int kWarpProducer = kMathWarps;   // TMA
-constexpr int kWarpMma = kMathWarps + 1;    // TMEM owner and MMA issuer
-constexpr int kThreads = (kMathWarps + 2) * 32;
+constexpr int kWarpMma = kMathWarps + 1;    // TMEM owner; issues the S and dP products
+// An issuing thread spends ~75-100 cycles per tcgen05.mma here (more when the tensor pipe's
+// queue is full), so the gradient products have issuers of their own and no longer wait
+// behind the next tile's S / dP issue: dq kernel warp 10 (dQ); dkdv kernel warps 10 (dV)
+// and 11 (dK).
+constexpr int kWarpMma2 = kMathWarps + 2;
+constexpr int kWarpMma3 = kMathWarps + 3;
+constexpr int kQThreads = (kMathWarps + 3) * 32;
+constexpr int kKThreads = (kMathWarps + 4) * 32;
+constexpr int kKMathRegs = 200;
+constexpr int kKControlRegs = 72;
+static_assert(kMathWarps * 32 * kKMathRegs + 4 * 32 * kKControlRegs <= kKThreads * 168,
+              "dkdv register split exceeds the launch allocation");
 constexpr int kErrTimeout = -6;
 enum : int { kSiteBwdProducer = 41, kSiteBwdMma = 42, kSiteBwdMath = 43, kSiteBwdEpi = 44 };
 constexpr float kLog2e = 1.4426950408889634f;
@@ -153,20 +168,22 @@ constexpr int kQOffK = kQOffG + kTileBytes;
 constexpr int kQOffV = kQOffK + kStages * kTileBytes;
 constexpr int kQOffBar = kQOffV + kStages * kTileBytes;
 constexpr int kQSmem = 1024 + kQOffBar + 256;
-// TMEM: S [0,128) dP [128,256) dS (bf16 pairs) [256,320) dQ [320,384)
-constexpr uint32_t kQColS = 0, kQColP = 128, kQColDS = 256, kQColDQ = 320;
+// TMEM: S [0,128) dP [128,256) dS of even tiles (bf16 pairs) [256,320) dQ [320,384) dS of
+// odd tiles [384,448): the math warps write dS(j+1) while dQ += dS(j) K_j still reads dS(j)
+constexpr uint32_t kQColS = 0, kQColP = 128, kQColDQ = 320;
+__device__ __forceinline__ uint32_t q_col_ds(int j) { return (j & 1) ? 384u : 256u; }
 // barriers
 constexpr int kQBarIn = 0;                     // Q, dO landed
 constexpr int kQBarKV = 1;                     // [kStages] K_j, V_j landed
-constexpr int kQBarKVEmpty = kQBarKV + kStages;  // [kStages] MMAs done with K_j, V_j
+constexpr int kQBarKVEmpty = kQBarKV + kStages;  // [kStages] both issuers done with K_j, V_j
 constexpr int kQBarSFull = kQBarKVEmpty + kStages;
 constexpr int kQBarSFree = kQBarSFull + 1;   // every math warp holds its S, dP half
-constexpr int kQBarDSFull = kQBarSFree + 1;  // every math warp wrote its dS half
-constexpr int kQBarDQDone = kQBarDSFull + 1; // dQ MMA done with dS
-constexpr int kQBarDrain = kQBarDQDone + 1;
+constexpr int kQBarDSFull = kQBarSFree + 1;  // [2] every math warp wrote its dS half
+constexpr int kQBarDQDone = kQBarDSFull + 2; // [2] dQ MMA done with that dS buffer
+constexpr int kQBarDrain = kQBarDQDone + 2;
 constexpr int kQNumBars = kQBarDrain + 1;
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     sdpa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
@@ -188,13 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kQBarIn), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kQBarKV + s), 1);
-      mbar_init(bar(kQBarKVEmpty + s), 1);
+      mbar_init(bar(kQBarKVEmpty + s), 2);  // the S/dP issuer and the dQ issuer
     }
     mbar_init(bar(kQBarSFull), 1);
     mbar_init(bar(kQBarSFree), kMathWarps);
-    mbar_init(bar(kQBarDSFull), kMathWarps);
-    mbar_init(bar(kQBarDQDone), 1);
-    mbar_init(bar(kQBarDrain), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kQBarDSFull + i), kMathWarps);
+      mbar_init(bar(kQBarDQDone + i), 1);
+    }
+    mbar_init(bar(kQBarDrain), 2);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -237,10 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait(bar(kQBarKV + i % kStages), (i / kStages) & 1, p.timeout_ns);
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S and dP issuer
     if (lane == 0 && nk > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
-      constexpr uint32_t idQ = idesc_bf16_f32(kT, kHD, false, true);
       const uint64_t dQd = smem_desc_sw128(smem_u32(smem + kQOffQ), 1024, 1024);
       const uint64_t dGd = smem_desc_sw128(smem_u32(smem + kQOffG), 1024, 1024);
       // S_j = Q K_j^T and dP_j = dO V_j^T into the single S/dP buffer
@@ -256,19 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kQColP, dGd + kk * 2, dV + kk * 2, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kQBarSFull));
+        mma_commit(bar(kQBarKVEmpty + s));  // this issuer is done with K_j, V_j
         return true;
       };
       bool ok = mbar_wait(bar(kQBarIn), 0, p.timeout_ns) && issue_s(0);
+      // once the math warps hold S_j and dP_j in registers the next tile's products run
+      // while they turn them into dS_j
+      for (int j = 0; ok && j + 1 < nk; ++j)
+        ok = mbar_wait(bar(kQBarSFree), j & 1, p.timeout_ns) && issue_s(j + 1);
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
+      mma_commit(bar(kQBarDrain));
+      (void)mbar_wait(bar(kQBarDrain), 0, p.timeout_ns);  // no MMA of this CTA in flight
+    }
+  } else if (warp == kWarpMma2) {
+    // ------------------------------------------------------------ dQ issuer
+    if (lane == 0 && nk > 0) {
+      constexpr uint32_t idQ = idesc_bf16_f32(kT, kHD, false, true);
+      bool ok = true;
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j % kStages;
-        // once the math warps hold S_j and dP_j in registers the next tile's products run
-        // while they turn them into dS_j
-        if (j + 1 < nk &&
-            (!mbar_wait(bar(kQBarSFree), j & 1, p.timeout_ns) || !issue_s(j + 1))) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(bar(kQBarDSFull), j & 1, p.timeout_ns)) {
+        // dS_j written (and K_j landed, which the S issuer saw before S_j)
+        if (!mbar_wait(bar(kQBarDSFull + (j & 1)), (j >> 1) & 1, p.timeout_ns) ||
+            !mbar_wait(bar(kQBarKV + s), (j / kStages) & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -277,9 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ += dS K_j: 16 keys (8 TMEM columns of dS, 16 K rows) per MMA
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_bf16_ts(tmem + kQColDQ, tmem + kQColDS + kk * 8, dK + kk * ((16 * 128) >> 4), idQ,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(kQBarDQDone));
+          mma_bf16_ts(tmem + kQColDQ, tmem + q_col_ds(j) + kk * 8, dK + kk * ((16 * 128) >> 4),
+                      idQ, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(kQBarDQDone + (j & 1)));
         mma_commit(bar(kQBarKVEmpty + s));
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
@@ -327,17 +354,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         dq_half<false>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
       else
         dq_half<true>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
-      // the previous dQ product must have read dS before it is overwritten
-      if (j > 0 && !warp_all(mbar_wait(bar(kQBarDQDone), (j - 1) & 1, p.timeout_ns))) {
+      // dS_j goes to buffer j % 2, which dQ += dS_{j-2} K_{j-2} must have finished reading
+      if (j > 1 && !warp_all(mbar_wait(bar(kQBarDQDone + (j & 1)), ((j >> 1) - 1) & 1,
+                                       p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteBwdMath);
         ok = false;
         break;
       }
-      tmem_st32(tmem + kQColDS + lane_off + half * 32, ds);
+      tmem_st32(tmem + q_col_ds(j) + lane_off + half * 32, ds);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kQBarDSFull));
+      if (lane == 0) mbar_arrive(bar(kQBarDSFull + (j & 1)));
     }
     // ---- epilogue: dQ * scale -> bf16, 32 of the 64 columns per warp
     __nv_bfloat16* dst =
@@ -346,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; ++i) r0[i] = 0u;
     if (ok && nk > 0) {
-      if (warp_all(mbar_wait(bar(kQBarDQDone), (nk - 1) & 1, p.timeout_ns))) {
+      if (warp_all(mbar_wait(bar(kQBarDQDone + ((nk - 1) & 1)), ((nk - 1) >> 1) & 1,
+                             p.timeout_ns))) {
         tc_fence_after();
         tmem_ld32(tmem + kQColDQ + lane_off + half * 32, r0);
         tmem_wait_ld();
@@ -379,15 +408,16 @@ constexpr uint32_t kKColS = 0, kKColP = 128, kKColPT = 256, kKColDS = 320, kKCol
                    kKColDK = 448;
 constexpr int kKBarIn = 0;                        // K, V landed
 constexpr int kKBarQ = 1;                         // [kStages] Q_i, dO_i, lse, D landed
-constexpr int kKBarQEmpty = kKBarQ + kStages;     // [kStages] MMAs done with Q_i, dO_i
+constexpr int kKBarQEmpty = kKBarQ + kStages;     // [kStages] all three issuers done with Q_i, dO_i
 constexpr int kKBarSFull = kKBarQEmpty + kStages;
 constexpr int kKBarSFree = kKBarSFull + 1;        // every math warp holds its S^T, dP^T half
 constexpr int kKBarPFull = kKBarSFree + 1;        // every math warp wrote its P^T, dS^T half
-constexpr int kKBarPVDone = kKBarPFull + 1;
-constexpr int kKBarDrain = kKBarPVDone + 1;
+constexpr int kKBarDVDone = kKBarPFull + 1;       // dV += P^T dO done with P^T
+constexpr int kKBarDKDone = kKBarDVDone + 1;      // dK += dS^T Q done with dS^T
+constexpr int kKBarDrain = kKBarDKDone + 1;
 constexpr int kKNumBars = kKBarDrain + 1;
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKThreads, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
@@ -412,13 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kKBarIn), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kKBarQ + s), 1);
-      mbar_init(bar(kKBarQEmpty + s), 1);
+      mbar_init(bar(kKBarQEmpty + s), 3);  // the S/dP, dV and dK issuers
     }
     mbar_init(bar(kKBarSFull), 1);
     mbar_init(bar(kKBarSFree), kMathWarps);
     mbar_init(bar(kKBarPFull), kMathWarps);
-    mbar_init(bar(kKBarPVDone), 1);
-    mbar_init(bar(kKBarDrain), 1);
+    mbar_init(bar(kKBarDVDone), 1);
+    mbar_init(bar(kKBarDKDone), 1);
+    mbar_init(bar(kKBarDrain), 3);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -430,6 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // register split (setmaxnreg): 384 threads launch with 168 registers each (64512); the
+  // control warpgroup (producer, three issuers) drops to 72 so the math warps can take 200:
+  // 256 x 200 + 128 x 72 = 60416 <= 64512
+  if (warp >= kMathWarps) regs_dec<kKControlRegs>();  // first: the math warps' increase waits on it
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer (TMA + stats)
     if (lane == 0 && ni > 0) {
@@ -466,10 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait(bar(kKBarQ + i % kStages), (i / kStages) & 1, p.timeout_ns);
     }
   } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S^T and dP^T issuer
     if (lane == 0 && ni > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(kT, kHD, false, true);
       const uint64_t dKd = smem_desc_sw128(smem_u32(smem + kKOffK), 1024, 1024);
       const uint64_t dVd = smem_desc_sw128(smem_u32(smem + kKOffV), 1024, 1024);
       // S^T_t = K Q_t^T and dP^T_t = V dO_t^T into the single S/dP buffer
@@ -485,34 +519,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + kKColP, dVd + kk * 2, dG + kk * 2, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(kKBarSFull));
+        mma_commit(bar(kKBarQEmpty + s));  // this issuer is done with Q_t, dO_t
         return true;
       };
       bool ok = mbar_wait(bar(kKBarIn), 0, p.timeout_ns) && issue_s(0);
+      // once the math warps hold S^T_t and dP^T_t in registers the next tile's products run
+      // while they turn them into P^T_t and dS^T_t
+      for (int t = 0; ok && t + 1 < ni; ++t)
+        ok = mbar_wait(bar(kKBarSFree), t & 1, p.timeout_ns) && issue_s(t + 1);
+      if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
+      mma_commit(bar(kKBarDrain));
+      (void)mbar_wait(bar(kKBarDrain), 0, p.timeout_ns);  // no MMA of this CTA in flight
+    }
+  } else if (warp == kWarpMma2 || warp == kWarpMma3) {
+    // ------------------------------------------------------------ dV issuer / dK issuer
+    if (lane == 0 && ni > 0) {
+      constexpr uint32_t idO = idesc_bf16_f32(kT, kHD, false, true);
+      const bool is_dv = warp == kWarpMma2;
+      // dV += P^T dO_t, dK += dS^T Q_t: 16 queries (8 TMEM columns, 16 smem rows) per MMA
+      const uint32_t acc = tmem + (is_dv ? kKColDV : kKColDK);
+      const uint32_t a_op = tmem + (is_dv ? kKColPT : kKColDS);
+      const int b_off = is_dv ? kKOffG : kKOffQ;
+      const int done_bar = is_dv ? kKBarDVDone : kKBarDKDone;
+      bool ok = true;
       for (int t = 0; ok && t < ni; ++t) {
         const int s = t % kStages;
-        // once the math warps hold S^T_t and dP^T_t in registers the next tile's products run
-        // while they turn them into P^T_t and dS^T_t
-        if (t + 1 < ni &&
-            (!mbar_wait(bar(kKBarSFree), t & 1, p.timeout_ns) || !issue_s(t + 1))) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(bar(kKBarPFull), t & 1, p.timeout_ns)) {
+        // P^T_t, dS^T_t written (and Q_t, dO_t landed, which the S issuer saw before S^T_t)
+        if (!mbar_wait(bar(kKBarPFull), t & 1, p.timeout_ns) ||
+            !mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t dQ = smem_desc_sw128(smem_u32(smem + kKOffQ + s * kTileBytes), 1024, 1024);
-        const uint64_t dG = smem_desc_sw128(smem_u32(smem + kKOffG + s * kTileBytes), 1024, 1024);
-        // dV += P^T dO_t and dK += dS^T Q_t: 16 queries (8 TMEM columns, 16 smem rows) per MMA
+        const uint64_t bd = smem_desc_sw128(smem_u32(smem + b_off + s * kTileBytes), 1024, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          mma_bf16_ts(tmem + kKColDV, tmem + kKColPT + kk * 8, dG + kk * ((16 * 128) >> 4), idO,
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_bf16_ts(acc, a_op + kk * 8, bd + kk * ((16 * 128) >> 4), idO,
                       (t > 0 || kk > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + kKColDK, tmem + kKColDS + kk * 8, dQ + kk * ((16 * 128) >> 4), idO,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(kKBarPVDone));
+        mma_commit(bar(done_bar));
         mma_commit(bar(kKBarQEmpty + s));
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteBwdMma);
@@ -521,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ math warps (one key row each)
+    regs_inc<kKMathRegs>();
     const int quarter = warp & 3, half = warp >> 2;
     const int r_local = quarter * 32 + lane;
     const int key = k0 + r_local;
@@ -565,13 +610,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
       else
         dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
-      // the previous dV/dK products must have read P^T and dS^T before they change
-      if (t > 0 && !warp_all(mbar_wait(bar(kKBarPVDone), (t - 1) & 1, p.timeout_ns))) {
+      // the previous dV product must have read P^T, and the previous dK product dS^T, before
+      // they change
+      if (t > 0 && !warp_all(mbar_wait(bar(kKBarDVDone), (t - 1) & 1, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteBwdMath);
         ok = false;
         break;
       }
       tmem_st32(tmem + kKColPT + lane_off + half * 32, pp);
+      if (t > 0 && !warp_all(mbar_wait(bar(kKBarDKDone), (t - 1) & 1, p.timeout_ns))) {
+        tmem_wait_st();
+        record_error(p.status, kErrTimeout, kSiteBwdMath);
+        ok = false;
+        break;
+      }
       tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
       tmem_wait_st();
       tc_fence_before();
@@ -586,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0u;
     const uint32_t col = half == 0 ? kKColDK : kKColDV;
     if (ok && ni > 0) {
-      if (warp_all(mbar_wait(bar(kKBarPVDone), (ni - 1) & 1, p.timeout_ns))) {
+      if (warp_all(mbar_wait(bar(half == 0 ? kKBarDKDone : kKBarDVDone), (ni - 1) & 1,
+                             p.timeout_ns))) {
         tc_fence_after();
         tmem_ld32(tmem + col + lane_off, a0);
         tmem_ld32(tmem + col + lane_off + 32, a1);
@@ -635,11 +688,18 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   e = cudaFuncSetAttribute(sdpa_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kKSmem);
   if (e != cudaSuccess) return e;
+  // the dkdv kernel's setmaxnreg split must fit in what its blocks launch with, or the
+  // increase would wait forever: refuse to launch if the compiled register count is too small
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, sdpa_bwd_dkdv_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * kKThreads < kMathWarps * 32 * kKMathRegs + 4 * 32 * kKControlRegs)
+    return cudaErrorInvalidConfiguration;
   p.out0 = static_cast<__nv_bfloat16*>(a.dQ);
   p.o0_b = a.st[5][0];
   p.o0_h = a.st[5][1];
   p.o0_n = a.st[5][2];
-  sdpa_bwd_dq_kernel<<<dim3((a.Nq + kT - 1) / kT, a.H, a.B), kThreads, kQSmem, s>>>(
+  sdpa_bwd_dq_kernel<<<dim3((a.Nq + kT - 1) / kT, a.H, a.B), kQThreads, kQSmem, s>>>(
       tmQ, tmK, tmV, tmG, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -651,7 +711,7 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.o1_b = a.st[7][0];
   p.o1_h = a.st[7][1];
   p.o1_n = a.st[7][2];
-  sdpa_bwd_dkdv_kernel<<<dim3((a.Nk + kT - 1) / kT, a.H, a.B), kThreads, kKSmem, s>>>(
+  sdpa_bwd_dkdv_kernel<<<dim3((a.Nk + kT - 1) / kT, a.H, a.B), kKThreads, kKSmem, s>>>(
       tmQ, tmK, tmV, tmG, p);
   return cudaGetLastError();
 }
