@@ -99,7 +99,8 @@ int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, 
 /*
  * mha_sdpa_bwd_workspace_size -- bytes of device workspace mha_sdpa_bwd needs: with
  * D_i = sum_d dO_id O_id, MHA_BF16 keeps 1 KB per (b, h, 128-row query tile) -- the tile's
- * D and lse in base-2 units, read by one bulk copy -- and MHA_F32 one fp32 D per query row.
+ * D and lse (lse in base-2 units), both negated, read by one bulk copy -- and MHA_F32 one
+ * fp32 D per query row.
  */
 int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes);
 

@@ -6,7 +6,7 @@
 // forward's log-sum-exp (P = 2^(s*c - lse2), c = scale*log2 e, lse2 = lse*log2 e), so the
 // n x n matrices never leave the SM:
 //   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_d dO_id O_id
-// (a small prior launch writes D and lse * log2 e per 128-row query tile, 1 KB per tile)
+// (a small prior launch writes -D and -lse * log2 e per 128-row query tile, 1 KB per tile)
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO
 // Two kernels, neither with atomics:
 //   dq   -- one CTA per 128-row query tile; K/V tiles stream through a TMA ring.
@@ -63,7 +63,7 @@ struct BwdParams {
   int H, Nq, Nk, mask;
   const int32_t* key_len;
   float scale;       // multiplies q.k
-  const float* stats;  // per (b, h, 128-row query tile): lse * log2 e [128], then D [128]
+  const float* stats;  // per (b, h, 128-row query tile): -lse * log2 e [128], then -D [128]
   __nv_bfloat16* out0;  // dq: dQ; dkdv: dK
   __nv_bfloat16* out1;  // dkdv: dV
   int64_t o0_b, o0_h, o0_n, o1_b, o1_h, o1_n;
@@ -95,52 +95,59 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* dst, const uint32_t* r0
 }
 
 // dS of one 64-key half of a query row: p = 2^(s*c - lse2) (0 past the row's last key when
-// kMask), dS = p * (dP - D), packed to bf16 pairs
+// kMask), dS = p * (dP - D), packed to bf16 pairs; nl = -lse2 and nd = -D, two keys per paired
+// fp32 instruction
 template <bool kMask>
 __device__ __forceinline__ void dq_half(const uint32_t* s0, const uint32_t* s1,
                                         const uint32_t* g0, const uint32_t* g1, int col0,
-                                        int limit, float c, float lse2, float Dr, uint32_t* ds) {
+                                        int limit, float c, float nl, float nd, uint32_t* ds) {
+  const float2 c2 = make_float2(c, c), nl2 = make_float2(nl, nl), nd2 = make_float2(nd, nd);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
-    const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
-    const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
-    const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
-    float pa = ex2_approx(fmaf(sa, c, -lse2));
-    float pb = ex2_approx(fmaf(sb, c, -lse2));
+    const float2 sv = make_float2(__uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]),
+                                  __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]));
+    const float2 gv = make_float2(__uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]),
+                                  __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]));
+    float2 pv = ffma2(sv, c2, nl2);
+    pv.x = ex2_approx(pv.x);
+    pv.y = ex2_approx(pv.y);
     if (kMask) {
-      if (col0 + 2 * i > limit) pa = 0.f;
-      if (col0 + 2 * i + 1 > limit) pb = 0.f;
+      if (col0 + 2 * i > limit) pv.x = 0.f;
+      if (col0 + 2 * i + 1 > limit) pv.y = 0.f;
     }
-    ds[i] = pack_bf16x2(pa * (ga - Dr), pb * (gb - Dr));
+    const float2 dv = fmul2(pv, fadd2(gv, nd2));
+    ds[i] = pack_bf16x2(dv.x, dv.y);
   }
 }
 
-// P^T and dS^T of one 64-query half of a key row; st: this query tile's lse2 [128] then
-// D [128] in shared memory, ca0 the half's first query column.  kMask: query q0 + ca sees
+// P^T and dS^T of one 64-query half of a key row; st: this query tile's -lse2 [128] then
+// -D [128] in shared memory, ca0 the half's first query column.  kMask: query q0 + ca sees
 // this key only when ca >= first_ok (causal) and the key is below the key limit (row_ok).
 template <bool kMask>
 __device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1,
                                           const uint32_t* g0, const uint32_t* g1,
                                           const float* st, int ca0, bool row_ok, int first_ok,
                                           float c, uint32_t* pp, uint32_t* ds) {
+  const float2 c2 = make_float2(c, c);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int ca = ca0 + 2 * i;  // query column within the tile
-    const float sa = __uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]);
-    const float sb = __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]);
-    const float ga = __uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]);
-    const float gb = __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]);
-    const float2 l2 = *reinterpret_cast<const float2*>(st + ca);
-    const float2 dd = *reinterpret_cast<const float2*>(st + kT + ca);
-    float pa = ex2_approx(fmaf(sa, c, -l2.x));
-    float pb = ex2_approx(fmaf(sb, c, -l2.y));
+    const float2 sv = make_float2(__uint_as_float(i < 16 ? s0[2 * i] : s1[2 * i - 32]),
+                                  __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]));
+    const float2 gv = make_float2(__uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]),
+                                  __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]));
+    const float2 nl2 = *reinterpret_cast<const float2*>(st + ca);
+    const float2 nd2 = *reinterpret_cast<const float2*>(st + kT + ca);
+    float2 pv = ffma2(sv, c2, nl2);
+    pv.x = ex2_approx(pv.x);
+    pv.y = ex2_approx(pv.y);
     if (kMask) {
-      if (!row_ok || ca < first_ok) pa = 0.f;
-      if (!row_ok || ca + 1 < first_ok) pb = 0.f;
+      if (!row_ok || ca < first_ok) pv.x = 0.f;
+      if (!row_ok || ca + 1 < first_ok) pv.y = 0.f;
     }
-    pp[i] = pack_bf16x2(pa, pb);
-    ds[i] = pack_bf16x2(pa * (ga - dd.x), pb * (gb - dd.y));
+    pp[i] = pack_bf16x2(pv.x, pv.y);
+    const float2 dv = fmul2(pv, fadd2(gv, nd2));
+    ds[i] = pack_bf16x2(dv.x, dv.y);
   }
 }
 
@@ -322,8 +329,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const bool live = row < p.Nq;
     const float* tile_st =
         p.stats + ((static_cast<int64_t>(b) * p.H + h) * gridDim.x + qt) * (2 * kT);
-    const float lse2 = __ldg(tile_st + r_local);  // +inf past Nq
-    const float Dr = __ldg(tile_st + kT + r_local);
+    const float nl = __ldg(tile_st + r_local);  // -lse2; -inf past Nq
+    const float nd = __ldg(tile_st + kT + r_local);  // -D
     const float c = p.scale * kLog2e;
     const int limit = (p.mask == 1) ? min(row, L - 1) : L - 1;  // keys j <= limit
     bool ok = true;
@@ -351,9 +358,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int col0 = j * kT + half * 64;
       uint32_t ds[32];
       if (warp_all(col0 + 63 <= limit))  // no key of this half is masked for any row here
-        dq_half<false>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
+        dq_half<false>(s0, s1, g0, g1, col0, limit, c, nl, nd, ds);
       else
-        dq_half<true>(s0, s1, g0, g1, col0, limit, c, lse2, Dr, ds);
+        dq_half<true>(s0, s1, g0, g1, col0, limit, c, nl, nd, ds);
       // dS_j goes to buffer j % 2, which dQ += dS_{j-2} K_{j-2} must have finished reading
       if (j > 1 && !warp_all(mbar_wait(bar(kQBarDQDone + (j & 1)), ((j >> 1) - 1) & 1,
                                        p.timeout_ns))) {
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // ============================================================================ dkdv kernel
-// smem: K, V (once), Q ring, dO ring, lse2/D ring (2 x 128 floats per stage), barriers
+// smem: K, V (once), Q ring, dO ring, -lse2/-D ring (2 x 128 floats per stage), barriers
 constexpr int kKOffK = 0;
 constexpr int kKOffV = kKOffK + kTileBytes;
 constexpr int kKOffQ = kKOffV + kTileBytes;
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
           ok = false;
           break;
         }
-        // Q_t, dO_t and the tile's statistics (lse2 and D, 1 KB) on one barrier
+        // Q_t, dO_t and the tile's statistics (-lse2 and -D, 1 KB) on one barrier
         mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes + 2 * kT * 4);
         tma_load_4d(smem_u32(smem + kKOffQ + s * kTileBytes), &tmQ, bar(kKBarQ + s), 0, qt * kT,
                     h, b);

@@ -52,8 +52,9 @@ __global__ void __launch_bounds__(kWarps * 32)
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
                            int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
                            const float* __restrict__ lse, int rows) {
-  // lse != null: the per-tile layout {lse * log2 e [128], D [128]} over rows up to a whole
-  // number of 128-row tiles; otherwise D alone as [B, H, Nq]
+  // lse != null: the per-tile layout {-lse * log2 e [128], -D [128]} (negated, so the
+  // tensor-core kernels add them in paired fp32 instructions) over rows up to a whole number
+  // of 128-row tiles; otherwise D alone as [B, H, Nq]
   const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -72,8 +73,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     Dv[bh * Nq + row] = acc;
   } else {
     float* tile = Dv + (bh * (rows / 128) + row / 128) * 256;
-    tile[row % 128] = row < Nq ? __ldg(lse + bh * Nq + row) * 1.4426950408889634f : INFINITY;
-    tile[128 + row % 128] = acc;
+    tile[row % 128] = row < Nq ? -(__ldg(lse + bh * Nq + row) * 1.4426950408889634f) : -INFINITY;
+    tile[128 + row % 128] = -acc;
   }
 }
 
