@@ -661,7 +661,7 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   // y = LayerNorm(x_q + A)
   mark(3);
   cudaError_t e =
-      mha::launch_residual_layernorm(dtype, Mq, D, ln_eps, x_q, A, gamma, beta, y, stream);
+      mha::launch_residual_layernorm(dtype, Mq, D, ln_eps, x_q, A, gamma, beta, y, ctx, stream);
   mark(4);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -703,7 +703,7 @@ int ffn_impl(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, con
   if (st != MHA_OK) return st;
   mark(2);
   // y = LayerNorm(x + F)
-  cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, ln_eps, x, F, gamma, beta, y, stream);
+  cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, ln_eps, x, F, gamma, beta, y, ctx, stream);
   mark(3);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -859,7 +859,7 @@ int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x
   DevCtx ctx;
   const int st = device_ctx(&ctx);
   if (st != MHA_OK) return st;
-  cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, eps, x, a, gamma, beta, y, stream);
+  cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, eps, x, a, gamma, beta, y, ctx, stream);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 

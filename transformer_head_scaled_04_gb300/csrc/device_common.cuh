@@ -131,6 +131,12 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+// Ask L2 to fetch `bytes` (a multiple of 16; 16-byte aligned) from global memory ahead of use.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
 // Tiled bulk store of a box from shared memory to global (bulk-group completion); the
 // innermost coordinate c0 must be a multiple of 16 bytes and no coordinate negative.  Rows
 // past the tensor's extent are not written.

@@ -122,9 +122,11 @@ cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C
                              int64_t ldy, int R_pad, cudaStream_t s);
 
 // ---- residual + LayerNorm: y = LN(x + a) * gamma + beta
+// bf16: persistent warps over rows with an L2 prefetch of each warp's next row; fp32: one
+// warp per row.  x, a, y contiguous [M, D], 16-byte aligned, D % 8 == 0, D <= 2048.
 cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,
                                       const void* a, const void* gamma, const void* beta,
-                                      void* y, cudaStream_t s);
+                                      void* y, const DevCtx& ctx, cudaStream_t s);
 
 // ---- bounded-wait self test (waits on a barrier nothing completes)
 cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t s);

@@ -8,6 +8,9 @@
 // passes (mean, then the sum of squared deviations) and the normalising write.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
+#include "device_common.cuh"
 #include "launchers.h"
 
 namespace mha {
@@ -119,6 +122,115 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
   }
 }
 
+// bf16 rows, persistent: warp w of the grid takes rows w, w + W, w + 2W, ... (W warps in the
+// grid) and asks L2 for its next row of x and a (one bulk prefetch each) before it loads and
+// normalises the current one, so the loads of the current row mostly hit L2 and DRAM keeps
+// far more bytes in flight than the registers of the resident warps could hold.
+template <int NIT>
+__global__ void __launch_bounds__(kRowsPerBlock * 32)
+    residual_layernorm_stream_kernel(const __nv_bfloat16* __restrict__ x,
+                                     const __nv_bfloat16* __restrict__ a,
+                                     const __nv_bfloat16* __restrict__ gamma,
+                                     const __nv_bfloat16* __restrict__ beta,
+                                     __nv_bfloat16* __restrict__ y, int M, int D, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * kRowsPerBlock;
+  int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const uint32_t row_bytes = static_cast<uint32_t>(D) * 2;
+  if (lane == 0 && row < M) {
+    prefetch_l2(x + static_cast<int64_t>(row) * D, row_bytes);
+    prefetch_l2(a + static_cast<int64_t>(row) * D, row_bytes);
+  }
+  for (; row < M; row += W) {
+    const int nxt = row + W;
+    if (lane == 0 && nxt < M) {
+      prefetch_l2(x + static_cast<int64_t>(nxt) * D, row_bytes);
+      prefetch_l2(a + static_cast<int64_t>(nxt) * D, row_bytes);
+    }
+    const int64_t base = static_cast<int64_t>(row) * D;
+    float r[NIT][8];
+    float sum = 0.f;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int col = (it * 32 + lane) * 8;
+      if (col < D) {
+        float xv[8], av[8];
+        Vec8<__nv_bfloat16>::load(x + base + col, xv);
+        Vec8<__nv_bfloat16>::load(a + base + col, av);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          r[it][e] = xv[e] + av[e];
+          sum += r[it][e];
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float mean = sum / static_cast<float>(D);
+    float sq = 0.f;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int col = (it * 32 + lane) * 8;
+      if (col < D) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = r[it][e] - mean;
+          sq = fmaf(d, d, sq);
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    const float rstd = 1.0f / sqrtf(sq / static_cast<float>(D) + eps);
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      const int col = (it * 32 + lane) * 8;
+      if (col < D) {
+        float g[8], bt[8], out[8];
+        if (gamma) {
+          Vec8<__nv_bfloat16>::load(gamma + col, g);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) g[e] = 1.f;
+        }
+        if (beta) {
+          Vec8<__nv_bfloat16>::load(beta + col, bt);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bt[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = (r[it][e] - mean) * rstd * g[e] + bt[e];
+        Vec8<__nv_bfloat16>::store(y + base + col, out);
+      }
+    }
+  }
+}
+
+cudaError_t launch_stream(int M, int D, float eps, const void* x, const void* a,
+                          const void* gamma, const void* beta, void* y, const DevCtx& ctx,
+                          cudaStream_t s) {
+  const int blocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
+  const int grid = std::min(blocks, 4 * std::max(ctx.num_sms, 1));  // 4 blocks fit an SM
+  auto go = [&](auto kern) {
+    kern<<<grid, kRowsPerBlock * 32, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
+        static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(beta),
+        static_cast<__nv_bfloat16*>(y), M, D, eps);
+    return cudaGetLastError();
+  };
+  switch ((D + 255) / 256) {
+    case 1: return go(residual_layernorm_stream_kernel<1>);
+    case 2: return go(residual_layernorm_stream_kernel<2>);
+    case 3: return go(residual_layernorm_stream_kernel<3>);
+    case 4: return go(residual_layernorm_stream_kernel<4>);
+    case 5: return go(residual_layernorm_stream_kernel<5>);
+    case 6: return go(residual_layernorm_stream_kernel<6>);
+    case 7: return go(residual_layernorm_stream_kernel<7>);
+    default: return go(residual_layernorm_stream_kernel<8>);
+  }
+}
+
 template <typename T>
 cudaError_t launch_t(int M, int D, float eps, const void* x, const void* a, const void* gamma,
                      const void* beta, void* y, cudaStream_t s) {
@@ -147,8 +259,8 @@ cudaError_t launch_t(int M, int D, float eps, const void* x, const void* a, cons
 
 cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const void* x,
                                       const void* a, const void* gamma, const void* beta,
-                                      void* y, cudaStream_t s) {
-  if (dtype == 1) return launch_t<__nv_bfloat16>(M, D, eps, x, a, gamma, beta, y, s);
+                                      void* y, const DevCtx& ctx, cudaStream_t s) {
+  if (dtype == 1) return launch_stream(M, D, eps, x, a, gamma, beta, y, ctx, s);
   return launch_t<float>(M, D, eps, x, a, gamma, beta, y, s);
 }
 
