@@ -91,6 +91,22 @@ def test_sdpa_bf16(B, H, Nq, Nk, mask, kl):
                 assert np.all(host(O)[b] == 0.0)
 
 
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_sdpa_bf16_more_blocks_than_sms(mask):
+    """More 256-row query blocks than SMs, with a short last round, so that persistent blocks
+    take over blocks that have not started: every row of O and of the log-sum-exp against
+    the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, N = 1, sms + 3, 512  # 2 blocks per head: one full round and 6 blocks more
+    Q, K, V, _ = si.draw_sdpa(B, H, N, N, dtype="bf16", seed=4242)
+    O, lse = mha.sdpa_with_lse(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
+                               to_dev(V, torch.bfloat16), mask)
+    ref = oracle.sdpa_ref(Q, K, V, mask)
+    assert_bf16_close(host(O), ref, f"sdpa bf16 {H} heads {mask}")
+    lse_ref = oracle.sdpa_lse_ref(Q, K, mask)
+    assert np.allclose(host(lse), lse_ref, rtol=0, atol=2e-3)
+
+
 def test_sdpa_bf16_large_scores_stay_finite():
     # scores of +-40 whose tile maxima grow along the keys: later tiles are exponentiated
     # against the smaller first-tile max (large but finite exponentials)
