@@ -853,8 +853,17 @@ def run_profile_case(args):
         C.check(lib.mha_linear_fwd(B * N, 3 * Dm, Dm, C.MHA_BF16, vp(x), Dm, vp(wq), None, vp(y),
                                    3 * Dm, sp), "mha_linear_fwd")
 
+    # the residual LayerNorm of the same rows: y = LN(x + a) over d_model features
+    a_ln = torch.randn((B * N, Dm), device=dev, generator=g).to(bf)
+    y_ln = torch.empty_like(a_ln)
+
+    def layernorm():
+        C.check(lib.mha_residual_layernorm_fwd(B * N, Dm, C.MHA_BF16, 1e-5, vp(x), vp(a_ln), None,
+                                               None, vp(y_ln), sp), "mha_residual_layernorm_fwd")
+
     fwd()
-    fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv}[args.profile_case]
+    fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv,
+          "layernorm": layernorm}[args.profile_case]
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -879,7 +888,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
-    ap.add_argument("--profile-case", choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv"], default=None,
+    ap.add_argument("--profile-case", choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm"], default=None,
                     help="run only this kernel family (for ncu captures), no bench line")
     ap.add_argument("--batch", type=int, default=4, help="batch of --profile-case")
     args = ap.parse_args()
