@@ -351,6 +351,21 @@ def test_layer_bf16_with_biases_and_affine(mask, cross, Nq, Nk):
     assert_bf16_close(host(y), ref_layer(inp, w), f"layer bf16 affine {mask} cross={cross}")
 
 
+@pytest.mark.parametrize("cross", [False, True])
+def test_layer_bf16_more_attention_units_than_sms(cross):
+    """More attention units (256-row query blocks) than SMs and a last round that fills at
+    most half of them, self- and cross-attention: the whole output against the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B = (sms + 8) // 4 + 1  # 2 heads x 2 query blocks per batch element
+    units = 4 * B
+    assert units > sms and 0 < units % sms <= sms // 2
+    w = si.Workload("t", "layer", "bf16", B=B, H=2, Nq=512, Nk=512 if not cross else 700,
+                    cross=cross, seed=91)
+    inp = si.draw_layer(w, affine=True)
+    y = run_layer(inp, w)
+    assert_bf16_close(host(y), ref_layer(inp, w), f"layer bf16 {B}x512 cross={cross}")
+
+
 @pytest.mark.parametrize("mask,cross,H,dk", [("none", False, 2, 64), ("causal", False, 3, 32),
                                              ("key_padding", True, 4, 16)])
 def test_layer_f32(mask, cross, H, dk):
