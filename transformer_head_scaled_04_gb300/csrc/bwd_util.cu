@@ -11,7 +11,10 @@
 //   colsum_partials + reduce_partials: a bias gradient, the column sums of a gradient matrix
 //   transpose: Y = X^T with the reduced dimension padded by zero rows to a whole number of
 //                  64-wide K slices, so the weight-gradient products run on the same GEMM
+//                  (bf16: 64 x 64 tiles moved as 16-byte vectors)
 #include <cuda_bf16.h>
+
+#include <cstdint>
 
 #include "launchers.h"
 
@@ -165,6 +168,48 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// bf16, 64 x 64 tiles moved as 16-byte vectors: each thread loads 8 consecutive elements of a
+// row of X, and stores 8 consecutive elements of a row of Y gathered from 8 rows of the tile
+// (row pitch 66 elements: both the 4-byte writes and the 2-byte gathers are conflict-free).
+// Needs C, ldx, ldy and R_pad multiples of 8 and 16-byte aligned X and Y.
+constexpr int kTp = 64;
+constexpr int kTpPitch = kTp + 2;
+__global__ void __launch_bounds__(256)
+    transpose_v8_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int R, int C,
+                        __nv_bfloat16* __restrict__ Y, int64_t ldy, int R_pad) {
+  __shared__ uint16_t tile[kTp * kTpPitch];
+  const int r0 = blockIdx.x * kTp, c0 = blockIdx.y * kTp;
+  const int t = threadIdx.x;
+  const int sub = (t & 7) * 8;  // 8-element chunk within a 64-wide row
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int row = (t >> 3) + 32 * pass;
+    const int r = r0 + row, c = c0 + sub;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);  // rows past R read as zeros (the padding)
+    if (r < R && c < C) v = *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(r) * ldx + c);
+    uint32_t* d = reinterpret_cast<uint32_t*>(tile + row * kTpPitch + sub);
+    d[0] = v.x;
+    d[1] = v.y;
+    d[2] = v.z;
+    d[3] = v.w;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int oc = (t >> 3) + 32 * pass;  // row of Y = column of X
+    const int c = c0 + oc, r = r0 + sub;
+    if (c < C && r < R_pad) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = static_cast<uint32_t>(tile[(sub + 2 * i) * kTpPitch + oc]) |
+               (static_cast<uint32_t>(tile[(sub + 2 * i + 1) * kTpPitch + oc]) << 16);
+      *reinterpret_cast<uint4*>(Y + static_cast<int64_t>(c) * ldy + r) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 constexpr int kChunkRows = 256;
 
 }  // namespace
@@ -232,6 +277,14 @@ cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
 
 cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C, void* Y,
                              int64_t ldy, int R_pad, cudaStream_t s) {
+  const bool v8 = dtype == 1 && C % 8 == 0 && ldx % 8 == 0 && ldy % 8 == 0 && R_pad % 8 == 0 &&
+                  reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(Y) % 16 == 0;
+  if (v8) {
+    const dim3 g64((R_pad + kTp - 1) / kTp, (C + kTp - 1) / kTp);
+    transpose_v8_kernel<<<g64, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), ldx, R, C,
+                                             static_cast<__nv_bfloat16*>(Y), ldy, R_pad);
+    return cudaGetLastError();
+  }
   const dim3 grid((R_pad + 31) / 32, (C + 31) / 32);
   if (dtype == 1)
     transpose_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
