@@ -168,6 +168,173 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- bf16 with 16-byte vectors (D, N, ld multiples of 8; 16-byte aligned rows)
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+// layernorm_bwd for bf16: one warp per row, each lane 8 consecutive features per 256
+template <int NIT>
+__global__ void __launch_bounds__(kRows * 32)
+    layernorm_bwd_v8_kernel(const __nv_bfloat16* __restrict__ x,
+                            const __nv_bfloat16* __restrict__ a,
+                            const __nv_bfloat16* __restrict__ gamma,
+                            const __nv_bfloat16* __restrict__ dy, __nv_bfloat16* __restrict__ dr,
+                            float2* __restrict__ stats, int M, int D, float eps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kRows + warp;
+  if (row >= M) return;
+  const int64_t base = static_cast<int64_t>(row) * D;
+  float r[NIT][8], g[NIT][8];
+  float sum = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int col = (it * 32 + lane) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[it][e] = g[it][e] = 0.f;
+    if (col < D) {
+      float xv[8], av[8], dv[8], gv[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + base + col), xv);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(a + base + col), av);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(dy + base + col), dv);
+      if (gamma) {
+        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(gamma + col)), gv);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gv[e] = 1.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        r[it][e] = xv[e] + av[e];
+        g[it][e] = dv[e] * gv[e];
+        sum += r[it][e];
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float mean = sum / static_cast<float>(D);
+  float sq = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it)
+    if ((it * 32 + lane) * 8 < D) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sq = fmaf(r[it][e] - mean, r[it][e] - mean, sq);
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  const float rstd = 1.0f / sqrtf(sq / static_cast<float>(D) + eps);
+  float sg = 0.f, sgr = 0.f;
+#pragma unroll
+  for (int it = 0; it < NIT; ++it)
+    if ((it * 32 + lane) * 8 < D) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        r[it][e] = (r[it][e] - mean) * rstd;  // rhat
+        sg += g[it][e];
+        sgr = fmaf(g[it][e], r[it][e], sgr);
+      }
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sg += __shfl_xor_sync(0xffffffffu, sg, off);
+    sgr += __shfl_xor_sync(0xffffffffu, sgr, off);
+  }
+  const float mg = sg / static_cast<float>(D), mgr = sgr / static_cast<float>(D);
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const int col = (it * 32 + lane) * 8;
+    if (col < D) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (g[it][e] - mg - r[it][e] * mgr) * rstd;
+      *reinterpret_cast<uint4*>(dr + base + col) = f32_to_bf16x8(o);
+    }
+  }
+  if (lane == 0) stats[row] = make_float2(mean, rstd);
+}
+
+// Column partial sums over a chunk of rows for bf16, 8 consecutive columns per thread:
+// blockDim (128, kRowGroups); row group y takes rows r0 + y, r0 + y + kRowGroups, ...; the
+// groups' sums are added in group order (deterministic).  kTerms = 3: dy * rhat, dy and dr
+// (LayerNorm parameters and db_o); kTerms = 1: the column sums of X (a bias gradient).
+constexpr int kRowGroups = 4;
+template <int kTerms>
+__global__ void __launch_bounds__(128 * kRowGroups)
+    colsum_v8_kernel(const __nv_bfloat16* __restrict__ X, int64_t ld,
+                     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ a,
+                     const __nv_bfloat16* __restrict__ dr, const float2* __restrict__ stats,
+                     int M, int N, int rows_per_chunk, float* __restrict__ part) {
+  __shared__ float red[kRowGroups - 1][kTerms][128 * 8];
+  const int col = (blockIdx.x * 128 + threadIdx.x) * 8;
+  const int chunk = blockIdx.y, grp = threadIdx.y;
+  const int r0 = chunk * rows_per_chunk, r1 = min(r0 + rows_per_chunk, M);
+  float acc[kTerms][8];
+#pragma unroll
+  for (int k = 0; k < kTerms; ++k)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+  if (col < N) {
+    for (int r = r0 + grp; r < r1; r += kRowGroups) {
+      float d[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + static_cast<int64_t>(r) * ld + col), d);
+      if (kTerms == 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[0][e] += d[e];
+      } else {
+        const int64_t i = static_cast<int64_t>(r) * N + col;
+        const float2 st = stats[r];
+        float xv[8], av[8], rv[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + i), xv);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(a + i), av);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(dr + i), rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[0][e] = fmaf(d[e], (xv[e] + av[e] - st.x) * st.y, acc[0][e]);
+          acc[1][e] += d[e];
+          acc[kTerms - 1][e] += rv[e];
+        }
+      }
+    }
+  }
+  if (grp > 0) {
+#pragma unroll
+    for (int k = 0; k < kTerms; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) red[grp - 1][k][threadIdx.x * 8 + e] = acc[k][e];
+  }
+  __syncthreads();
+  if (grp == 0 && col < N) {
+#pragma unroll
+    for (int k = 0; k < kTerms; ++k) {
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float v = acc[k][e];
+#pragma unroll
+        for (int q = 0; q < kRowGroups - 1; ++q) v += red[q][k][threadIdx.x * 8 + e];
+        o[e] = v;
+      }
+      float4* dst = reinterpret_cast<float4*>(part + (static_cast<int64_t>(chunk) * kTerms + k) * N + col);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
 // bf16, 64 x 64 tiles moved as 16-byte vectors: each thread loads 8 consecutive elements of a
 // row of X, and stores 8 consecutive elements of a row of Y gathered from 8 rows of the tile
 // (row pitch 66 elements: both the 4-byte writes and the 2-byte gathers are conflict-free).
@@ -222,6 +389,29 @@ cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void*
   const dim3 grid_rows((M + kRows - 1) / kRows);
   const int nit = (D + 31) / 32;
   const dim3 grid_cols((D + 255) / 256, bwd_row_chunks(M));
+  auto al16 = [](const void* q) { return q == nullptr || reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+  if (dtype == 1 && D % 8 == 0 && D <= 2048 && al16(x) && al16(a) && al16(gamma) && al16(dy) &&
+      al16(dr)) {
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const auto* ab = static_cast<const __nv_bfloat16*>(a);
+    const auto* gb = static_cast<const __nv_bfloat16*>(gamma);
+    const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
+    auto* drb = static_cast<__nv_bfloat16*>(dr);
+    switch ((D + 255) / 256) {
+      case 1: layernorm_bwd_v8_kernel<1><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 2: layernorm_bwd_v8_kernel<2><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 3: layernorm_bwd_v8_kernel<3><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 4: layernorm_bwd_v8_kernel<4><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 5: case 6: layernorm_bwd_v8_kernel<6><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      default: layernorm_bwd_v8_kernel<8><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const dim3 g8((D + 1023) / 1024, bwd_row_chunks(M));
+    colsum_v8_kernel<3><<<g8, dim3(128, kRowGroups), 0, s>>>(dyb, D, xb, ab, drb, stats, M, D,
+                                                             kChunkRows, part);
+    return cudaGetLastError();
+  }
 #define MHA_LN_BWD(T, N)                                                                    \
   layernorm_bwd_kernel<T, N><<<grid_rows, kRows * 32, 0, s>>>(                              \
       static_cast<const T*>(x), static_cast<const T*>(a), static_cast<const T*>(gamma),     \
@@ -253,6 +443,13 @@ cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void*
 
 cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, int N,
                                    float* part, cudaStream_t s) {
+  if (dtype == 1 && N % 8 == 0 && ld % 8 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0) {
+    const dim3 g8((N + 1023) / 1024, bwd_row_chunks(M));
+    colsum_v8_kernel<1><<<g8, dim3(128, kRowGroups), 0, s>>>(
+        static_cast<const __nv_bfloat16*>(X), ld, nullptr, nullptr, nullptr, nullptr, M, N,
+        kChunkRows, part);
+    return cudaGetLastError();
+  }
   const dim3 grid((N + 255) / 256, bwd_row_chunks(M));
   if (dtype == 1)
     colsum_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
