@@ -73,6 +73,62 @@ def window_pairs(B: int, H: int, N: int, window: int) -> int:
     return int(B * H * per_row.sum())
 
 
+def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
+    """The base model's sublayer workloads (d_model=512, h=8) and the small fp32 attention
+    call: one mha_layer_fwd (mha_sdpa_fwd) per step, L2 flushed before each, CUDA events.
+    These are launch- and latency-bound sizes; the big workload is the throughput case."""
+    import torch
+
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    out = {}
+
+    def timeit(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    for name in ("enc_self_base_b32_n128", "dec_causal_base_b32_n256",
+                 "cross_pad_base_b32_q128_k256"):
+        w = si.WORKLOADS[name]
+        inp = si.draw_layer(w)
+        t = {k: (None if v is None else torch.from_numpy(v).to(dev, torch.bfloat16))
+             for k, v in inp.items() if k != "key_len"}
+        kl = None if inp["key_len"] is None else torch.from_numpy(inp["key_len"]).to(dev)
+        n = ctypes.c_size_t(0)
+        C.check(lib.mha_layer_workspace_size(w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v,
+                                             C.MHA_BF16, ctypes.byref(n)), "workspace")
+        ws = torch.empty(max(n.value, 256), dtype=torch.uint8, device=dev)
+        y = torch.empty_like(t["x_q"])
+        a = (w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16, C.MASKS[w.mask], vp(kl), 1e-5,
+             vp(t["x_q"]), vp(t["x_kv"]), vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]),
+             vp(t["b_o"]), vp(t["gamma"]), vp(t["beta"]), vp(y), vp(ws), ws.numel(), sp)
+        ms = timeit(lambda: C.check(lib.mha_layer_fwd(*a), "mha_layer_fwd"))
+        fl = layer_flops(w, w.mask, inp["key_len"])
+        out[name] = {"ms": ms, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+                     "tokens_per_s": w.B * w.Nq / (ms * 1e-3), "flops_per_step": fl}
+    # the small fp32 attention call (B=1, h=8, n=32, d=64): latency
+    w = si.WORKLOADS["sdpa_f32_b1_h8_n32"]
+    Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="f32", seed=w.seed)
+    tq, tk, tv = (torch.from_numpy(np.ascontiguousarray(x)).to(dev, torch.float32)
+                  for x in (Q, K, V))
+    O = torch.empty_like(tq)
+    a = (w.B, w.H, w.Nq, w.Nk, 64, 64, C.MHA_F32, 0, None, 0.0, vp(tq), vp(tk), vp(tv), vp(O),
+         None, sp)
+    ms = timeit(lambda: C.check(lib.mha_sdpa_fwd(*a), "mha_sdpa_fwd"))
+    out["sdpa_f32_b1_h8_n32"] = {"us": ms * 1e3, "flops_per_call": sdpa_flops(w, "none")}
+    return out
+
+
 def measure_window(lib, C, dev, stream, flush, steps, warmup, peak, window=WINDOW):
     """Restricted self-attention on the big model's heads at n = 4096 (neighbourhood
     2 * window + 1), as one attention launch on contiguous [B, H, N, 64] Q, K, V."""
@@ -676,6 +732,7 @@ def run_ours(args):
     # the feed-forward sublayer and the whole encoder layer on the same tokens
     ffn = measure_ffn(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
     window = measure_window(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
+    base = measure_base_configs(lib, C, dev, stream, flush, args.steps, args.warmup)
     window["speedup_vs_full_attention_time"] = sdpa_ms / window["ms"]
     decode = measure_decode(lib, C, dev, stream, flush, args.steps, args.warmup,
                             float(peaks["hbm_gbs"]))
@@ -793,6 +850,7 @@ def run_ours(args):
         "encoder_layer": encoder,
         "backward": backward,
         "window": window,
+        "base_configs": base,
         "decode": decode,
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -6,10 +6,13 @@
 //   ("Attention Is All You Need", lettle.cn translation, 3.2.1 缩放点积注意力;
 //    "Transformer：抛弃循环与卷积的序列建模", Self-Attention的优势).
 //
-// One warp per query row.  Lane k handles keys k, k+32, ...: pass 1 takes the row maximum
-// of the allowed scores, pass 2 recomputes each score, accumulates exp(s - max) and the
-// weighted value sum in fp32 registers, and a butterfly reduction across the warp joins
-// the lanes' partial sums.  expf is the accurate CUDA function (no fast-math).
+// One warp per query row, eight rows (of one batch element and head) per block.  The block
+// walks the keys its rows may see in chunks of 32: the chunk's K and V rows are staged in
+// shared memory with coalesced loads (row pitch d + 1: conflict-free per-lane row reads),
+// lane k scores key k of the chunk, and an online softmax (running max m, sum l, the value
+// accumulator rescaled by exp(m_old - m_new) when the max grows) folds the chunk in: each
+// weight is broadcast across the warp and lane k accumulates value features k, k + 32, ...
+// expf is the accurate CUDA function (no fast-math).
 #include <cmath>
 
 #include "launchers.h"
@@ -19,6 +22,8 @@ namespace {
 
 constexpr int kMaxD = 128;
 constexpr int kWarps = 8;
+constexpr int kChunk = 32;             // keys per shared-memory chunk
+constexpr int kPitch = kMaxD + 1;      // padded row pitch of a staged K / V row
 
 __global__ void __launch_bounds__(kWarps * 32)
     sdpa_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
@@ -29,77 +34,105 @@ __global__ void __launch_bounds__(kWarps * 32)
                     int64_t kn, int64_t kd, int64_t vb, int64_t vh, int64_t vn, int64_t vd,
                     int64_t ob, int64_t oh, int64_t on, int64_t od) {
   __shared__ float sq[kWarps][kMaxD];
+  __shared__ float sk[kChunk * kPitch];
+  __shared__ float sv[kChunk * kPitch];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kWarps + warp;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
-  if (row >= Nq) return;  // whole warp leaves together
+  const bool live = row < Nq;  // warps past Nq still help stage the chunks
 
-  const float* q = Q + b * qb + h * qh + static_cast<int64_t>(row) * qn;
-  for (int t = lane; t < d_k; t += 32) sq[warp][t] = q[t * qd];
-  __syncwarp();
-
-  int limit;  // allowed keys: first <= j <= limit
-  int first = 0;
-  if (mask == 1) {
-    limit = row;
-  } else if (mask == 2) {
-    limit = min(max(key_len[b], 0), Nk) - 1;
-  } else if (mask == kMaskWindow) {
-    limit = min(row + window, Nk - 1);
-    first = max(row - window, 0);
-  } else if (mask == kMaskCausalCache) {
-    // the Nq queries are the newest of L cached positions: row sits at L - Nq + row
-    const int L = min(max(key_len[b], 0), Nk);
-    limit = min(L - Nq + row, L - 1);
-  } else {
-    limit = Nk - 1;
+  if (live) {
+    const float* q = Q + b * qb + h * qh + static_cast<int64_t>(row) * qn;
+    for (int t = lane; t < d_k; t += 32) sq[warp][t] = q[t * qd];
   }
-  const int nkeys = min(limit + 1, Nk);
+
+  // allowed keys of a row: first <= j <= limit
+  auto bounds = [&](int r, int& first, int& limit) {
+    first = 0;
+    if (mask == 1) {
+      limit = r;
+    } else if (mask == 2) {
+      limit = min(max(key_len[b], 0), Nk) - 1;
+    } else if (mask == kMaskWindow) {
+      limit = min(r + window, Nk - 1);
+      first = max(r - window, 0);
+    } else if (mask == kMaskCausalCache) {
+      // the Nq queries are the newest of L cached positions: row r sits at L - Nq + r
+      const int L = min(max(key_len[b], 0), Nk);
+      limit = min(L - Nq + r, L - 1);
+    } else {
+      limit = Nk - 1;
+    }
+    limit = min(limit, Nk - 1);
+  };
+  int first, limit;
+  bounds(min(row, Nq - 1), first, limit);
+  // the keys any row of the block may see: rows are consecutive and both bounds grow with r
+  int blk_first, blk_limit, last_first, last_limit;
+  bounds(blockIdx.x * kWarps, blk_first, blk_limit);
+  bounds(min(blockIdx.x * kWarps + kWarps - 1, Nq - 1), last_first, last_limit);
+  blk_first = max(min(blk_first, last_first), 0);
+  blk_limit = max(blk_limit, last_limit);
 
   const float* kbase = K + b * kb + h * kh;
   const float* vbase = V + b * vb + h * vh;
-  auto score = [&](int j) {
-    const float* kr = kbase + static_cast<int64_t>(j) * kn;
-    float acc = 0.f;
-    for (int t = 0; t < d_k; ++t) acc = fmaf(sq[warp][t], kr[t * kd], acc);
-    return acc * scale;
-  };
+  float m = -INFINITY, l = 0.f;
+  float acc[kMaxD / 32];  // value features lane, lane + 32, ...
+#pragma unroll
+  for (int i = 0; i < kMaxD / 32; ++i) acc[i] = 0.f;
 
-  float m = -INFINITY;
-  for (int j = first + lane; j < nkeys; j += 32) m = fmaxf(m, score(j));
+  for (int j0 = blk_first; j0 <= blk_limit; j0 += kChunk) {
+    __syncthreads();  // the previous chunk is consumed
+    const int nj = min(kChunk, blk_limit + 1 - j0);
+    for (int e = threadIdx.x; e < nj * d_k; e += kWarps * 32) {
+      const int jj = e / d_k, t = e - jj * d_k;
+      sk[jj * kPitch + t] = kbase[static_cast<int64_t>(j0 + jj) * kn + t * kd];
+    }
+    for (int e = threadIdx.x; e < nj * d_v; e += kWarps * 32) {
+      const int jj = e / d_v, t = e - jj * d_v;
+      sv[jj * kPitch + t] = vbase[static_cast<int64_t>(j0 + jj) * vn + t * vd];
+    }
+    __syncthreads();
+    if (!live) continue;
+    const int j = j0 + lane;
+    const bool ok = lane < nj && j >= first && j <= limit;
+    float sc = -INFINITY;
+    if (ok) {
+      float a = 0.f;
+      for (int t = 0; t < d_k; ++t) a = fmaf(sq[warp][t], sk[lane * kPitch + t], a);
+      sc = a * scale;
+    }
+    float cm = sc;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-
-  float l = 0.f;
-  float acc[kMaxD];
+    for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    if (cm == -INFINITY) continue;  // no allowed key of this row in the chunk
+    const float m_new = fmaxf(m, cm);
+    const float alpha = (m == -INFINITY) ? 0.f : expf(m - m_new);
+    m = m_new;
+    const float pj = ok ? expf(sc - m) : 0.f;
+    l = l * alpha + pj;
 #pragma unroll
-  for (int t = 0; t < kMaxD; ++t) acc[t] = 0.f;
-  for (int j = first + lane; j < nkeys; j += 32) {
-    const float pj = expf(score(j) - m);
-    l += pj;
-    const float* vr = vbase + static_cast<int64_t>(j) * vn;
+    for (int i = 0; i < kMaxD / 32; ++i) acc[i] *= alpha;
+    for (int jj = 0; jj < nj; ++jj) {
+      const float p = __shfl_sync(0xffffffffu, pj, jj);
 #pragma unroll
-    for (int t = 0; t < kMaxD; ++t)
-      if (t < d_v) acc[t] = fmaf(pj, vr[t * vd], acc[t]);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-  const float inv = (nkeys > first && l > 0.f) ? 1.f / l : 0.f;  // no allowed key: zeros
-  if (lse != nullptr && lane == 0)
-    lse[(static_cast<int64_t>(b) * gridDim.y + h) * Nq + row] =
-        (nkeys > first && l > 0.f) ? m + logf(l) : INFINITY;
-  float* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
-#pragma unroll
-  for (int t = 0; t < kMaxD; ++t) {
-    if (t < d_v) {  // d_v is uniform across the warp
-      float v = acc[t];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == (t & 31)) o[t * od] = v * inv;
+      for (int i = 0; i < kMaxD / 32; ++i)
+        if (lane + 32 * i < d_v) acc[i] = fmaf(p, sv[jj * kPitch + lane + 32 * i], acc[i]);
     }
   }
+  if (!live) return;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  const bool any = m != -INFINITY && l > 0.f;
+  const float inv = any ? 1.f / l : 0.f;  // no allowed key: zeros
+  if (lse != nullptr && lane == 0)
+    lse[(static_cast<int64_t>(b) * gridDim.y + h) * Nq + row] = any ? m + logf(l) : INFINITY;
+  float* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
+#pragma unroll
+  for (int i = 0; i < kMaxD / 32; ++i)
+    if (lane + 32 * i < d_v) o[(lane + 32 * i) * od] = acc[i] * inv;
 }
 
 }  // namespace
