@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "mha.h"
 #include "device_common.cuh"
@@ -78,6 +79,38 @@ int device_ctx(DevCtx* ctx) {
   return MHA_OK;
 }
 
+// ------------------------------------------------------------------ kernel preparation
+}  // namespace
+
+namespace mha {
+cudaError_t prepare_kernel(const void* func, int smem_bytes, int* num_regs) {
+  struct Entry {
+    const void* func;
+    int dev, smem, regs;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& x : done)
+    if (x.func == func && x.dev == dev && x.smem == smem_bytes) {
+      if (num_regs != nullptr) *num_regs = x.regs;
+      return cudaSuccess;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, func);
+  if (e != cudaSuccess) return e;
+  done.push_back({func, dev, smem_bytes, fa.numRegs});
+  if (num_regs != nullptr) *num_regs = fa.numRegs;
+  return cudaSuccess;
+}
+}  // namespace mha
+
+namespace {
 // ------------------------------------------------------------------ TMA descriptors
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -278,8 +278,7 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUte
                       const void* R) {
   using S = GemmShape<BN>;
   auto kern = gemm_bias_bf16_kernel<BN, kRelu>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), S::kSmemBytes, nullptr);
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM);
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);

@@ -15,6 +15,11 @@ struct DevCtx {
   int num_sms;
 };
 
+// ---- per-kernel launch preparation: raises the kernel's dynamic shared-memory limit to
+// smem_bytes and reports its register count (num_regs may be null), once per (kernel, device);
+// later calls return the cached result without driver calls.
+cudaError_t prepare_kernel(const void* func, int smem_bytes, int* num_regs);
+
 // ---- projections: Y[M,N] = act(X[M,K] W[N,K]^T + bias), act = identity or ReLU (relu)
 // bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W
 // {K, N}, box {64, block_n}; tmY: 2-D map over Y {N, M}, box {64, 32}; all 128-byte swizzled.

@@ -713,15 +713,13 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.so_n = a.so[2];
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
-  cudaError_t e = cudaFuncSetAttribute(sdpa_fwd_bf16_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  int regs = 0;
+  cudaError_t e =
+      prepare_kernel(reinterpret_cast<const void*>(sdpa_fwd_bf16_kernel), kSmemBytes, &regs);
   if (e != cudaSuccess) return e;
   // The setmaxnreg split must fit in what the block is launched with, or the increase would
   // wait forever: refuse to launch if the compiled register count is too small for it.
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, sdpa_fwd_bf16_kernel);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
+  if (regs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
     return cudaErrorInvalidConfiguration;
   dim3 grid((a.Nq + 2 * kBQ - 1) / (2 * kBQ), a.H, a.B);
   sdpa_fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQ, tmK, tmV, tmO, p);

@@ -689,18 +689,15 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.stats = a.Dv;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
-  cudaError_t e = cudaFuncSetAttribute(sdpa_bwd_dq_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(sdpa_bwd_dq_kernel), kQSmem,
+                                 nullptr);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(sdpa_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kKSmem);
+  int regs = 0;
+  e = prepare_kernel(reinterpret_cast<const void*>(sdpa_bwd_dkdv_kernel), kKSmem, &regs);
   if (e != cudaSuccess) return e;
   // the dkdv kernel's setmaxnreg split must fit in what its blocks launch with, or the
   // increase would wait forever: refuse to launch if the compiled register count is too small
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, sdpa_bwd_dkdv_kernel);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs * kKThreads < kMathWarps * 32 * kKMathRegs + 4 * 32 * kKControlRegs)
+  if (regs * kKThreads < kMathWarps * 32 * kKMathRegs + 4 * 32 * kKControlRegs)
     return cudaErrorInvalidConfiguration;
   p.out0 = static_cast<__nv_bfloat16*>(a.dQ);
   p.o0_b = a.st[5][0];

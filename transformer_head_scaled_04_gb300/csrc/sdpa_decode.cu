@@ -265,8 +265,8 @@ cudaError_t launch_partial(const CUtensorMap& tmK, const CUtensorMap& tmV, const
                            dim3 grid, cudaStream_t s) {
   static_assert(NQ <= kDecodeMaxQ, "query rows beyond the decode limit");
   auto kern = decode_partial_kernel<NQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DecodeSmem<NQ>::kBytes);
+  cudaError_t e =
+      prepare_kernel(reinterpret_cast<const void*>(kern), DecodeSmem<NQ>::kBytes, nullptr);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, DecodeSmem<NQ>::kBytes, s>>>(tmK, tmV, p);
   return cudaGetLastError();
