@@ -114,8 +114,24 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
              vp(t["b_o"]), vp(t["gamma"]), vp(t["beta"]), vp(y), vp(ws), ws.numel(), sp)
         ms = timeit(lambda: C.check(lib.mha_layer_fwd(*a), "mha_layer_fwd"))
         fl = layer_flops(w, w.mask, inp["key_len"])
+        # where the time goes: events at the step boundaries (median over the steps)
+        per = []
+        for _ in range(steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            for e in evs:
+                e.record(stream)
+            flush.zero_()
+            arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
+            C.check(lib.mha_layer_fwd_timed(*a, ctypes.cast(arr, ctypes.c_void_p), 5),
+                    "mha_layer_fwd_timed")
+            evs[4].synchronize()
+            per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(4)])
+        med = np.median(np.array(per), axis=0)
         out[name] = {"ms": ms, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
-                     "tokens_per_s": w.B * w.Nq / (ms * 1e-3), "flops_per_step": fl}
+                     "tokens_per_s": w.B * w.Nq / (ms * 1e-3), "flops_per_step": fl,
+                     "step_breakdown_ms": {"qkv_proj": float(med[0]), "sdpa": float(med[1]),
+                                           "out_proj": float(med[2]),
+                                           "residual_layernorm": float(med[3])}}
     # the small fp32 attention call (B=1, h=8, n=32, d=64): latency
     w = si.WORKLOADS["sdpa_f32_b1_h8_n32"]
     Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="f32", seed=w.seed)

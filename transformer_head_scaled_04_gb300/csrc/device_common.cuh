@@ -176,6 +176,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ dependent launches
+// A kernel launched with programmatic stream serialization may start while the previous
+// kernel of the stream is still running: pdl_launch_dependents lets the next kernel's blocks
+// be scheduled as SMs free up, and pdl_wait blocks until the previous kernel has completed
+// and its memory is visible (a no-op without that launch attribute).  Kernels call both after
+// their shared-memory / TMEM set-up and before their first global access.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ persistent blocks
 // Ask the launch queue for a block of this grid that has not started yet; the 16-byte
 // response lands at `resp` and completes `bar` (armed for 16 bytes by the caller).

@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output (X, the bias, R) is complete from here on
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -282,11 +284,9 @@ cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUte
   if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM);
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-  kern<<<grid, kThreads, S::kSmemBytes, s>>>(tmX, tmW, tmY, static_cast<const __nv_bfloat16*>(bias),
-                                             static_cast<__nv_bfloat16*>(Y), M, N, K, ldy,
-                                             ctx.status, ctx.timeout_ns,
-                                             static_cast<const __nv_bfloat16*>(R));
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), S::kSmemBytes, s, tmX, tmW, tmY,
+                    static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(Y), M,
+                    N, K, ldy, ctx.status, ctx.timeout_ns, static_cast<const __nv_bfloat16*>(R));
 }
 
 }  // namespace

@@ -1,9 +1,11 @@
 // launchers.h -- host-side entry points of the kernels, used by the C ABI layer (capi.cu).
 #pragma once
 
-#include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
+#include <utility>
 
 namespace mha {
 
@@ -19,6 +21,24 @@ struct DevCtx {
 // smem_bytes and reports its register count (num_regs may be null), once per (kernel, device);
 // later calls return the cached result without driver calls.
 cudaError_t prepare_kernel(const void* func, int smem_bytes, int* num_regs);
+
+// ---- launch with programmatic stream serialization: the kernel may begin (its set-up up to
+// pdl_wait) while the previous kernel in the stream finishes
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- projections: Y[M,N] = act(X[M,K] W[N,K]^T + bias), act = identity or ReLU (relu)
 // bf16 tensor-core path.  tmX: 2-D map over X {K, M}, box {64, 128}; tmW: 2-D map over W

@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
                                      __nv_bfloat16* __restrict__ y, int M, int D, float eps) {
   const int lane = threadIdx.x & 31;
   const int W = gridDim.x * kRowsPerBlock;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output (a) is complete from here on
   int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const uint32_t row_bytes = static_cast<uint32_t>(D) * 2;
   if (lane == 0 && row < M) {
@@ -213,11 +215,11 @@ cudaError_t launch_stream(int M, int D, float eps, const void* x, const void* a,
   const int blocks = (M + kRowsPerBlock - 1) / kRowsPerBlock;
   const int grid = std::min(blocks, 4 * std::max(ctx.num_sms, 1));  // 4 blocks fit an SM
   auto go = [&](auto kern) {
-    kern<<<grid, kRowsPerBlock * 32, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
-        static_cast<const __nv_bfloat16*>(gamma), static_cast<const __nv_bfloat16*>(beta),
-        static_cast<__nv_bfloat16*>(y), M, D, eps);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kRowsPerBlock * 32), 0, s,
+                      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
+                      static_cast<const __nv_bfloat16*>(gamma),
+                      static_cast<const __nv_bfloat16*>(beta), static_cast<__nv_bfloat16*>(y),
+                      M, D, eps);
   };
   switch ((D + 255) / 256) {
     case 1: return go(residual_layernorm_stream_kernel<1>);

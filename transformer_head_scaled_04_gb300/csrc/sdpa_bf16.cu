@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output (Q, K, V) is complete from here on
   // The i-th unit of this CTA is followed by the unit named in launch-cancel response i (slot
   // i % 2), which the producer requests once it has issued the i-th unit's loads.  Every role
   // reads every response, so all roles walk the same units; -1 ends the walk.
@@ -722,8 +724,8 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   if (regs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
     return cudaErrorInvalidConfiguration;
   dim3 grid((a.Nq + 2 * kBQ - 1) / (2 * kBQ), a.H, a.B);
-  sdpa_fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmQ, tmK, tmV, tmO, p);
-  return cudaGetLastError();
+  return launch_pdl(sdpa_fwd_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, tmQ, tmK, tmV,
+                    tmO, p);
 }
 
 }  // namespace mha
