@@ -16,6 +16,7 @@
 
 #include <cstdint>
 
+#include "device_common.cuh"
 #include "launchers.h"
 
 namespace mha {
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(kRows * 32)
                          const T* __restrict__ gamma, const T* __restrict__ dy,
                          T* __restrict__ dr, float2* __restrict__ stats, int M, int D,
                          float eps) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRows + warp;
   if (row >= M) return;
@@ -103,6 +106,8 @@ __global__ void __launch_bounds__(256)
                              const T* __restrict__ dy, const T* __restrict__ dr,
                              const float2* __restrict__ stats, float* __restrict__ part, int M,
                              int D, int rows_per_chunk) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int col = blockIdx.x * 256 + threadIdx.x;
   const int chunk = blockIdx.y;
   if (col >= D) return;
@@ -128,6 +133,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     colsum_partials_kernel(const T* __restrict__ X, int64_t ld, int M, int N,
                            int rows_per_chunk, float* __restrict__ part) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int col = blockIdx.x * 256 + threadIdx.x;
   const int chunk = blockIdx.y;
   if (col >= N) return;
@@ -142,6 +149,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     reduce_partials_kernel(const float* __restrict__ part, int nchunk, int64_t chunk_stride,
                            int N, T* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int col = blockIdx.x * 256 + threadIdx.x;
   if (col >= N) return;
   float s = 0.f;
@@ -154,6 +163,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     transpose_kernel(const T* __restrict__ X, int64_t ldx, int R, int C, T* __restrict__ Y,
                      int64_t ldy, int R_pad) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ T tile[32][33];
   const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
@@ -194,6 +205,8 @@ __global__ void __launch_bounds__(kRows * 32)
                             const __nv_bfloat16* __restrict__ gamma,
                             const __nv_bfloat16* __restrict__ dy, __nv_bfloat16* __restrict__ dr,
                             float2* __restrict__ stats, int M, int D, float eps) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRows + warp;
   if (row >= M) return;
@@ -278,6 +291,8 @@ __global__ void __launch_bounds__(128 * kRowGroups)
                      const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ a,
                      const __nv_bfloat16* __restrict__ dr, const float2* __restrict__ stats,
                      int M, int N, int rows_per_chunk, float* __restrict__ part) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float red[kRowGroups - 1][kTerms][128 * 8];
   const int col = (blockIdx.x * 128 + threadIdx.x) * 8;
   const int chunk = blockIdx.y, grp = threadIdx.y;
@@ -344,6 +359,8 @@ constexpr int kTpPitch = kTp + 2;
 __global__ void __launch_bounds__(256)
     transpose_v8_kernel(const __nv_bfloat16* __restrict__ X, int64_t ldx, int R, int C,
                         __nv_bfloat16* __restrict__ Y, int64_t ldy, int R_pad) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ uint16_t tile[kTp * kTpPitch];
   const int r0 = blockIdx.x * kTp, c0 = blockIdx.y * kTp;
   const int t = threadIdx.x;
@@ -398,22 +415,22 @@ cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void*
     const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
     auto* drb = static_cast<__nv_bfloat16*>(dr);
     switch ((D + 255) / 256) {
-      case 1: layernorm_bwd_v8_kernel<1><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
-      case 2: layernorm_bwd_v8_kernel<2><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
-      case 3: layernorm_bwd_v8_kernel<3><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
-      case 4: layernorm_bwd_v8_kernel<4><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
-      case 5: case 6: layernorm_bwd_v8_kernel<6><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
-      default: layernorm_bwd_v8_kernel<8><<<grid_rows, kRows * 32, 0, s>>>(xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 1: (void)launch_pdl(layernorm_bwd_v8_kernel<1>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 2: (void)launch_pdl(layernorm_bwd_v8_kernel<2>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 3: (void)launch_pdl(layernorm_bwd_v8_kernel<3>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 4: (void)launch_pdl(layernorm_bwd_v8_kernel<4>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      case 5: case 6: (void)launch_pdl(layernorm_bwd_v8_kernel<6>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
+      default: (void)launch_pdl(layernorm_bwd_v8_kernel<8>, dim3(grid_rows), dim3(kRows * 32), 0, s, xb, ab, gb, dyb, drb, stats, M, D, eps); break;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const dim3 g8((D + 1023) / 1024, bwd_row_chunks(M));
-    colsum_v8_kernel<3><<<g8, dim3(128, kRowGroups), 0, s>>>(dyb, D, xb, ab, drb, stats, M, D,
+    (void)launch_pdl(colsum_v8_kernel<3>, dim3(g8), dim3(dim3(128, kRowGroups)), 0, s, dyb, D, xb, ab, drb, stats, M, D,
                                                              kChunkRows, part);
     return cudaGetLastError();
   }
 #define MHA_LN_BWD(T, N)                                                                    \
-  layernorm_bwd_kernel<T, N><<<grid_rows, kRows * 32, 0, s>>>(                              \
+  (void)launch_pdl(layernorm_bwd_kernel<T, N>, dim3(grid_rows), dim3(kRows * 32), 0, s, \
       static_cast<const T*>(x), static_cast<const T*>(a), static_cast<const T*>(gamma),     \
       static_cast<const T*>(dy), static_cast<T*>(dr), stats, M, D, eps)
   if (dtype == 1) {
@@ -429,13 +446,11 @@ cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void*
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (dtype == 1)
-    ln_param_partials_kernel<__nv_bfloat16><<<grid_cols, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
+    (void)launch_pdl(ln_param_partials_kernel<__nv_bfloat16>, dim3(grid_cols), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
         static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(dr), stats,
         part, M, D, kChunkRows);
   else
-    ln_param_partials_kernel<float><<<grid_cols, 256, 0, s>>>(
-        static_cast<const float*>(x), static_cast<const float*>(a),
+    (void)launch_pdl(ln_param_partials_kernel<float>, dim3(grid_cols), dim3(256), 0, s, static_cast<const float*>(x), static_cast<const float*>(a),
         static_cast<const float*>(dy), static_cast<const float*>(dr), stats, part, M, D,
         kChunkRows);
   return cudaGetLastError();
@@ -445,17 +460,15 @@ cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, 
                                    float* part, cudaStream_t s) {
   if (dtype == 1 && N % 8 == 0 && ld % 8 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0) {
     const dim3 g8((N + 1023) / 1024, bwd_row_chunks(M));
-    colsum_v8_kernel<1><<<g8, dim3(128, kRowGroups), 0, s>>>(
-        static_cast<const __nv_bfloat16*>(X), ld, nullptr, nullptr, nullptr, nullptr, M, N,
+    (void)launch_pdl(colsum_v8_kernel<1>, dim3(g8), dim3(dim3(128, kRowGroups)), 0, s, static_cast<const __nv_bfloat16*>(X), ld, nullptr, nullptr, nullptr, nullptr, M, N,
         kChunkRows, part);
     return cudaGetLastError();
   }
   const dim3 grid((N + 255) / 256, bwd_row_chunks(M));
   if (dtype == 1)
-    colsum_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(X), ld, M, N, kChunkRows, part);
+    (void)launch_pdl(colsum_partials_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(X), ld, M, N, kChunkRows, part);
   else
-    colsum_partials_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), ld, M, N,
+    (void)launch_pdl(colsum_partials_kernel<float>, dim3(grid), dim3(256), 0, s, static_cast<const float*>(X), ld, M, N,
                                                        kChunkRows, part);
   return cudaGetLastError();
 }
@@ -464,10 +477,9 @@ cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
                                    int64_t chunk_stride, int N, void* out, cudaStream_t s) {
   const dim3 grid((N + 255) / 256);
   if (dtype == 1)
-    reduce_partials_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        part, nchunk, chunk_stride, N, static_cast<__nv_bfloat16*>(out));
+    (void)launch_pdl(reduce_partials_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, part, nchunk, chunk_stride, N, static_cast<__nv_bfloat16*>(out));
   else
-    reduce_partials_kernel<float><<<grid, 256, 0, s>>>(part, nchunk, chunk_stride, N,
+    (void)launch_pdl(reduce_partials_kernel<float>, dim3(grid), dim3(256), 0, s, part, nchunk, chunk_stride, N,
                                                        static_cast<float*>(out));
   return cudaGetLastError();
 }
@@ -478,17 +490,16 @@ cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C
                   reinterpret_cast<uintptr_t>(X) % 16 == 0 && reinterpret_cast<uintptr_t>(Y) % 16 == 0;
   if (v8) {
     const dim3 g64((R_pad + kTp - 1) / kTp, (C + kTp - 1) / kTp);
-    transpose_v8_kernel<<<g64, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(X), ldx, R, C,
+    (void)launch_pdl(transpose_v8_kernel, dim3(g64), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(X), ldx, R, C,
                                              static_cast<__nv_bfloat16*>(Y), ldy, R_pad);
     return cudaGetLastError();
   }
   const dim3 grid((R_pad + 31) / 32, (C + 31) / 32);
   if (dtype == 1)
-    transpose_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(X), ldx, R, C, static_cast<__nv_bfloat16*>(Y), ldy,
+    (void)launch_pdl(transpose_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, static_cast<const __nv_bfloat16*>(X), ldx, R, C, static_cast<__nv_bfloat16*>(Y), ldy,
         R_pad);
   else
-    transpose_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), ldx, R, C,
+    (void)launch_pdl(transpose_kernel<float>, dim3(grid), dim3(256), 0, s, static_cast<const float*>(X), ldx, R, C,
                                                  static_cast<float*>(Y), ldy, R_pad);
   return cudaGetLastError();
 }

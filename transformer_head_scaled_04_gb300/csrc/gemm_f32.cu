@@ -4,6 +4,7 @@
 // translation, 3.2.2 多头注意力; "Attention Is All You Need" on likecs.com, 1.3 按地址的前向
 // 反馈网络).  64x64 output tile per 256-thread block, 4x4 per thread, K staged through
 // shared memory 16 at a time.
+#include "device_common.cuh"
 #include "launchers.h"
 
 namespace mha {
@@ -16,6 +17,8 @@ __global__ void __launch_bounds__(256)
     gemm_f32_kernel(const float* __restrict__ X, int64_t ldx, const float* __restrict__ W,
                     const float* __restrict__ bias, bool relu, float* __restrict__ Y,
                     int64_t ldy, int M, int N, int K, const float* __restrict__ R) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float sx[kKT][kT + 4];
   __shared__ float sw[kKT][kT + 4];
   const int tx = threadIdx.x & 15;  // column group
@@ -68,7 +71,7 @@ cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const f
                             bool relu, float* Y, int64_t ldy, int M, int N, int K,
                             cudaStream_t s, const float* R) {
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
-  gemm_f32_kernel<<<grid, 256, 0, s>>>(X, ldx, W, bias, relu, Y, ldy, M, N, K, R);
+  (void)launch_pdl(gemm_f32_kernel, dim3(grid), dim3(256), 0, s, X, ldx, W, bias, relu, Y, ldy, M, N, K, R);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
     residual_layernorm_kernel(const T* __restrict__ x, const T* __restrict__ a,
                               const T* __restrict__ gamma, const T* __restrict__ beta,
                               T* __restrict__ y, int M, int D, float eps) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * kRowsPerBlock + warp;
@@ -240,7 +242,7 @@ cudaError_t launch_t(int M, int D, float eps, const void* x, const void* a, cons
   dim3 grid((M + kRowsPerBlock - 1) / kRowsPerBlock);
   dim3 block(kRowsPerBlock * 32);
   auto args = [&](auto kern) {
-    kern<<<grid, block, 0, s>>>(static_cast<const T*>(x), static_cast<const T*>(a),
+    (void)launch_pdl(kern, dim3(grid), dim3(block), 0, s, static_cast<const T*>(x), static_cast<const T*>(a),
                                 static_cast<const T*>(gamma), static_cast<const T*>(beta),
                                 static_cast<T*>(y), M, D, eps);
   };

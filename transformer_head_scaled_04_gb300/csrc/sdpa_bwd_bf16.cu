@@ -195,6 +195,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQOffBar);
@@ -429,6 +431,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKOffBar);
@@ -703,8 +707,7 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.o0_b = a.st[5][0];
   p.o0_h = a.st[5][1];
   p.o0_n = a.st[5][2];
-  sdpa_bwd_dq_kernel<<<dim3((a.Nq + kT - 1) / kT, a.H, a.B), kQThreads, kQSmem, s>>>(
-      tmQ, tmK, tmV, tmG, p);
+  (void)launch_pdl(sdpa_bwd_dq_kernel, dim3(dim3((a.Nq + kT - 1) / kT, a.H, a.B)), dim3(kQThreads), kQSmem, s, tmQ, tmK, tmV, tmG, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   p.out0 = static_cast<__nv_bfloat16*>(a.dK);
@@ -715,8 +718,7 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.o1_b = a.st[7][0];
   p.o1_h = a.st[7][1];
   p.o1_n = a.st[7][2];
-  sdpa_bwd_dkdv_kernel<<<dim3((a.Nk + kT - 1) / kT, a.H, a.B), kKThreads, kKSmem, s>>>(
-      tmQ, tmK, tmV, tmG, p);
+  (void)launch_pdl(sdpa_bwd_dkdv_kernel, dim3(dim3((a.Nk + kT - 1) / kT, a.H, a.B)), dim3(kKThreads), kKSmem, s, tmQ, tmK, tmV, tmG, p);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@
 
 #include <cmath>
 
+#include "device_common.cuh"
 #include "launchers.h"
 
 namespace mha {
@@ -52,6 +53,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
                            int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
                            const float* __restrict__ lse, int rows) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   // lse != null: the per-tile layout {-lse * log2 e [128], -D [128]} (negated, so the
   // tensor-core kernels add them in paired fp32 instructions) over rows up to a whole number
   // of 128-row tiles; otherwise D alone as [B, H, Nq]
@@ -88,6 +91,8 @@ struct BwdF32 {
 };
 
 __global__ void __launch_bounds__(kWarps * 32) sdpa_bwd_dq_f32_kernel(const BwdF32 p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float sq[kWarps][kMaxD];
   __shared__ float sg[kWarps][kMaxD];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,6 +138,8 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_bwd_dq_f32_kernel(const BwdF
 // kWantK: dK (from dS and Q) or dV (from P and dO); two passes keep one accumulator row
 template <bool kWantK>
 __global__ void __launch_bounds__(kWarps * 32) sdpa_bwd_dkdv_f32_kernel(const BwdF32 p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float sk[kWarps][kMaxD];
   __shared__ float sv[kWarps][kMaxD];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,13 +197,11 @@ cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t
   const int rows = dtype == 1 ? (a.Nq + 127) / 128 * 128 : a.Nq;
   dim3 grid((rows + kWarps - 1) / kWarps, a.H, a.B);
   if (dtype == 1)
-    sdpa_bwd_rowdot_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.Dv,
+    (void)launch_pdl(sdpa_bwd_rowdot_kernel<__nv_bfloat16>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.Dv,
         a.H, a.Nq, a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1],
         a.st[4][2], a.lse, rows);
   else
-    sdpa_bwd_rowdot_kernel<float><<<grid, kWarps * 32, 0, s>>>(
-        static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
+    (void)launch_pdl(sdpa_bwd_rowdot_kernel<float>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
         a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], nullptr,
         rows);
   return cudaGetLastError();
@@ -224,14 +229,14 @@ cudaError_t launch_sdpa_bwd_f32(const SdpaBwdArgs& a, cudaStream_t s) {
   p.window = a.window;
   p.key_len = a.key_len;
   p.scale = a.scale;
-  sdpa_bwd_dq_f32_kernel<<<dim3((a.Nq + kWarps - 1) / kWarps, a.H, a.B), kWarps * 32, 0, s>>>(p);
+  (void)launch_pdl(sdpa_bwd_dq_f32_kernel, dim3(dim3((a.Nq + kWarps - 1) / kWarps, a.H, a.B)), dim3(kWarps * 32), 0, s, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid_k((a.Nk + kWarps - 1) / kWarps, a.H, a.B);
-  sdpa_bwd_dkdv_f32_kernel<false><<<grid_k, kWarps * 32, 0, s>>>(p);
+  (void)launch_pdl(sdpa_bwd_dkdv_f32_kernel<false>, dim3(grid_k), dim3(kWarps * 32), 0, s, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  sdpa_bwd_dkdv_f32_kernel<true><<<grid_k, kWarps * 32, 0, s>>>(p);
+  (void)launch_pdl(sdpa_bwd_dkdv_f32_kernel<true>, dim3(grid_k), dim3(kWarps * 32), 0, s, p);
   return cudaGetLastError();
 }
 

@@ -70,6 +70,8 @@ template <int NQ>
 __global__ void __launch_bounds__(kThreads)
     decode_partial_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   using Sm = DecodeSmem<NQ>;
   constexpr int kOffK = Sm::kOffK, kOffV = Sm::kOffV, kOffQ = Sm::kOffQ, kOffS = Sm::kOffS,
                 kOffO = Sm::kOffO, kOffStat = Sm::kOffStat, kOffBar = Sm::kOffBar;
@@ -238,6 +240,8 @@ __global__ void __launch_bounds__(kDecodeMaxQ * kD)
     decode_combine_kernel(const float* __restrict__ part, int H, int Nq, int n_split,
                           float scale, __nv_bfloat16* __restrict__ O, int64_t so_b,
                           int64_t so_h, int64_t so_n) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   const int h = blockIdx.x, b = blockIdx.y;
   const int q = threadIdx.x / kD, d = threadIdx.x % kD;
   if (q >= Nq) return;
@@ -268,7 +272,7 @@ cudaError_t launch_partial(const CUtensorMap& tmK, const CUtensorMap& tmV, const
   cudaError_t e =
       prepare_kernel(reinterpret_cast<const void*>(kern), DecodeSmem<NQ>::kBytes, nullptr);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, DecodeSmem<NQ>::kBytes, s>>>(tmK, tmV, p);
+  (void)launch_pdl(kern, dim3(grid), dim3(kThreads), DecodeSmem<NQ>::kBytes, s, tmK, tmV, p);
   return cudaGetLastError();
 }
 
@@ -307,8 +311,7 @@ cudaError_t launch_sdpa_decode_bf16(const CUtensorMap& tmK, const CUtensorMap& t
   else
     e = launch_partial<16>(tmK, tmV, p, grid, s);
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<dim3(a.H, a.B), kDecodeMaxQ * kD, 0, s>>>(
-      part, a.H, a.Nq, p.n_split, a.scale, static_cast<__nv_bfloat16*>(a.O), a.so[0], a.so[1],
+  (void)launch_pdl(decode_combine_kernel, dim3(dim3(a.H, a.B)), dim3(kDecodeMaxQ * kD), 0, s, part, a.H, a.Nq, p.n_split, a.scale, static_cast<__nv_bfloat16*>(a.O), a.so[0], a.so[1],
       a.so[2]);
   return cudaGetLastError();
 }

@@ -15,6 +15,7 @@
 // expf is the accurate CUDA function (no fast-math).
 #include <cmath>
 
+#include "device_common.cuh"
 #include "launchers.h"
 
 namespace mha {
@@ -33,6 +34,8 @@ __global__ void __launch_bounds__(kWarps * 32)
                     int64_t qb, int64_t qh, int64_t qn, int64_t qd, int64_t kb, int64_t kh,
                     int64_t kn, int64_t kd, int64_t vb, int64_t vh, int64_t vn, int64_t vd,
                     int64_t ob, int64_t oh, int64_t on, int64_t od) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float sq[kWarps][kMaxD];
   __shared__ float sk[kChunk * kPitch];
   __shared__ float sv[kChunk * kPitch];
@@ -139,8 +142,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s) {
   dim3 grid((a.Nq + kWarps - 1) / kWarps, a.H, a.B);
-  sdpa_f32_kernel<<<grid, kWarps * 32, 0, s>>>(
-      static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
+  (void)launch_pdl(sdpa_f32_kernel, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
       static_cast<const float*>(a.V), static_cast<float*>(a.O), a.Nq, a.Nk, a.d_k, a.d_v,
       a.mask, a.window, a.key_len, a.scale, a.lse, a.sq[0], a.sq[1], a.sq[2], a.sq[3], a.sk[0], a.sk[1], a.sk[2],
       a.sk[3], a.sv[0], a.sv[1], a.sv[2], a.sv[3], a.so[0], a.so[1], a.so[2], a.so[3]);
