@@ -261,6 +261,7 @@ def test_sdpa_bf16_deterministic():
     (1000, 1536, 512, True),     # 128-wide tiles
     (9800, 512, 512, True),      # enough tiles for the 256-wide variant
     (4096, 1024, 1024, False),
+    (8192, 3072, 256, True),
 ])
 def test_linear_bf16(M, N, K, bias):
     g = np.random.Generator(np.random.PCG64(M + N + K))
