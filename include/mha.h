@@ -99,8 +99,8 @@ int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, 
 /*
  * mha_sdpa_bwd_workspace_size -- bytes of device workspace mha_sdpa_bwd needs: with
  * D_i = sum_d dO_id O_id, MHA_BF16 keeps 1 KB per (b, h, 128-row query tile) -- the tile's
- * D and lse (lse in base-2 units), both negated, read by one bulk copy -- and MHA_F32 one
- * fp32 D per query row.
+ * D and lse (lse in base-2 units), both negated, read by one bulk copy -- followed by an fp32
+ * dQ accumulator of 128 x 64 values (32 KB) per tile; MHA_F32 one fp32 D per query row.
  */
 int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes);
 
@@ -117,8 +117,14 @@ int mha_sdpa_bwd_workspace_size(int B, int H, int Nq, int dtype, size_t* bytes);
  *   strides: NULL for contiguous, or 32 element strides {Q, K, V, O, dO, dQ, dK, dV} x
  *   {b, h, n, d} (d stride 1).  workspace: mha_sdpa_bwd_workspace_size() bytes, 256-byte
  *   aligned.  dtype MHA_BF16: d_k == d_v == 64, other strides multiples of 8, 16-byte aligned
- *   pointers; tensor-core kernels (one CTA per 128 query rows for dQ, one per 128 keys for
- *   dK and dV; no atomics).  dtype MHA_F32: d <= 128, SIMT kernels.
+ *   pointers; tensor-core kernels.  By default one CTA per 128 keys computes dK, dV and that
+ *   key tile's part of dQ (dS K for every query tile it sees), which it adds in fp32 into the
+ *   workspace's accumulator with bulk tensor reductions; a last launch scales it into dQ.
+ *   The additions run in whatever order the key tiles finish, so dQ can differ between
+ *   calls by fp32 rounding (then rounded to bf16).  After mha_set_deterministic(1), dQ comes
+ *   from its own kernel (one CTA per 128 query rows, S and dP rebuilt, no atomics) and all
+ *   three gradients are bitwise reproducible.  dtype MHA_F32: d <= 128, SIMT kernels,
+ *   always reproducible.
  */
 int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
                  const int32_t* key_len, float scale, const void* Q, const void* K,
@@ -250,8 +256,9 @@ int mha_layer_bwd_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, i
  *   dx_q [B,Nq,D]; dx_kv [B,Nk,D] for cross-attention (ignored, may be NULL, for self);
  *   dW_qkv like W_qkv; db_qkv [H*(2*d_k+d_v)]; dW_o like W_o; db_o, dgamma, dbeta [D]
  *   (always written, also when the forward passed NULL for the bias, gamma or beta).
- *   Sums over rows run per chunk of 256 rows and then over the chunks in a fixed order:
- *   results are deterministic.  workspace: mha_layer_bwd_workspace_size() bytes, 256-byte
+ *   Sums over rows run per chunk of 256 rows and then over the chunks in a fixed order;
+ *   the attention backward inside follows mha_set_deterministic (see mha_sdpa_bwd): with 1
+ *   every result is bitwise reproducible.  workspace: mha_layer_bwd_workspace_size() bytes, 256-byte
  *   aligned.  Limits and errors as for mha_layer_fwd; MHA_ERR_INVALID for a NULL output.
  * Launches (all on `stream`): the forward's GEMMs, attention and W^O GEMM again, the
  * LayerNorm backward, the attention backward, the data- and weight-gradient GEMMs on the
@@ -387,6 +394,17 @@ int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mha_status_string(int status);
+
+/*
+ * mha_set_deterministic -- process-wide switch (0 by default) for the bf16 attention
+ * backward, also inside mha_layer_bwd: 1 computes dQ by a separate kernel that rebuilds S and
+ * dP per query tile, bitwise reproducible; 0 adds every key tile's dQ part into an fp32
+ * accumulator by bulk reductions, faster, reproducible up to the order of fp32 additions.
+ * Returns MHA_ERR_INVALID unless `on` is 0 or 1.  Takes effect for calls issued after it.
+ * mha_get_deterministic -- the current setting.
+ */
+int mha_set_deterministic(int on);
+int mha_get_deterministic(void);
 
 /*
  * mha_debug_last_device_status -- synchronises `stream`, returns the first device-side error

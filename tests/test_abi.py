@@ -282,7 +282,8 @@ def test_decode_workspace_and_validation(lib):
 def test_sdpa_backward_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.mha_sdpa_bwd_workspace_size(8, 16, 4096, 1, ctypes.byref(n)) == 0
-    assert n.value == 8 * 16 * 32 * 1024           # per 128-row tile: lse and D, 1 KB
+    # per 128-row tile: lse and D (1 KB), then the fp32 dQ accumulator's 128 x 64 values
+    assert n.value == 8 * 16 * 32 * (1024 + 128 * 64 * 4)
     assert lib.mha_sdpa_bwd_workspace_size(8, 16, 4096, 0, ctypes.byref(n)) == 0
     assert n.value == 8 * 16 * 4096 * 4            # fp32 path: D per row
     assert lib.mha_sdpa_bwd_workspace_size(0, 16, 4096, 1, ctypes.byref(n)) == C.MHA_ERR_INVALID
@@ -311,6 +312,18 @@ def test_sdpa_backward_validation(lib):
         C.MHA_ERR_INVALID
     assert f(1, 1, 8, 8, 64, 64, 1, 0, None, 0.0, FAKE, FAKE, FAKE, FAKE, None,
              ctypes.c_void_p(0x10002), None) == C.MHA_ERR_ALIGN
+
+
+def test_deterministic_switch(lib):
+    before = lib.mha_get_deterministic()
+    try:
+        assert lib.mha_set_deterministic(1) == C.MHA_OK and lib.mha_get_deterministic() == 1
+        assert lib.mha_set_deterministic(0) == C.MHA_OK and lib.mha_get_deterministic() == 0
+        assert lib.mha_set_deterministic(2) == C.MHA_ERR_INVALID
+        assert lib.mha_set_deterministic(-1) == C.MHA_ERR_INVALID
+        assert lib.mha_get_deterministic() == 0
+    finally:
+        lib.mha_set_deterministic(before)
 
 
 def test_layer_backward_validation(lib):

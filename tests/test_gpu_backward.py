@@ -29,6 +29,15 @@ def _built():
     assert mha.device_status() == 0, "a kernel recorded a device-side error"
 
 
+@pytest.fixture(params=[False, True], ids=["fused_dq", "deterministic"])
+def det_mode(request):
+    """Both bf16 dQ paths: the fused accumulation (default) and the separate dQ kernel."""
+    before = mha.get_deterministic()
+    mha.set_deterministic(request.param)
+    yield request.param
+    mha.set_deterministic(before)
+
+
 def dev(a, dtype):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dtype)
 
@@ -68,7 +77,7 @@ CASES = [  # B, H, Nq, Nk, mask, key_len
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,mask,kl", CASES)
-def test_sdpa_backward_bf16(B, H, Nq, Nk, mask, kl):
+def test_sdpa_backward_bf16(B, H, Nq, Nk, mask, kl, det_mode):
     Q, K, V, dO = draw(B, H, Nq, Nk, "bf16", seed=500 + Nq + Nk)
     O, lse, dq, dk, dv = run(Q, K, V, dO, mask, kl, "bf16")
     key_len = None if kl is None else np.asarray(kl, np.int32)
@@ -134,3 +143,31 @@ def test_sdpa_backward_bf16_big_heads():
         assert_bf16_grad_close(dq[sl], rq, f"big dQ b={b} h={h}")
         assert_bf16_grad_close(dk[sl], rk, f"big dK b={b} h={h}")
         assert_bf16_grad_close(dv[sl], rv, f"big dV b={b} h={h}")
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_sdpa_backward_bf16_modes(mask):
+    """The deterministic path repeats bitwise; the fused one repeats dK and dV bitwise (each
+    key tile's own accumulators) and dQ up to the order of its fp32 additions; the two paths'
+    gradients agree to bf16 rounding."""
+    Q, K, V, dO = draw(2, 4, 1000, 1000, "bf16", seed=571)
+    before = mha.get_deterministic()
+    try:
+        mha.set_deterministic(True)
+        assert mha.get_deterministic()
+        a = run(Q, K, V, dO, mask, None, "bf16")
+        b = run(Q, K, V, dO, mask, None, "bf16")
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+        mha.set_deterministic(False)
+        assert not mha.get_deterministic()
+        c = run(Q, K, V, dO, mask, None, "bf16")
+        e = run(Q, K, V, dO, mask, None, "bf16")
+    finally:
+        mha.set_deterministic(before)
+    for i in (3, 4):  # dK, dV
+        assert np.array_equal(c[i], e[i])
+    for i in (2, 3, 4):
+        scale = np.abs(a[i]).max()
+        assert np.abs(c[i] - a[i]).max() <= 2 ** -7 * scale
+    assert np.abs(c[2] - e[2]).max() <= 2 ** -7 * np.abs(a[2]).max()

@@ -129,8 +129,13 @@ def test_layer_backward_is_deterministic():
     w = si.WORKLOADS["dec_causal_base_b32_n256"]
     inp = si.draw_layer(w, affine=True)
     dy = draw_dy(w, 83, "bf16")
-    a = run_gpu(inp, dy, w, torch.bfloat16)
-    b = run_gpu(inp, dy, w, torch.bfloat16)
+    before = mha.get_deterministic()
+    mha.set_deterministic(True)
+    try:
+        a = run_gpu(inp, dy, w, torch.bfloat16)
+        b = run_gpu(inp, dy, w, torch.bfloat16)
+    finally:
+        mha.set_deterministic(before)
     for k in PER_TOKEN + PARAMS:
         if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k

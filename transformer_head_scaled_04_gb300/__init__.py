@@ -18,6 +18,7 @@ from .api import (  # noqa: F401
     encoder_layer_workspace_size,
     ffn,
     ffn_workspace_size,
+    get_deterministic,
     layer_bwd_workspace_size,
     layer_workspace_size,
     linear,
@@ -28,5 +29,6 @@ from .api import (  # noqa: F401
     sdpa_backward,
     sdpa_decode,
     sdpa_with_lse,
+    set_deterministic,
     wait_selftest,
 )

@@ -48,6 +48,8 @@ PROTOTYPES = {
                               + [_size, _vp]),
     "mha_residual_layernorm_fwd": (_c_int, [_c_int] * 3 + [_c_float] + [_vp] * 6),
     "mha_status_string": (ctypes.c_char_p, [_c_int]),
+    "mha_set_deterministic": (_c_int, [_c_int]),
+    "mha_get_deterministic": (_c_int, []),
     "mha_debug_last_device_status": (_c_int, [_vp]),
     "mha_debug_wait_selftest": (_c_int, [_i64, _vp]),
     "mha_abi_version": (_c_int, []),

@@ -347,6 +347,18 @@ def residual_layernorm(x, a, gamma=None, beta=None, eps=1e-5, out=None):
     return out
 
 
+def set_deterministic(on: bool) -> None:
+    """Process-wide switch of the bf16 attention backward (``mha_set_deterministic``): True
+    computes dQ by its own kernel, bitwise reproducible; False (the default) adds each key
+    tile's part of dQ into an fp32 accumulator, faster, reproducible up to fp32 rounding."""
+    C.check(C.load().mha_set_deterministic(1 if on else 0), "mha_set_deterministic")
+
+
+def get_deterministic() -> bool:
+    """The current ``mha_set_deterministic`` setting."""
+    return bool(C.load().mha_get_deterministic())
+
+
 def device_status(stream=None) -> int:
     """First device-side error since the last call on the current device (0 = none); syncs."""
     s = _stream(torch.cuda.current_device()) if stream is None else stream

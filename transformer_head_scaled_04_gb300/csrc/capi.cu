@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -163,7 +164,27 @@ bool map_bhnd_bf16(CUtensorMap* m, const void* base, int B, int H, int N, const 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// the fp32 dQ accumulator of the fused bf16 attention backward, [B, H, rows, 64] contiguous:
+// one 32 x 32 box (128-byte rows, 128-byte swizzle) per bulk reduction
+bool map_dq_acc_f32(CUtensorMap* m, const void* base, int B, int H, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {64 * 4, static_cast<cuuint64_t>(rows) * 64 * 4,
+                           static_cast<cuuint64_t>(H) * rows * 64 * 4};
+  cuuint32_t box[4] = {32, 32, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// mha_set_deterministic: the bf16 attention backward's dQ by its own kernel (bitwise
+// reproducible) instead of fp32 bulk reductions in whatever order the key tiles finish
+std::atomic<int> g_deterministic{0};
 
 // ------------------------------------------------------------------ step launchers
 int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
@@ -203,17 +224,21 @@ int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t 
 }
 
 // rowdot (D) and the gradient kernels of one attention backward; a.Dv is the caller's scratch
-int run_sdpa_bwd(const mha::SdpaBwdArgs& a, int dtype, const DevCtx& ctx, cudaStream_t s) {
+int run_sdpa_bwd(mha::SdpaBwdArgs a, int dtype, const DevCtx& ctx, cudaStream_t s) {
+  a.deterministic = g_deterministic.load(std::memory_order_relaxed) != 0;
   cudaError_t e = mha::launch_sdpa_bwd_rowdot(a, dtype, s);
   if (e != cudaSuccess) return MHA_ERR_CUDA;
   if (dtype == MHA_BF16) {
-    CUtensorMap tq, tk, tv, tg;
+    CUtensorMap tq, tk, tv, tg, tdq;
+    const void* acc = reinterpret_cast<const char*>(a.Dv) +
+                      mha::sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq);
     if (!map_bhnd_bf16(&tq, a.Q, a.B, a.H, a.Nq, a.st[0]) ||
         !map_bhnd_bf16(&tk, a.K, a.B, a.H, a.Nk, a.st[1]) ||
         !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.st[2]) ||
-        !map_bhnd_bf16(&tg, a.dO, a.B, a.H, a.Nq, a.st[4]))
+        !map_bhnd_bf16(&tg, a.dO, a.B, a.H, a.Nq, a.st[4]) ||
+        !map_dq_acc_f32(&tdq, acc, a.B, a.H, (a.Nq + 127) / 128 * 128))
       return MHA_ERR_CUDA;
-    e = mha::launch_sdpa_bwd_bf16(tq, tk, tv, tg, a, ctx, s);
+    e = mha::launch_sdpa_bwd_bf16(tq, tk, tv, tg, tdq, a, ctx, s);
   } else {
     e = mha::launch_sdpa_bwd_f32(a, s);
   }
@@ -895,6 +920,14 @@ int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x
   cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, eps, x, a, gamma, beta, y, ctx, stream);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
+
+int mha_set_deterministic(int on) {
+  if (on != 0 && on != 1) return MHA_ERR_INVALID;
+  g_deterministic.store(on, std::memory_order_relaxed);
+  return MHA_OK;
+}
+
+int mha_get_deterministic(void) { return g_deterministic.load(std::memory_order_relaxed); }
 
 int mha_debug_last_device_status(cudaStream_t stream) {
   DevCtx ctx;

@@ -152,6 +152,22 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
                ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1)
                : "memory");
 }
+// Tiled bulk reduction: adds a box from shared memory element-wise into global memory (the
+// element type is the tensor map's; the addition is done at L2, atomically per element, in no
+// fixed order across CTAs).  Same coordinate rules as tma_store_4d.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, uint32_t src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Wait until every committed bulk operation of this thread has completed (its global writes
+// performed), not only read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 // Wait until at most N of this thread's most recent committed bulk stores still have to read
 // shared memory.
 template <int N>

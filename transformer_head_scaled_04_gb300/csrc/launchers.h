@@ -113,21 +113,32 @@ struct SdpaBwdArgs {
   // rowsum(dO * O) as [B, H, Nq]; bf16 path, per 128-row query tile of every (b, h) the
   // tile's lse * log2(e) [128] then its D [128] (rows past Nq: +inf and 0), so one 1 KB bulk
   // copy brings a tile's statistics into shared memory
+  // bf16 path, after those statistics (at sdpa_bwd_dq_acc_offset bytes into the scratch):
+  // an fp32 dQ accumulator [B, H, 128 * tiles, 64] that the rowdot launch zeroes and the
+  // fused kernel adds every key tile's dS K into; unused when deterministic
   float* Dv;
+  bool deterministic;        // bf16: dQ by its own kernel instead of the fused accumulation
   void *dQ, *dK, *dV;
   int64_t st[8][4];          // element strides b, h, n, d of Q, K, V, O, dO, dQ, dK, dV
 };
 cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s);
+inline size_t sdpa_bwd_dq_acc_offset(int B, int H, int Nq) {
+  return static_cast<size_t>(B) * H * ((Nq + 127) / 128) * 1024;
+}
 // bytes of the Dv scratch above
 inline size_t sdpa_bwd_scratch_bytes(int B, int H, int Nq, int dtype) {
-  return dtype == 1 ? static_cast<size_t>(B) * H * ((Nq + 127) / 128) * 1024
+  return dtype == 1 ? sdpa_bwd_dq_acc_offset(B, H, Nq) +
+                          static_cast<size_t>(B) * H * ((Nq + 127) / 128) * 128 * 64 * 4
                     : static_cast<size_t>(B) * H * Nq * 4;
 }
 cudaError_t launch_sdpa_bwd_f32(const SdpaBwdArgs& a, cudaStream_t s);
-// bf16 (d = 64): Q, K, V, dO through 4-D TMA maps {64, n, h, b}, box {64, 128, 1, 1}
+// bf16 (d = 64): Q, K, V, dO through 4-D TMA maps {64, n, h, b}, box {64, 128, 1, 1};
+// tmDQ: the fp32 dQ accumulator {64, 128 * tiles, h, b}, box {32, 32, 1, 1}, 128-byte
+// swizzle (read only when !a.deterministic)
 cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmG,
-                                 const SdpaBwdArgs& a, const DevCtx& ctx, cudaStream_t s);
+                                 const CUtensorMap& tmDQ, const SdpaBwdArgs& a,
+                                 const DevCtx& ctx, cudaStream_t s);
 
 // ---- memory-bound steps of the sublayer backward (bwd_util.cu)
 int bwd_row_chunks(int M);  // chunks of rows the partial column sums use

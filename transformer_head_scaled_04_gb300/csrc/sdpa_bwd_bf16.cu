@@ -28,6 +28,7 @@
 // skipped, and the d = 64 heads of the forward kernel are assumed.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "device_common.cuh"
@@ -404,17 +405,30 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // ============================================================================ dkdv kernel
-// smem: K, V (once), Q ring, dO ring, -lse2/-D ring (2 x 128 floats per stage), barriers
+// One CTA per 128-key tile.  kFused (the default path) also produces this key tile's share of
+// dQ: dQ_i += dS_i K for every query tile i it walks, added in fp32 into a workspace
+// accumulator by bulk tensor reductions, so no second kernel rebuilds S and dP for dQ.
+// smem: K, V (once), Q ring, dO ring, -lse2/-D ring (2 x 128 floats per stage), then, fused,
+// dS^T (two 64-query halves, each laid out like a 128-row swizzled tile) and one 32 x 32 fp32
+// staging box per math warp, then barriers
 constexpr int kKOffK = 0;
 constexpr int kKOffV = kKOffK + kTileBytes;
 constexpr int kKOffQ = kKOffV + kTileBytes;
 constexpr int kKOffG = kKOffQ + kStages * kTileBytes;
 constexpr int kKOffStat = kKOffG + kStages * kTileBytes;  // float [kStages][2][128]
-constexpr int kKOffBar = kKOffStat + kStages * 2 * kT * 4;
-constexpr int kKSmem = 1024 + kKOffBar + 256;
-// TMEM: S^T [0,128) dP^T [128,256) P^T [256,320) dS^T [320,384) dV [384,448) dK [448,512)
-constexpr uint32_t kKColS = 0, kKColP = 128, kKColPT = 256, kKColDS = 320, kKColDV = 384,
-                   kKColDK = 448;
+constexpr int kKOffDS = kKOffStat + kStages * 2 * kT * 4;  // fused only
+constexpr int kKOffStage = kKOffDS + 2 * kTileBytes;       // fused only: [kMathWarps][4 KB]
+constexpr int kStageBytes = 32 * 32 * 4;
+__host__ __device__ constexpr int k_off_bar(bool fused) {
+  return fused ? kKOffStage + kMathWarps * kStageBytes : kKOffDS;
+}
+__host__ __device__ constexpr int k_smem(bool fused) { return 1024 + k_off_bar(fused) + 256; }
+static_assert(kKOffDS % 1024 == 0 && kKOffStage % 1024 == 0, "swizzled buffers need 1 KB alignment");
+static_assert(k_smem(true) <= 227 * 1024, "fused dkdv shared memory");
+// TMEM: S^T [0,128) dP^T [128,256) P^T [256,320) dS^T (fused: dQ of one query tile) [320,384)
+// dV [384,448) dK [448,512)
+constexpr uint32_t kKColS = 0, kKColP = 128, kKColPT = 256, kKColDS = 320, kKColDQ = 320,
+                   kKColDV = 384, kKColDK = 448;
 constexpr int kKBarIn = 0;                        // K, V landed
 constexpr int kKBarQ = 1;                         // [kStages] Q_i, dO_i, lse, D landed
 constexpr int kKBarQEmpty = kKBarQ + kStages;     // [kStages] all three issuers done with Q_i, dO_i
@@ -422,20 +436,32 @@ constexpr int kKBarSFull = kKBarQEmpty + kStages;
 constexpr int kKBarSFree = kKBarSFull + 1;        // every math warp holds its S^T, dP^T half
 constexpr int kKBarPFull = kKBarSFree + 1;        // every math warp wrote its P^T, dS^T half
 constexpr int kKBarDVDone = kKBarPFull + 1;       // dV += P^T dO done with P^T
-constexpr int kKBarDKDone = kKBarDVDone + 1;      // dK += dS^T Q done with dS^T
+constexpr int kKBarDKDone = kKBarDVDone + 1;      // dK += dS^T Q (fused: and dQ = dS K) done
 constexpr int kKBarDrain = kKBarDKDone + 1;
 constexpr int kKNumBars = kKBarDrain + 1;
 
+// 32 consecutive 32-bit words of a thread's row into a 128-byte row of a 128-byte-swizzled
+// buffer: 16-byte unit u lands at u ^ (row % 8), the layout tensor-core operands and bulk
+// tensor copies use (row % 8 == lane % 8 for every caller here)
+__device__ __forceinline__ void st_row_sw128(uint32_t row_addr, int lane, const uint32_t* v) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    st_shared_v4(row_addr + ((u ^ (lane & 7)) << 4),
+                 make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]));
+}
+
+template <bool kFused>
 __global__ void __launch_bounds__(kKThreads, 1)
     sdpa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmG, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmG,
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kKOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + k_off_bar(kFused));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKNumBars);
   float* sstat = reinterpret_cast<float*>(smem + kKOffStat);
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -543,15 +569,22 @@ __global__ void __launch_bounds__(kKThreads, 1)
       (void)mbar_wait(bar(kKBarDrain), 0, p.timeout_ns);  // no MMA of this CTA in flight
     }
   } else if (warp == kWarpMma2 || warp == kWarpMma3) {
-    // ------------------------------------------------------------ dV issuer / dK issuer
+    // ------------------------------------------------------------ dV issuer / dK (+dQ) issuer
     if (lane == 0 && ni > 0) {
+      // B = dO_t or Q_t as an MN-major operand (head dim contiguous); 16 queries per MMA
       constexpr uint32_t idO = idesc_bf16_f32(kT, kHD, false, true);
       const bool is_dv = warp == kWarpMma2;
-      // dV += P^T dO_t, dK += dS^T Q_t: 16 queries (8 TMEM columns, 16 smem rows) per MMA
       const uint32_t acc = tmem + (is_dv ? kKColDV : kKColDK);
-      const uint32_t a_op = tmem + (is_dv ? kKColPT : kKColDS);
       const int b_off = is_dv ? kKOffG : kKOffQ;
       const int done_bar = is_dv ? kKBarDVDone : kKBarDKDone;
+      // fused dK: A = dS^T from shared memory, K-major (queries contiguous in each 64-query
+      // half); dQ_t = dS K: A = the same bytes read as dS, MN-major (the two 64-query halves
+      // are the leading-dimension step), B = K, MN-major; 16 keys per MMA
+      constexpr uint32_t idQ = idesc_bf16_f32(kT, kHD, true, true);
+      const uint32_t sDS = smem_u32(smem + kKOffDS);
+      const uint64_t dsK = smem_desc_sw128(sDS, 1024, 1024);
+      const uint64_t dsM = smem_desc_sw128(sDS, kTileBytes, 1024);
+      const uint64_t dKt = smem_desc_sw128(smem_u32(smem + kKOffK), 1024, 1024);
       bool ok = true;
       for (int t = 0; ok && t < ni; ++t) {
         const int s = t % kStages;
@@ -563,10 +596,23 @@ __global__ void __launch_bounds__(kKThreads, 1)
         }
         tc_fence_after();
         const uint64_t bd = smem_desc_sw128(smem_u32(smem + b_off + s * kTileBytes), 1024, 1024);
+        if (kFused && !is_dv) {
 #pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_bf16_ts(acc, a_op + kk * 8, bd + kk * ((16 * 128) >> 4), idO,
-                      (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_bf16_ss(acc, dsK + (kk >> 2) * (kTileBytes >> 4) + (kk & 3) * 2,
+                        bd + kk * ((16 * 128) >> 4), idO, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_bf16_ss(tmem + kKColDQ, dsM + kk * ((16 * 128) >> 4),
+                        dKt + kk * ((16 * 128) >> 4), idQ, kk > 0 ? 1u : 0u);
+        } else {
+          // dV += P^T dO_t, dK += dS^T Q_t with A in TMEM (8 columns of bf16 pairs per MMA)
+          const uint32_t a_op = tmem + (is_dv ? kKColPT : kKColDS);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_bf16_ts(acc, a_op + kk * 8, bd + kk * ((16 * 128) >> 4), idO,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(bar(done_bar));
         mma_commit(bar(kKBarQEmpty + s));
       }
@@ -582,6 +628,20 @@ __global__ void __launch_bounds__(kKThreads, 1)
     const int key = k0 + r_local;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale * kLog2e;
+    // fused: this warp's dQ box (query rows 32*quarter.., columns 32*half..) of one query tile
+    // goes TMEM -> registers -> its staging buffer -> one bulk reduction into the accumulator
+    const uint32_t sStage = smem_u32(smem + kKOffStage + warp * kStageBytes);
+    auto reduce_dq = [&](const uint32_t* v, int q0) {
+      if (lane == 0) bulk_wait_group_read0();  // the previous box has left the buffer
+      __syncwarp();
+      st_row_sw128(sStage + lane * 128, lane, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_4d(&tmDQ, sStage, half * 32, q0 + quarter * 32, h, b);
+        bulk_commit_group();
+      }
+    };
     bool ok = true;
     for (int t = 0; t < ni; ++t) {
       const int s = t % kStages;
@@ -621,8 +681,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
       else
         dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
-      // the previous dV product must have read P^T, and the previous dK product dS^T, before
-      // they change
+      // the previous dV product must have read P^T, and the previous dK (and dQ) product
+      // dS^T, before they change
       if (t > 0 && !warp_all(mbar_wait(bar(kKBarDVDone), (t - 1) & 1, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteBwdMath);
         ok = false;
@@ -635,11 +695,45 @@ __global__ void __launch_bounds__(kKThreads, 1)
         ok = false;
         break;
       }
-      tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kKBarPFull));
+      if constexpr (kFused) {
+        // dQ_{t-1} leaves TMEM before dQ_t (issued after this tile's PFull) overwrites it
+        uint32_t dq[32];
+        tc_fence_after();
+        if (t > 0) tmem_ld32(tmem + kKColDQ + lane_off + half * 32, dq);
+        st_row_sw128(smem_u32(smem + kKOffDS + half * kTileBytes) + r_local * 128, lane, ds);
+        tmem_wait_st();
+        if (t > 0) {
+          tmem_wait_ld();
+          reg_fence(dq);
+        }
+        fence_proxy_async_smem();  // dS^T visible to the tensor core
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kKBarPFull));
+        if (t > 0) reduce_dq(dq, q0 - kT);
+      } else {
+        tmem_st32(tmem + kKColDS + lane_off + half * 32, ds);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kKBarPFull));
+      }
+    }
+    if constexpr (kFused) {
+      // the last query tile's dQ box
+      if (ok && ni > 0) {
+        if (warp_all(mbar_wait(bar(kKBarDKDone), (ni - 1) & 1, p.timeout_ns))) {
+          uint32_t dq[32];
+          tc_fence_after();
+          tmem_ld32(tmem + kKColDQ + lane_off + half * 32, dq);
+          tmem_wait_ld();
+          reg_fence(dq);
+          reduce_dq(dq, (i0 + ni - 1) * kT);
+        } else {
+          record_error(p.status, kErrTimeout, kSiteBwdEpi);
+          ok = false;
+        }
+      }
     }
     // ---- epilogue: warps of half 0 write dK * scale, those of half 1 dV, as bf16 (zeros for
     // keys no query sees)
@@ -669,6 +763,8 @@ __global__ void __launch_bounds__(kKThreads, 1)
         store_row(p.out1 + b * p.o1_b + h * p.o1_h + static_cast<int64_t>(key) * p.o1_n, a0,
                   a1, 1.f);
     }
+    // this warp's reductions have landed in global memory before the block ends
+    if (kFused && lane == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -678,11 +774,39 @@ __global__ void __launch_bounds__(kKThreads, 1)
   }
 }
 
+// dQ = scale * accumulator, as bf16 in dQ's layout; one thread per 8 consecutive values
+__global__ void __launch_bounds__(256)
+    sdpa_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                               int H, int Nq, int rows, int64_t sb, int64_t sh, int64_t sn,
+                               float scale, int64_t total) {
+  pdl_launch_dependents();
+  pdl_wait();  // the fused kernel's reductions are complete from here on
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int part = static_cast<int>(i & 7);
+    const int64_t r = i >> 3;  // (b, h, n) with n < Nq
+    const int n = static_cast<int>(r % Nq);
+    const int64_t bh = r / Nq;
+    const int hh = static_cast<int>(bh % H);
+    const int64_t bb = bh / H;
+    const float4* src = reinterpret_cast<const float4*>(acc + (bh * rows + n) * 64 + part * 8);
+    const float4 x = __ldcs(src), y = __ldcs(src + 1);
+    uint4 v;
+    v.x = pack_bf16x2(x.x * scale, x.y * scale);
+    v.y = pack_bf16x2(x.z * scale, x.w * scale);
+    v.z = pack_bf16x2(y.x * scale, y.y * scale);
+    v.w = pack_bf16x2(y.z * scale, y.w * scale);
+    *reinterpret_cast<uint4*>(dq + bb * sb + hh * sh + static_cast<int64_t>(n) * sn + part * 8) =
+        v;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                                  const CUtensorMap& tmV, const CUtensorMap& tmG,
-                                 const SdpaBwdArgs& a, const DevCtx& ctx, cudaStream_t s) {
+                                 const CUtensorMap& tmDQ, const SdpaBwdArgs& a,
+                                 const DevCtx& ctx, cudaStream_t s) {
   BwdParams p;
   p.H = a.H;
   p.Nq = a.Nq;
@@ -693,23 +817,28 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.stats = a.Dv;
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
-  cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(sdpa_bwd_dq_kernel), kQSmem,
-                                 nullptr);
-  if (e != cudaSuccess) return e;
+  const bool fused = !a.deterministic;
+  const void* kdkdv = fused ? reinterpret_cast<const void*>(sdpa_bwd_dkdv_kernel<true>)
+                            : reinterpret_cast<const void*>(sdpa_bwd_dkdv_kernel<false>);
   int regs = 0;
-  e = prepare_kernel(reinterpret_cast<const void*>(sdpa_bwd_dkdv_kernel), kKSmem, &regs);
+  cudaError_t e = prepare_kernel(kdkdv, k_smem(fused), &regs);
   if (e != cudaSuccess) return e;
   // the dkdv kernel's setmaxnreg split must fit in what its blocks launch with, or the
   // increase would wait forever: refuse to launch if the compiled register count is too small
   if (regs * kKThreads < kMathWarps * 32 * kKMathRegs + 4 * 32 * kKControlRegs)
     return cudaErrorInvalidConfiguration;
-  p.out0 = static_cast<__nv_bfloat16*>(a.dQ);
-  p.o0_b = a.st[5][0];
-  p.o0_h = a.st[5][1];
-  p.o0_n = a.st[5][2];
-  (void)launch_pdl(sdpa_bwd_dq_kernel, dim3(dim3((a.Nq + kT - 1) / kT, a.H, a.B)), dim3(kQThreads), kQSmem, s, tmQ, tmK, tmV, tmG, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!fused) {
+    e = prepare_kernel(reinterpret_cast<const void*>(sdpa_bwd_dq_kernel), kQSmem, nullptr);
+    if (e != cudaSuccess) return e;
+    p.out0 = static_cast<__nv_bfloat16*>(a.dQ);
+    p.o0_b = a.st[5][0];
+    p.o0_h = a.st[5][1];
+    p.o0_n = a.st[5][2];
+    (void)launch_pdl(sdpa_bwd_dq_kernel, dim3((a.Nq + kT - 1) / kT, a.H, a.B), dim3(kQThreads),
+                     kQSmem, s, tmQ, tmK, tmV, tmG, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   p.out0 = static_cast<__nv_bfloat16*>(a.dK);
   p.o0_b = a.st[6][0];
   p.o0_h = a.st[6][1];
@@ -718,7 +847,24 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.o1_b = a.st[7][0];
   p.o1_h = a.st[7][1];
   p.o1_n = a.st[7][2];
-  (void)launch_pdl(sdpa_bwd_dkdv_kernel, dim3(dim3((a.Nk + kT - 1) / kT, a.H, a.B)), dim3(kKThreads), kKSmem, s, tmQ, tmK, tmV, tmG, p);
+  const dim3 grid((a.Nk + kT - 1) / kT, a.H, a.B);
+  if (fused)
+    (void)launch_pdl(sdpa_bwd_dkdv_kernel<true>, grid, dim3(kKThreads), k_smem(true), s, tmQ, tmK,
+                     tmV, tmG, tmDQ, p);
+  else
+    (void)launch_pdl(sdpa_bwd_dkdv_kernel<false>, grid, dim3(kKThreads), k_smem(false), s, tmQ,
+                     tmK, tmV, tmG, tmDQ, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !fused) return e;
+  const int rows = (a.Nq + kT - 1) / kT * kT;
+  const int64_t total = static_cast<int64_t>(a.B) * a.H * a.Nq * 8;
+  const int64_t want = (total + 255) / 256;
+  const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(ctx.num_sms) * 8));
+  (void)launch_pdl(sdpa_bwd_dq_convert_kernel, dim3(blocks), dim3(256), 0, s,
+                   reinterpret_cast<const float*>(reinterpret_cast<const char*>(a.Dv) +
+                                                  sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)),
+                   static_cast<__nv_bfloat16*>(a.dQ), a.H, a.Nq, rows, a.st[5][0], a.st[5][1],
+                   a.st[5][2], a.scale, total);
   return cudaGetLastError();
 }
 

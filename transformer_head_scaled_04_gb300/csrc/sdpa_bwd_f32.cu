@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     sdpa_bwd_rowdot_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
                            int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
-                           const float* __restrict__ lse, int rows) {
+                           const float* __restrict__ lse, int rows, float* __restrict__ dq_acc) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   // lse != null: the per-tile layout {-lse * log2 e [128], -D [128]} (negated, so the
@@ -70,8 +70,11 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   }
-  if (lane != 0) return;
   const int64_t bh = static_cast<int64_t>(b) * H + h;
+  // the fused bf16 backward adds dQ contributions into a zeroed fp32 row of 64 per query
+  if (dq_acc != nullptr)
+    reinterpret_cast<float2*>(dq_acc + (bh * rows + row) * 64)[lane] = make_float2(0.f, 0.f);
+  if (lane != 0) return;
   if (lse == nullptr) {
     Dv[bh * Nq + row] = acc;
   } else {
@@ -199,11 +202,14 @@ cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t
   if (dtype == 1)
     (void)launch_pdl(sdpa_bwd_rowdot_kernel<__nv_bfloat16>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.Dv,
         a.H, a.Nq, a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1],
-        a.st[4][2], a.lse, rows);
+        a.st[4][2], a.lse, rows,
+        a.deterministic ? nullptr
+                        : reinterpret_cast<float*>(reinterpret_cast<char*>(a.Dv) +
+                                                   sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)));
   else
     (void)launch_pdl(sdpa_bwd_rowdot_kernel<float>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
         a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], nullptr,
-        rows);
+        rows, nullptr);
   return cudaGetLastError();
 }
 
