@@ -282,8 +282,9 @@ def test_decode_workspace_and_validation(lib):
 def test_sdpa_backward_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.mha_sdpa_bwd_workspace_size(8, 16, 4096, 1, ctypes.byref(n)) == 0
-    # per 128-row tile: lse and D (1 KB), then the fp32 dQ accumulator's 128 x 64 values
-    assert n.value == 8 * 16 * 32 * (1024 + 128 * 64 * 4)
+    # per 128-row tile: lse and D (1 KB), the dK/dV kernel's extra-K-step operand (8 KB),
+    # then the fp32 dQ accumulator's 128 x 64 values
+    assert n.value == 8 * 16 * 32 * (1024 + 8192 + 128 * 64 * 4)
     assert lib.mha_sdpa_bwd_workspace_size(8, 16, 4096, 0, ctypes.byref(n)) == 0
     assert n.value == 8 * 16 * 4096 * 4            # fp32 path: D per row
     assert lib.mha_sdpa_bwd_workspace_size(0, 16, 4096, 1, ctypes.byref(n)) == C.MHA_ERR_INVALID

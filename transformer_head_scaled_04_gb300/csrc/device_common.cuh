@@ -330,6 +330,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
+// The same descriptor for a K-major operand without swizzle (layout type 0): 8-row x 16-byte
+// core matrices, `lbo_bytes` apart along K and `sbo_bytes` apart along M / N.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t addr, uint32_t lbo_bytes,
+                                                        uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
 // Instruction descriptor for tcgen05.mma kind::f16 with bf16 A and B and an fp32 accumulator.
 // a_mn / b_mn select MN-major operands (else K-major).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {

@@ -113,17 +113,24 @@ struct SdpaBwdArgs {
   // rowsum(dO * O) as [B, H, Nq]; bf16 path, per 128-row query tile of every (b, h) the
   // tile's lse * log2(e) [128] then its D [128] (rows past Nq: +inf and 0), so one 1 KB bulk
   // copy brings a tile's statistics into shared memory
-  // bf16 path, after those statistics (at sdpa_bwd_dq_acc_offset bytes into the scratch):
-  // an fp32 dQ accumulator [B, H, 128 * tiles, 64] that the rowdot launch zeroes and the
-  // fused kernel adds every key tile's dS K into; unused when deterministic
+  // bf16 path, after those statistics (at sdpa_bwd_aug_offset): per query tile an 8 KB
+  // operand block for the dK/dV kernel's tensor-core products, four 128 x 8 bf16 column
+  // chunks (row r of chunk k at (k * 128 + r) * 16 bytes, the no-swizzle K-major layout):
+  // chunk 0 = (-lse / scale) as a sum of three bf16 terms, chunk 2 = -D likewise, chunks 1
+  // and 3 zero; then (at sdpa_bwd_dq_acc_offset) an fp32 dQ accumulator
+  // [B, H, 128 * tiles, 64] that the rowdot launch zeroes and the fused kernel adds every key
+  // tile's dS K into (unused when deterministic)
   float* Dv;
   bool deterministic;        // bf16: dQ by its own kernel instead of the fused accumulation
   void *dQ, *dK, *dV;
   int64_t st[8][4];          // element strides b, h, n, d of Q, K, V, O, dO, dQ, dK, dV
 };
 cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s);
-inline size_t sdpa_bwd_dq_acc_offset(int B, int H, int Nq) {
+inline size_t sdpa_bwd_aug_offset(int B, int H, int Nq) {
   return static_cast<size_t>(B) * H * ((Nq + 127) / 128) * 1024;
+}
+inline size_t sdpa_bwd_dq_acc_offset(int B, int H, int Nq) {
+  return static_cast<size_t>(B) * H * ((Nq + 127) / 128) * (1024 + 8192);
 }
 // bytes of the Dv scratch above
 inline size_t sdpa_bwd_scratch_bytes(int B, int H, int Nq, int dtype) {

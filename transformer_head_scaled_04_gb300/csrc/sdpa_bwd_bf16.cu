@@ -65,6 +65,7 @@ struct BwdParams {
   const int32_t* key_len;
   float scale;       // multiplies q.k
   const float* stats;  // per (b, h, 128-row query tile): -lse * log2 e [128], then -D [128]
+  const uint8_t* aug;  // per (b, h, query tile): the dkdv kernel's 8 KB extra-K-step operand
   __nv_bfloat16* out0;  // dq: dQ; dkdv: dK
   __nv_bfloat16* out1;  // dkdv: dV
   int64_t o0_b, o0_h, o0_n, o1_b, o1_h, o1_n;
@@ -121,14 +122,15 @@ __device__ __forceinline__ void dq_half(const uint32_t* s0, const uint32_t* s1,
   }
 }
 
-// P^T and dS^T of one 64-query half of a key row; st: this query tile's -lse2 [128] then
-// -D [128] in shared memory, ca0 the half's first query column.  kMask: query q0 + ca sees
-// this key only when ca >= first_ok (causal) and the key is below the key limit (row_ok).
+// P^T and dS^T of one 64-query half of a key row.  The products already hold the query
+// statistics (an extra K step adds -lse / scale to S^T and -D to dP^T, column by column), so
+// p = 2^(c s') and dS = p dP'; ca0 is the half's first query column.  kMask: query q0 + ca
+// sees this key only when ca >= first_ok (causal) and the key is below the key limit (row_ok).
 template <bool kMask>
 __device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1,
-                                          const uint32_t* g0, const uint32_t* g1,
-                                          const float* st, int ca0, bool row_ok, int first_ok,
-                                          float c, uint32_t* pp, uint32_t* ds) {
+                                          const uint32_t* g0, const uint32_t* g1, int ca0,
+                                          bool row_ok, int first_ok, float c, uint32_t* pp,
+                                          uint32_t* ds) {
   const float2 c2 = make_float2(c, c);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -137,9 +139,7 @@ __device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1
                                   __uint_as_float(i < 16 ? s0[2 * i + 1] : s1[2 * i + 1 - 32]));
     const float2 gv = make_float2(__uint_as_float(i < 16 ? g0[2 * i] : g1[2 * i - 32]),
                                   __uint_as_float(i < 16 ? g0[2 * i + 1] : g1[2 * i + 1 - 32]));
-    const float2 nl2 = *reinterpret_cast<const float2*>(st + ca);
-    const float2 nd2 = *reinterpret_cast<const float2*>(st + kT + ca);
-    float2 pv = ffma2(sv, c2, nl2);
+    float2 pv = fmul2(sv, c2);
     pv.x = ex2_approx(pv.x);
     pv.y = ex2_approx(pv.y);
     if (kMask) {
@@ -147,7 +147,7 @@ __device__ __forceinline__ void dkdv_half(const uint32_t* s0, const uint32_t* s1
       if (!row_ok || ca + 1 < first_ok) pv.y = 0.f;
     }
     pp[i] = pack_bf16x2(pv.x, pv.y);
-    const float2 dv = fmul2(pv, fadd2(gv, nd2));
+    const float2 dv = fmul2(pv, gv);
     ds[i] = pack_bf16x2(dv.x, dv.y);
   }
 }
@@ -408,15 +408,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // One CTA per 128-key tile.  kFused (the default path) also produces this key tile's share of
 // dQ: dQ_i += dS_i K for every query tile i it walks, added in fp32 into a workspace
 // accumulator by bulk tensor reductions, so no second kernel rebuilds S and dP for dQ.
-// smem: K, V (once), Q ring, dO ring, -lse2/-D ring (2 x 128 floats per stage), then, fused,
+// smem: K, V (once), Q ring, dO ring, ring of the query tiles' 8 KB extra-K-step operands
+// (-lse / scale and -D, no swizzle), the key side's constant extra-K-step operand, then, fused,
 // dS^T (two 64-query halves, each laid out like a 128-row swizzled tile) and one 32 x 32 fp32
 // staging box per math warp, then barriers
 constexpr int kKOffK = 0;
 constexpr int kKOffV = kKOffK + kTileBytes;
 constexpr int kKOffQ = kKOffV + kTileBytes;
 constexpr int kKOffG = kKOffQ + kStages * kTileBytes;
-constexpr int kKOffStat = kKOffG + kStages * kTileBytes;  // float [kStages][2][128]
-constexpr int kKOffDS = kKOffStat + kStages * 2 * kT * 4;  // fused only
+constexpr int kAugBytes = 8192;
+constexpr int kKOffAug = kKOffG + kStages * kTileBytes;    // [kStages][4 chunks][128][16 B]
+constexpr int kKOffKAug = kKOffAug + kStages * kAugBytes;  // [2 chunks][128][16 B]
+constexpr int kKOffDS = kKOffKAug + 4096;                  // fused only
 constexpr int kKOffStage = kKOffDS + 2 * kTileBytes;       // fused only: [kMathWarps][4 KB]
 constexpr int kStageBytes = 32 * 32 * 4;
 __host__ __device__ constexpr int k_off_bar(bool fused) {
@@ -463,7 +466,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
   uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + k_off_bar(kFused));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kKNumBars);
-  float* sstat = reinterpret_cast<float*>(smem + kKOffStat);
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -489,6 +491,14 @@ __global__ void __launch_bounds__(kKThreads, 1)
     mbar_init(bar(kKBarDrain), 3);
     fence_mbar_init();
   }
+  if (threadIdx.x < kT) {
+    // the key side of the extra K step: columns 0-2 of every row are 1 (they pick up the
+    // three bf16 terms of the query side), the rest 0; core matrices without swizzle
+    const uint32_t row = smem_u32(smem + kKOffKAug) + threadIdx.x * 16;
+    st_shared_v4(row, make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u));
+    st_shared_v4(row + kT * 16, make_uint4(0u, 0u, 0u, 0u));
+    fence_proxy_async_smem();
+  }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -503,7 +513,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
   // 256 x 200 + 128 x 72 = 60416 <= 64512
   if (warp >= kMathWarps) regs_dec<kKControlRegs>();  // first: the math warps' increase waits on it
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer (TMA + stats)
+    // ------------------------------------------------------------ producer (TMA)
     if (lane == 0 && ni > 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
@@ -512,7 +522,7 @@ __global__ void __launch_bounds__(kKThreads, 1)
       mbar_arrive_expect_tx(bar(kKBarIn), 2 * kTileBytes);
       tma_load_4d(smem_u32(smem + kKOffK), &tmK, bar(kKBarIn), 0, k0, h, b);
       tma_load_4d(smem_u32(smem + kKOffV), &tmV, bar(kKBarIn), 0, k0, h, b);
-      const float* st_bh = p.stats + (static_cast<int64_t>(b) * p.H + h) * nqt * (2 * kT);
+      const uint8_t* aug_bh = p.aug + (static_cast<int64_t>(b) * p.H + h) * nqt * kAugBytes;
       bool ok = true;
       int issued = 0;
       for (int t = 0; t < ni; ++t) {
@@ -522,13 +532,13 @@ __global__ void __launch_bounds__(kKThreads, 1)
           ok = false;
           break;
         }
-        // Q_t, dO_t and the tile's statistics (-lse2 and -D, 1 KB) on one barrier
-        mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes + 2 * kT * 4);
+        // Q_t, dO_t and the tile's extra-K-step operand (-lse / scale, -D: 8 KB) on one barrier
+        mbar_arrive_expect_tx(bar(kKBarQ + s), 2 * kTileBytes + kAugBytes);
         tma_load_4d(smem_u32(smem + kKOffQ + s * kTileBytes), &tmQ, bar(kKBarQ + s), 0, qt * kT,
                     h, b);
         tma_load_4d(smem_u32(smem + kKOffG + s * kTileBytes), &tmG, bar(kKBarQ + s), 0, qt * kT,
                     h, b);
-        bulk_load(smem_u32(sstat + s * 2 * kT), st_bh + qt * (2 * kT), 2 * kT * 4,
+        bulk_load(smem_u32(smem + kKOffAug + s * kAugBytes), aug_bh + qt * kAugBytes, kAugBytes,
                   bar(kKBarQ + s));
         issued = t + 1;
       }
@@ -543,7 +553,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
       constexpr uint32_t idS = idesc_bf16_f32(kT, kT, false, false);
       const uint64_t dKd = smem_desc_sw128(smem_u32(smem + kKOffK), 1024, 1024);
       const uint64_t dVd = smem_desc_sw128(smem_u32(smem + kKOffV), 1024, 1024);
-      // S^T_t = K Q_t^T and dP^T_t = V dO_t^T into the single S/dP buffer
+      // the extra K step (no swizzle: 16-byte core-matrix rows, K chunks 2 KB apart): key side
+      // all ones in columns 0-2, query side -lse / scale (chunks 0-1) or -D (chunks 2-3)
+      const uint64_t dKa = smem_desc_noswizzle(smem_u32(smem + kKOffKAug), kT * 16, 128);
+      // S^T_t = K Q_t^T - lse / scale and dP^T_t = V dO_t^T - D into the single S/dP buffer
       auto issue_s = [&](int t) -> bool {
         const int s = t % kStages;
         if (!mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns)) return false;
@@ -555,6 +568,10 @@ __global__ void __launch_bounds__(kKThreads, 1)
           mma_bf16_ss(tmem + kKColS, dKd + kk * 2, dQ + kk * 2, idS, kk > 0 ? 1u : 0u);
           mma_bf16_ss(tmem + kKColP, dVd + kk * 2, dG + kk * 2, idS, kk > 0 ? 1u : 0u);
         }
+        const uint64_t dA =
+            smem_desc_noswizzle(smem_u32(smem + kKOffAug + s * kAugBytes), kT * 16, 128);
+        mma_bf16_ss(tmem + kKColS, dKa, dA, idS, 1u);
+        mma_bf16_ss(tmem + kKColP, dKa, dA + ((2 * kT * 16) >> 4), idS, 1u);
         mma_commit(bar(kKBarSFull));
         mma_commit(bar(kKBarQEmpty + s));  // this issuer is done with Q_t, dO_t
         return true;
@@ -644,7 +661,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
     };
     bool ok = true;
     for (int t = 0; t < ni; ++t) {
-      const int s = t % kStages;
       const int q0 = (i0 + t) * kT;
       if (!warp_all(mbar_wait(bar(kKBarSFull), t & 1, p.timeout_ns))) {
         record_error(p.status, kErrTimeout, kSiteBwdMath);
@@ -652,14 +668,6 @@ __global__ void __launch_bounds__(kKThreads, 1)
         break;
       }
       tc_fence_after();
-      // the statistics came by bulk copy on the Q_t barrier: observe its completion here too
-      // (it completed before S^T_t was issued) so their bytes are visible to these threads
-      if (!warp_all(mbar_wait(bar(kKBarQ + s), (t / kStages) & 1, p.timeout_ns))) {
-        record_error(p.status, kErrTimeout, kSiteBwdMath);
-        ok = false;
-        break;
-      }
-      const float* st = sstat + s * 2 * kT;
       uint32_t s0[32], s1[32], g0[32], g1[32];
       tmem_ld32(tmem + kKColS + lane_off + half * 64, s0);
       tmem_ld32(tmem + kKColS + lane_off + half * 64 + 32, s1);
@@ -678,9 +686,9 @@ __global__ void __launch_bounds__(kKThreads, 1)
       const bool row_ok = key < L;
       const int first_ok = (p.mask == 1) ? key - q0 : -kT;
       if (warp_all(row_ok && first_ok <= half * 64))  // every pair of this half is allowed
-        dkdv_half<false>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
+        dkdv_half<false>(s0, s1, g0, g1, half * 64, row_ok, first_ok, c, pp, ds);
       else
-        dkdv_half<true>(s0, s1, g0, g1, st, half * 64, row_ok, first_ok, c, pp, ds);
+        dkdv_half<true>(s0, s1, g0, g1, half * 64, row_ok, first_ok, c, pp, ds);
       // the previous dV product must have read P^T, and the previous dK (and dQ) product
       // dS^T, before they change
       if (t > 0 && !warp_all(mbar_wait(bar(kKBarDVDone), (t - 1) & 1, p.timeout_ns))) {
@@ -815,6 +823,7 @@ cudaError_t launch_sdpa_bwd_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.key_len = a.key_len;
   p.scale = a.scale;
   p.stats = a.Dv;
+  p.aug = reinterpret_cast<const uint8_t*>(a.Dv) + sdpa_bwd_aug_offset(a.B, a.H, a.Nq);
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
   const bool fused = !a.deterministic;

@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     sdpa_bwd_rowdot_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
                            int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
-                           const float* __restrict__ lse, int rows, float* __restrict__ dq_acc) {
+                           const float* __restrict__ lse, int rows, float* __restrict__ dq_acc,
+                           uint4* __restrict__ aug, float c) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   // lse != null: the per-tile layout {-lse * log2 e [128], -D [128]} (negated, so the
@@ -74,6 +75,28 @@ __global__ void __launch_bounds__(kWarps * 32)
   // the fused bf16 backward adds dQ contributions into a zeroed fp32 row of 64 per query
   if (dq_acc != nullptr)
     reinterpret_cast<float2*>(dq_acc + (bh * rows + row) * 64)[lane] = make_float2(0.f, 0.f);
+  // the dK/dV kernel's extra K step: row `row` of the tile's four 8-column chunks; chunk 0
+  // holds -lse / scale (so that c * (s - lse / scale) = s * c - lse * log2 e with
+  // c = scale * log2 e) and chunk 2 holds -D, each as three bf16 terms whose sum is the fp32
+  // value to within fp32 rounding; rows past Nq get a large negative stand-in for -inf (and a
+  // fully masked row's +inf is clamped the same way: its keys are masked in the kernel)
+  if (aug != nullptr && lane < 4) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0 || lane == 2) {
+      float x = lane == 2 ? -acc
+                          : (row < Nq ? -(__ldg(lse + bh * Nq + row) * 1.4426950408889634f) / c
+                                      : -1e30f);
+      if (!(fabsf(x) <= 1e30f)) x = x > 0.f ? 1e30f : -1e30f;
+      const __nv_bfloat16 t0 = __float2bfloat16_rn(x);
+      const float r1 = x - __bfloat162float(t0);
+      const __nv_bfloat16 t1 = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 t2 = __float2bfloat16_rn(r1 - __bfloat162float(t1));
+      v.x = static_cast<uint32_t>(__bfloat16_as_ushort(t0)) |
+            (static_cast<uint32_t>(__bfloat16_as_ushort(t1)) << 16);
+      v.y = static_cast<uint32_t>(__bfloat16_as_ushort(t2));
+    }
+    aug[(bh * (rows / 128) + row / 128) * 512 + lane * 128 + row % 128] = v;
+  }
   if (lane != 0) return;
   if (lse == nullptr) {
     Dv[bh * Nq + row] = acc;
@@ -205,11 +228,14 @@ cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t
         a.st[4][2], a.lse, rows,
         a.deterministic ? nullptr
                         : reinterpret_cast<float*>(reinterpret_cast<char*>(a.Dv) +
-                                                   sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)));
+                                                   sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)),
+        reinterpret_cast<uint4*>(reinterpret_cast<char*>(a.Dv) +
+                                 sdpa_bwd_aug_offset(a.B, a.H, a.Nq)),
+        a.scale * 1.4426950408889634f);
   else
     (void)launch_pdl(sdpa_bwd_rowdot_kernel<float>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
         a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], nullptr,
-        rows, nullptr);
+        rows, nullptr, nullptr, 0.f);
   return cudaGetLastError();
 }
 
