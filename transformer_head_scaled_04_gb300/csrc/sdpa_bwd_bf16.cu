@@ -3,27 +3,33 @@
 // The chain rule through O = softmax(Q K^T * scale, masked) V ("Transformer：抛弃循环与卷积的
 // 序列建模", Transformer 训练样例 > 反向传播; "Attention Is All You Need", lettle.cn
 // translation, 3.2.1 缩放点积注意力).  The softmax weights are rebuilt tile by tile from the
-// forward's log-sum-exp (P = 2^(s*c - lse2), c = scale*log2 e, lse2 = lse*log2 e), so the
-// n x n matrices never leave the SM:
-//   dS = P * (dP - D),  dP = dO V^T,  D_i = sum_d dO_id O_id
-// (a small prior launch writes -D and -lse * log2 e per 128-row query tile, 1 KB per tile)
+// forward's log-sum-exp, so the n x n matrices never leave the SM:
+//   P = 2^(s*c - lse2) (c = scale*log2 e, lse2 = lse*log2 e),  dP = dO V^T,
+//   dS = P * (dP - D),  D_i = sum_d dO_id O_id,
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO
-// Two kernels, neither with atomics:
-//   dq   -- one CTA per 128-row query tile; K/V tiles stream through a TMA ring.
-//           tcgen05.mma: S = Q K^T and dP = dO V^T (128x128x16, fp32 in TMEM); four math
-//           warps (one query row per thread) turn a 64-key half at a time into bf16 dS in
-//           TMEM; dQ += dS K (128x64x16, A = dS from TMEM, B = K as an MN-major operand).
-//   dkdv -- one CTA per 128-key tile; Q/dO tiles (and their lse, D) stream through a ring.
-//           S^T = K Q^T and dP^T = V dO^T; the math warps (one key row per thread) write bf16
-//           P^T and dS^T into TMEM; dV += P^T dO and dK += dS^T Q accumulate in TMEM
-//           (all 512 columns: S^T, dP^T, P^T, dS^T, dV, dK).
+// A small prior launch writes, per 128-row query tile, -D and -lse2 (1 KB) and an 8 KB operand
+// block holding -lse / scale and -D as three bf16 terms each, and zeroes an fp32 dQ
+// accumulator.  Then:
+//   dkdv -- one CTA per 128-key tile; Q/dO tiles (with their operand blocks) stream through a
+//           TMA ring.  S^T = K Q^T and dP^T = V dO^T (tcgen05.mma 128x128x16, fp32 in TMEM),
+//           each with a fifth K step against a constant "ones" operand, so TMEM already holds
+//           s - lse / scale and dP - D and the math warps (one key row per thread) read no
+//           statistics: p = 2^(c s'), dS = p dP'.  They write bf16 P^T into TMEM and dS^T into
+//           shared memory; dV += P^T dO (A from TMEM) and dK += dS^T Q (A from shared memory)
+//           accumulate in TMEM.  By default the same issuer then computes this key tile's part
+//           of dQ for the query tile, dS K (A = dS^T's bytes read MN-major, B = K), which the
+//           math warps move out of TMEM and add into the accumulator with one bulk tensor
+//           reduction per warp (32 x 32 fp32 box); a last launch scales it into bf16 dQ.
+//   dq   -- only when deterministic results are asked for (no atomics anywhere): one CTA per
+//           128-row query tile rebuilds S and dP from K/V tiles streamed through a ring, four
+//           math warps per column half turn them into bf16 dS in TMEM, dQ += dS K.
 // Warps: 0-7 math (two per sub-partition: warps w and w+4 share TMEM lanes 32*(w%4).. and
 // take the two 64-column halves of every tile), 8 TMA producer, 9 TMEM owner and issuer of S
 // and dP (S^T and dP^T), then the gradient issuers: dq kernel warp 10 (dQ, with dS double-
 // buffered in TMEM so the math warps write dS_{j+1} while dQ still reads dS_j), dkdv kernel
-// warps 10 (dV) and 11 (dK; its math warps run at 200 registers through setmaxnreg).  Every
-// wait is bounded; a timeout records MHA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs
-// land, frees TMEM.
+// warps 10 (dV) and 11 (dK, and dQ when fused; its math warps run at 200 registers through
+// setmaxnreg).  Every wait is bounded; a timeout records MHA_ERR_DEVICE_TIMEOUT, lets
+// in-flight copies and MMAs land, frees TMEM.
 // Masks: none, causal (j <= i) and key padding (j < key_len[b]); fully masked tiles are
 // skipped, and the d = 64 heads of the forward kernel are assumed.
 #include <cuda_bf16.h>
