@@ -52,8 +52,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     sdpa_bwd_rowdot_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                            float* __restrict__ Dv, int H, int Nq, int d_v, int64_t ob,
                            int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
-                           const float* __restrict__ lse, int rows, float* __restrict__ dq_acc,
-                           uint4* __restrict__ aug, float c) {
+                           const float* __restrict__ lse, int rows) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   // lse != null: the per-tile layout {-lse * log2 e [128], -D [128]} (negated, so the
@@ -71,39 +70,84 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   }
-  const int64_t bh = static_cast<int64_t>(b) * H + h;
-  // the fused bf16 backward adds dQ contributions into a zeroed fp32 row of 64 per query
-  if (dq_acc != nullptr)
-    reinterpret_cast<float2*>(dq_acc + (bh * rows + row) * 64)[lane] = make_float2(0.f, 0.f);
-  // the dK/dV kernel's extra K step: row `row` of the tile's four 8-column chunks; chunk 0
-  // holds -lse / scale (so that c * (s - lse / scale) = s * c - lse * log2 e with
-  // c = scale * log2 e) and chunk 2 holds -D, each as three bf16 terms whose sum is the fp32
-  // value to within fp32 rounding; rows past Nq get a large negative stand-in for -inf (and a
-  // fully masked row's +inf is clamped the same way: its keys are masked in the kernel)
-  if (aug != nullptr && lane < 4) {
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 0 || lane == 2) {
-      float x = lane == 2 ? -acc
-                          : (row < Nq ? -(__ldg(lse + bh * Nq + row) * 1.4426950408889634f) / c
-                                      : -1e30f);
-      if (!(fabsf(x) <= 1e30f)) x = x > 0.f ? 1e30f : -1e30f;
-      const __nv_bfloat16 t0 = __float2bfloat16_rn(x);
-      const float r1 = x - __bfloat162float(t0);
-      const __nv_bfloat16 t1 = __float2bfloat16_rn(r1);
-      const __nv_bfloat16 t2 = __float2bfloat16_rn(r1 - __bfloat162float(t1));
-      v.x = static_cast<uint32_t>(__bfloat16_as_ushort(t0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(t1)) << 16);
-      v.y = static_cast<uint32_t>(__bfloat16_as_ushort(t2));
-    }
-    aug[(bh * (rows / 128) + row / 128) * 512 + lane * 128 + row % 128] = v;
-  }
   if (lane != 0) return;
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
   if (lse == nullptr) {
     Dv[bh * Nq + row] = acc;
   } else {
     float* tile = Dv + (bh * (rows / 128) + row / 128) * 256;
     tile[row % 128] = row < Nq ? -(__ldg(lse + bh * Nq + row) * 1.4426950408889634f) : -INFINITY;
     tile[128 + row % 128] = -acc;
+  }
+}
+
+// bf16 tensor-core path: per query row, D = sum_d dO_d O_d (d = 64) and the per-tile layouts
+// the backward kernels read; 16-byte loads, eight lanes per row, four rows per warp.
+//   stats: per (b, h, 128-row tile) -lse * log2 e [128] then -D [128] (rows past Nq: -inf, 0)
+//   aug:   per tile four 128 x 8 bf16 column chunks (row r of chunk k at (k * 128 + r) * 16
+//          bytes): chunk 0 = -lse / scale, chunk 2 = -D, each as three bf16 terms summing to
+//          the fp32 value; chunks 1 and 3 zero.  c = scale * log2 e, so c * (-lse / scale) =
+//          -lse * log2 e.  Rows past Nq get a large negative stand-in for -inf, and so does a
+//          fully masked row's +inf (its keys are masked by the kernel that reads it).
+//   dq_acc (may be null): the row's 64 fp32 dQ accumulators zeroed
+__device__ __forceinline__ uint4 three_bf16_terms(float x) {
+  if (!(fabsf(x) <= 1e30f)) x = x > 0.f ? 1e30f : -1e30f;
+  const __nv_bfloat16 t0 = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(t0);
+  const __nv_bfloat16 t1 = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 t2 = __float2bfloat16_rn(r1 - __bfloat162float(t1));
+  return make_uint4(static_cast<uint32_t>(__bfloat16_as_ushort(t0)) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(t1)) << 16),
+                    static_cast<uint32_t>(__bfloat16_as_ushort(t2)), 0u, 0u);
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    sdpa_bwd_rowdot_bf16_kernel(const __nv_bfloat16* __restrict__ O,
+                                const __nv_bfloat16* __restrict__ dO, int H, int Nq, int64_t ob,
+                                int64_t oh, int64_t on, int64_t gb, int64_t gh, int64_t gn,
+                                const float* __restrict__ lse, int rows, float c,
+                                float* __restrict__ stats, uint4* __restrict__ aug,
+                                float* __restrict__ dq_acc) {
+  pdl_launch_dependents();
+  pdl_wait();  // the previous kernel's output is complete from here on
+  const int lane = threadIdx.x & 31, part = lane & 7;
+  const int row = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * 4 + (lane >> 3);
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (row >= rows) return;  // rows is a multiple of 128: whole 8-lane groups leave together
+  const bool valid = row < Nq;
+  float acc = 0.f;
+  if (valid) {
+    const uint4 o = __ldg(reinterpret_cast<const uint4*>(O + b * ob + h * oh +
+                                                         static_cast<int64_t>(row) * on) + part);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + b * gb + h * gh +
+                                                         static_cast<int64_t>(row) * gn) + part);
+    const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[i]));
+      const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gv[i]));
+      acc = fmaf(of.x, gf.x, acc);
+      acc = fmaf(of.y, gf.y, acc);
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
+  const int64_t tile = bh * (rows / 128) + row / 128;
+  const float l2 = valid ? __ldg(lse + bh * Nq + row) * 1.4426950408889634f : INFINITY;
+  if (part == 0) stats[tile * 256 + row % 128] = -l2;
+  if (part == 1) stats[tile * 256 + 128 + row % 128] = -acc;
+  if (part < 4) {
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (part == 0) v = three_bf16_terms(valid ? -l2 / c : -1e30f);
+    if (part == 2) v = three_bf16_terms(-acc);
+    aug[tile * 512 + part * 128 + row % 128] = v;
+  }
+  if (dq_acc != nullptr) {
+    uint4* z = reinterpret_cast<uint4*>(dq_acc + (bh * rows + row) * 64) + part * 2;
+    z[0] = make_uint4(0u, 0u, 0u, 0u);
+    z[1] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -220,22 +264,25 @@ __global__ void __launch_bounds__(kWarps * 32) sdpa_bwd_dkdv_f32_kernel(const Bw
 }  // namespace
 
 cudaError_t launch_sdpa_bwd_rowdot(const SdpaBwdArgs& a, int dtype, cudaStream_t s) {
-  const int rows = dtype == 1 ? (a.Nq + 127) / 128 * 128 : a.Nq;
-  dim3 grid((rows + kWarps - 1) / kWarps, a.H, a.B);
-  if (dtype == 1)
-    (void)launch_pdl(sdpa_bwd_rowdot_kernel<__nv_bfloat16>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.Dv,
-        a.H, a.Nq, a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1],
-        a.st[4][2], a.lse, rows,
-        a.deterministic ? nullptr
-                        : reinterpret_cast<float*>(reinterpret_cast<char*>(a.Dv) +
-                                                   sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)),
-        reinterpret_cast<uint4*>(reinterpret_cast<char*>(a.Dv) +
-                                 sdpa_bwd_aug_offset(a.B, a.H, a.Nq)),
-        a.scale * 1.4426950408889634f);
-  else
-    (void)launch_pdl(sdpa_bwd_rowdot_kernel<float>, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H, a.Nq,
-        a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], nullptr,
-        rows, nullptr, nullptr, 0.f);
+  if (dtype == 1) {
+    const int rows = (a.Nq + 127) / 128 * 128;
+    char* base = reinterpret_cast<char*>(a.Dv);
+    (void)launch_pdl(sdpa_bwd_rowdot_bf16_kernel, dim3(rows / (4 * kWarps), a.H, a.B),
+                     dim3(kWarps * 32), 0, s, static_cast<const __nv_bfloat16*>(a.O),
+                     static_cast<const __nv_bfloat16*>(a.dO), a.H, a.Nq, a.st[3][0], a.st[3][1],
+                     a.st[3][2], a.st[4][0], a.st[4][1], a.st[4][2], a.lse, rows,
+                     a.scale * 1.4426950408889634f, a.Dv,
+                     reinterpret_cast<uint4*>(base + sdpa_bwd_aug_offset(a.B, a.H, a.Nq)),
+                     a.deterministic ? nullptr
+                                     : reinterpret_cast<float*>(
+                                           base + sdpa_bwd_dq_acc_offset(a.B, a.H, a.Nq)));
+    return cudaGetLastError();
+  }
+  dim3 grid((a.Nq + kWarps - 1) / kWarps, a.H, a.B);
+  (void)launch_pdl(sdpa_bwd_rowdot_kernel<float>, dim3(grid), dim3(kWarps * 32), 0, s,
+                   static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.Dv, a.H,
+                   a.Nq, a.d_v, a.st[3][0], a.st[3][1], a.st[3][2], a.st[4][0], a.st[4][1],
+                   a.st[4][2], nullptr, a.Nq);
   return cudaGetLastError();
 }
 
