@@ -256,9 +256,11 @@ int mha_layer_bwd_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, i
  *   dx_q [B,Nq,D]; dx_kv [B,Nk,D] for cross-attention (ignored, may be NULL, for self);
  *   dW_qkv like W_qkv; db_qkv [H*(2*d_k+d_v)]; dW_o like W_o; db_o, dgamma, dbeta [D]
  *   (always written, also when the forward passed NULL for the bias, gamma or beta).
- *   Sums over rows run per chunk of 256 rows and then over the chunks in a fixed order;
- *   the attention backward inside follows mha_set_deterministic (see mha_sdpa_bwd): with 1
- *   every result is bitwise reproducible.  workspace: mha_layer_bwd_workspace_size() bytes, 256-byte
+ *   Sums over rows run per chunk of 256 rows and then over the chunks in a fixed order.  By
+ *   default (bf16) the attention backward inside accumulates dQ in fp32 (see mha_sdpa_bwd)
+ *   and the weight-gradient GEMMs, whose K is the token count, split K over several CTAs
+ *   whose fp32 partials are added in no fixed order when that fills the SMs better; after
+ *   mha_set_deterministic(1) neither happens and every result is bitwise reproducible.  workspace: mha_layer_bwd_workspace_size() bytes, 256-byte
  *   aligned.  Limits and errors as for mha_layer_fwd; MHA_ERR_INVALID for a NULL output.
  * Launches (all on `stream`): the forward's GEMMs, attention and W^O GEMM again, the
  * LayerNorm backward, the attention backward, the data- and weight-gradient GEMMs on the
@@ -396,10 +398,12 @@ int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x
 const char* mha_status_string(int status);
 
 /*
- * mha_set_deterministic -- process-wide switch (0 by default) for the bf16 attention
- * backward, also inside mha_layer_bwd: 1 computes dQ by a separate kernel that rebuilds S and
- * dP per query tile, bitwise reproducible; 0 adds every key tile's dQ part into an fp32
- * accumulator by bulk reductions, faster, reproducible up to the order of fp32 additions.
+ * mha_set_deterministic -- process-wide switch (0 by default) for the bf16 backward: 1
+ * computes the attention's dQ by a separate kernel that rebuilds S and dP per query tile and
+ * runs mha_layer_bwd's weight-gradient GEMMs without splitting K, all bitwise reproducible;
+ * 0 adds every key tile's dQ part into an fp32 accumulator by bulk reductions and lets the
+ * weight-gradient GEMMs add fp32 partials of K slices the same way: faster, reproducible up
+ * to the order of fp32 additions.
  * Returns MHA_ERR_INVALID unless `on` is 0 or 1.  Takes effect for calls issued after it.
  * mha_get_deterministic -- the current setting.
  */

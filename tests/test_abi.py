@@ -334,7 +334,16 @@ def test_layer_backward_validation(lib):
     self_bytes = n.value
     assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 1, 0,
                                             ctypes.byref(n)) == 0
-    assert n.value > self_bytes          # cross-attention keeps separate key/value buffers
+    assert n.value > 0
+    # cross-attention keeps separate key/value buffers (fp32: no split-K scratch, whose size
+    # follows the largest weight gradient and is smaller for cross-attention)
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 0, 1,
+                                            ctypes.byref(n)) == 0
+    self_f32 = n.value
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 0, 0,
+                                            ctypes.byref(n)) == 0
+    assert n.value > self_f32
+    assert self_bytes > 0
     assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 90, 128, 64, 64, 1, 1,
                                             ctypes.byref(n)) == C.MHA_ERR_INVALID
     assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 96, 64, 64, 1, 1,

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -147,6 +148,19 @@ bool map_2d_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows, cols] contiguous, box {32, 32}: the split-K GEMM's accumulator
+bool map_2d_f32_acc(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [B, H, N, 64] bf16 tensor with element strides st = {b, h, n, d=1}; box {64, box_rows, 1, 1}.
 bool map_bhnd_bf16(CUtensorMap* m, const void* base, int B, int H, int N, const int64_t* st,
                    uint32_t box_rows = 128) {
@@ -204,6 +218,45 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
                              static_cast<const float*>(bias), relu, static_cast<float*>(Y), ldy,
                              M, N, K, s, static_cast<const float*>(residual));
   }
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// K slices for a weight-gradient GEMM whose 128 x 128 tiles alone would fill the SMs badly:
+// the smallest split whose work units fill >= 90% of their last round (else the best of
+// 1..8), with at least 8 K blocks of 64 per slice
+int wgrad_ksplit(int M, int N, int K, int num_sms) {
+  const int64_t tiles = static_cast<int64_t>((M + 127) / 128) * ((N + 127) / 128);
+  int best = 1;
+  double best_eff = 0.0;
+  for (int ks = 1; ks <= 8 && (K / 64) / ks >= 8; ++ks) {
+    const int64_t units = tiles * ks;
+    const int64_t rounds = (units + num_sms - 1) / num_sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(rounds * num_sms);
+    if (eff >= 0.9) return ks;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+// dW [M, N] = A [M, K] B [N, K]^T for the weight gradients (K = tokens); bf16 through the
+// split-K GEMM when that fills the GPU better, acc: fp32 scratch of M * N values
+int run_linear_wgrad(int M, int N, int K, int dtype, const void* A, int64_t lda, const void* Bm,
+                     void* Y, int64_t ldy, float* acc, const DevCtx& ctx, cudaStream_t s) {
+  // the split-K partials are added in whatever order the slices finish: not in the
+  // deterministic mode
+  if (dtype != MHA_BF16 || N % 8 != 0 || g_deterministic.load(std::memory_order_relaxed) != 0)
+    return run_linear(M, N, K, dtype, A, lda, Bm, nullptr, Y, ldy, ctx, s);
+  const int ks = wgrad_ksplit(M, N, K, ctx.num_sms);
+  if (ks == 1) return run_linear(M, N, K, dtype, A, lda, Bm, nullptr, Y, ldy, ctx, s);
+  CUtensorMap tmA, tmB, tmAcc;
+  if (!map_2d_bf16(&tmA, A, K, M, lda, 128) || !map_2d_bf16(&tmB, Bm, K, N, K, 128) ||
+      !map_2d_f32_acc(&tmAcc, acc, N, M))
+    return MHA_ERR_CUDA;
+  const cudaError_t e =
+      mha::launch_gemm_bf16_splitk(tmA, tmB, tmAcc, acc, ks, Y, M, N, K, ldy, ctx, s);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
@@ -967,7 +1020,7 @@ struct LayerBwdPlan {
   int Mq, Mk, Mq_pad, Mk_pad, nqk, nv, ld_q, ld_kv;  // ld_q: row pitch of the Q projection
   size_t off_q, off_kv, off_c, off_a, off_lse, off_dvec, off_stats, off_part, off_dr, off_dc,
       off_dq, off_dkv, off_wot, off_wqt, off_wkvt, off_drt, off_ct, off_dqt, off_dkvt, off_xqt,
-      off_xkvt, total;
+      off_xkvt, off_wacc, total;
 };
 
 LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
@@ -1011,6 +1064,10 @@ LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_
   p.off_dkvt = self ? p.off_dqt : take(static_cast<size_t>(p.ld_kv) * p.Mk_pad * es);
   p.off_xqt = take(static_cast<size_t>(D) * p.Mq_pad * es);
   p.off_xkvt = self ? p.off_xqt : take(static_cast<size_t>(D) * p.Mk_pad * es);
+  // fp32 accumulator of the split-K weight-gradient GEMMs (the largest dW)
+  const size_t wmax = static_cast<size_t>(D) *
+                      std::max(std::max(p.ld_q, p.ld_kv), std::max(p.nv, p.nqk + p.nv));
+  p.off_wacc = take(dtype == MHA_BF16 ? wmax * 4 : 0);
   p.total = o;
   return p;
 }
@@ -1112,8 +1169,9 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                    pl.Mq_pad, stream)));
   MHA_TRY(ok(mha::launch_transpose(dtype, W(pl.off_c), nv, Mq, nv, W(pl.off_ct), pl.Mq_pad,
                                    pl.Mq_pad, stream)));
-  MHA_TRY(run_linear(D, nv, pl.Mq_pad, dtype, W(pl.off_drt), pl.Mq_pad, W(pl.off_ct), nullptr,
-                     dW_o, nv, ctx, stream));
+  float* wacc = static_cast<float*>(W(pl.off_wacc));
+  MHA_TRY(run_linear_wgrad(D, nv, pl.Mq_pad, dtype, W(pl.off_drt), pl.Mq_pad, W(pl.off_ct),
+                           dW_o, nv, wacc, ctx, stream));
 
   // ---- attention backward: dQ, dK, dV into buffers laid out like the projections
   mha::SdpaBwdArgs g;
@@ -1145,8 +1203,8 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      pl.Mq_pad, pl.Mq_pad, stream)));
     MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
                                      stream)));
-    MHA_TRY(run_linear(pl.ld_q, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
-                       nullptr, dW_qkv, D, ctx, stream));
+    MHA_TRY(run_linear_wgrad(pl.ld_q, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad,
+                             W(pl.off_xqt), dW_qkv, D, wacc, ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, pl.ld_q, Mq, pl.ld_q, part, stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, pl.ld_q, pl.ld_q, db_qkv,
                                            stream)));
@@ -1162,8 +1220,8 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      pl.Mq_pad, stream)));
     MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
                                      stream)));
-    MHA_TRY(run_linear(nqk, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
-                       nullptr, dWb, D, ctx, stream));
+    MHA_TRY(run_linear_wgrad(nqk, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
+                             dWb, D, wacc, ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, nqk, Mq, nqk, part, stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, nqk, nqk, dbb, stream)));
     // key/value side
@@ -1176,8 +1234,9 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      pl.Mk_pad, pl.Mk_pad, stream)));
     MHA_TRY(ok(mha::launch_transpose(dtype, src_kv, D, Mk, D, W(pl.off_xkvt), pl.Mk_pad,
                                      pl.Mk_pad, stream)));
-    MHA_TRY(run_linear(pl.ld_kv, D, pl.Mk_pad, dtype, W(pl.off_dkvt), pl.Mk_pad, W(pl.off_xkvt),
-                       nullptr, dWb + static_cast<size_t>(nqk) * D * es, D, ctx, stream));
+    MHA_TRY(run_linear_wgrad(pl.ld_kv, D, pl.Mk_pad, dtype, W(pl.off_dkvt), pl.Mk_pad,
+                             W(pl.off_xkvt), dWb + static_cast<size_t>(nqk) * D * es, D, wacc,
+                             ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dkvbuf, pl.ld_kv, Mk, pl.ld_kv, part,
                                            stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_k, pl.ld_kv, pl.ld_kv,

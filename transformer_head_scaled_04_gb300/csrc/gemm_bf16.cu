@@ -18,6 +18,10 @@
 //              bias, ReLU if asked, round to bf16 (nearest even), hand the accumulator back;
 //              each warp writes its 32 rows 64 columns at a time into one of two swizzled
 //              shared-memory staging boxes and issues one bulk tensor store per box.
+// Split-K (kAcc, for the weight-gradient GEMMs whose K is the token count and whose few
+// output tiles would leave SMs idle): the work units are (K slice, tile) pairs, each unit's
+// fp32 partial goes through the same staging boxes as 32 x 32 fp32 boxes and is added into a
+// zeroed fp32 [M, N] buffer by bulk tensor reductions; a separate launch rounds it to bf16.
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -48,14 +52,14 @@ struct GemmShape {
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
-template <int BN, bool kRelu>
+template <int BN, bool kRelu, bool kAcc>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmY,
                           const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ Y,
                           int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns,
-                          const __nv_bfloat16* __restrict__ R) {
+                          const __nv_bfloat16* __restrict__ R, int ksplit) {
   using S = GemmShape<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -72,6 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_kb = K / kBK;
   const int tiles_n = (N + BN - 1) / BN;
   const int tiles = tiles_n * ((M + kBM - 1) / kBM);
+  // work unit u: tile u % tiles, K slice u / tiles (units running together share K slices)
+  const int units = tiles * ksplit;
+  auto kb_begin = [&](int u) { return (u / tiles) * num_kb / ksplit; };
+  auto kb_end = [&](int u) { return (u / tiles + 1) * num_kb / ksplit; };
 
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + S::kStages + s); };
@@ -108,10 +116,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmW);
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      const int tile = u % tiles;
       const int m0 = (tile / tiles_n) * kBM;
       const int n0 = (tile % tiles_n) * BN;
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = kb_begin(u), kb1 = kb_end(u); kb < kb1; ++kb, ++it) {
         const int s = it % S::kStages;
         if (!mbar_wait_backoff(empty_bar(s), ((it / S::kStages) & 1) ^ 1, timeout_ns)) {
           record_error(status, kErrTimeout, kSiteGemmProducer);
@@ -131,15 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
     int it = 0, tcount = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++tcount) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tcount) {
       const int buf = tcount & 1;
       const uint32_t d = tmem + buf * BN;
+      const int kb0 = kb_begin(u);
       if (!mbar_wait(acc_empty(buf), ((tcount >> 1) & 1) ^ 1, timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      for (int kb = kb0, kb1 = kb_end(u); kb < kb1; ++kb, ++it) {
         const int s = it % S::kStages;
         if (!mbar_wait(full_bar(s), (it / S::kStages) & 1, timeout_ns)) {
           ok = false;
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kBK / 16; ++k) {
           const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
           const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
-          mma_bf16_ss(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_bf16_ss(d, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
         }
         mma_commit(empty_bar(s));
       }
@@ -167,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     int tcount = 0;
     int box = 0;  // staging boxes used so far (alternating)
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++tcount) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++tcount) {
+      const int tile = u % tiles;
       const int buf = tcount & 1;
       const int m0 = (tile / tiles_n) * kBM;
       const int n0 = (tile % tiles_n) * BN;
@@ -202,6 +213,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int col = n0 + c * 64;
         if (wrow0 >= M || col >= N) continue;  // nothing of this box is inside Y
+        if constexpr (kAcc) {
+          // two 32 x 32 fp32 boxes (128-byte rows, swizzled) added into the fp32 buffer
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh, ++box) {
+            const uint32_t sb = sOut + (quarter * 2 + (box & 1)) * S::kOutBoxBytes;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(sb + lane * 128 + ((q ^ (lane & 7)) << 4),
+                           make_uint4(r[hh * 32 + q * 4], r[hh * 32 + q * 4 + 1],
+                                      r[hh * 32 + q * 4 + 2], r[hh * 32 + q * 4 + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tmY, sb, col + hh * 32, wrow0);
+              bulk_commit_group();
+            }
+          }
+          --box;  // the loop header counts one box per chunk
+          continue;
+        }
         float bv[64];
         if (bias != nullptr) {
           const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
@@ -262,7 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_group_read<0>();  // staging stays until every store has read it
+    // staging stays until every store has read it; reductions have also landed
+    if (lane == 0) {
+      if (kAcc)
+        bulk_wait_group0();
+      else
+        bulk_wait_group_read<0>();
+    }
   }
 
   tc_fence_before();
@@ -273,20 +312,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool kRelu>
+template <int BN, bool kRelu, bool kAcc>
 cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
                       const void* bias, void* Y,
                       int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
-                      const void* R) {
+                      const void* R, int ksplit) {
   using S = GemmShape<BN>;
-  auto kern = gemm_bias_bf16_kernel<BN, kRelu>;
+  auto kern = gemm_bias_bf16_kernel<BN, kRelu, kAcc>;
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), S::kSmemBytes, nullptr);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM);
-  const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  const int64_t units =
+      static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM) * ksplit;
+  const int grid = static_cast<int>(units < ctx.num_sms ? units : ctx.num_sms);
   return launch_pdl(kern, dim3(grid), dim3(kThreads), S::kSmemBytes, s, tmX, tmW, tmY,
                     static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(Y), M,
-                    N, K, ldy, ctx.status, ctx.timeout_ns, static_cast<const __nv_bfloat16*>(R));
+                    N, K, ldy, ctx.status, ctx.timeout_ns, static_cast<const __nv_bfloat16*>(R),
+                    ksplit);
+}
+
+// acc [M, N] fp32 -> Y bf16 (row pitch ldy), 8 values per thread
+__global__ void __launch_bounds__(256)
+    acc_to_bf16_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ Y, int M,
+                       int N, int64_t ldy) {
+  pdl_launch_dependents();
+  pdl_wait();  // the split-K GEMM's reductions are complete from here on
+  const int64_t per_row = N / 8;
+  const int64_t total = static_cast<int64_t>(M) * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / per_row;
+    const int col = static_cast<int>(i % per_row) * 8;
+    const float4* src = reinterpret_cast<const float4*>(acc + row * N + col);
+    const float4 x = __ldcs(src), y = __ldcs(src + 1);
+    uint4 v;
+    v.x = pack_bf16x2(x.x, x.y);
+    v.y = pack_bf16x2(x.z, x.w);
+    v.z = pack_bf16x2(y.x, y.y);
+    v.w = pack_bf16x2(y.z, y.w);
+    *reinterpret_cast<uint4*>(Y + row * ldy + col) = v;
+  }
 }
 
 }  // namespace
@@ -296,11 +360,30 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s, const void* R) {
   if (relu) {
-    if (block_n == 256) return launch_bn<256, true>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
-    return launch_bn<128, true>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
+    if (block_n == 256)
+      return launch_bn<256, true, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
+    return launch_bn<128, true, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
   }
-  if (block_n == 256) return launch_bn<256, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
-  return launch_bn<128, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R);
+  if (block_n == 256)
+    return launch_bn<256, false, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
+  return launch_bn<128, false, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
+}
+
+cudaError_t launch_gemm_bf16_splitk(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                    const CUtensorMap& tmAcc, float* acc, int ksplit, void* Y,
+                                    int M, int N, int K, int64_t ldy, const DevCtx& ctx,
+                                    cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, s);
+  if (e != cudaSuccess) return e;
+  e = launch_bn<128, false, true>(tmX, tmW, tmAcc, nullptr, nullptr, M, N, K, N, ctx, s, nullptr,
+                                  ksplit);
+  if (e != cudaSuccess) return e;
+  const int64_t total = static_cast<int64_t>(M) * (N / 8);
+  const int64_t want = (total + 255) / 256;
+  const int blocks =
+      static_cast<int>(want < static_cast<int64_t>(ctx.num_sms) * 8 ? want : ctx.num_sms * 8);
+  return launch_pdl(acc_to_bf16_kernel, dim3(blocks), dim3(256), 0, s,
+                    static_cast<const float*>(acc), static_cast<__nv_bfloat16*>(Y), M, N, ldy);
 }
 
 }  // namespace mha

@@ -50,6 +50,14 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                              const void* residual = nullptr);
+// Split-K form for weight gradients (no bias, no activation): acc [M, N] fp32 scratch is
+// zeroed, each of ksplit K slices of every 128 x 128 tile is added into it by bulk tensor
+// reductions through tmAcc (fp32 {N, M}, box {32, 32}, 128-byte swizzle), then Y = bf16(acc).
+// K / 64 must be at least ksplit.
+cudaError_t launch_gemm_bf16_splitk(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                    const CUtensorMap& tmAcc, float* acc, int ksplit, void* Y,
+                                    int M, int N, int K, int64_t ldy, const DevCtx& ctx,
+                                    cudaStream_t s);
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
                             bool relu, float* Y, int64_t ldy, int M, int N, int K,
                             cudaStream_t s, const float* residual = nullptr);
