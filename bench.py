@@ -414,7 +414,7 @@ def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
                   "tokens_per_s": w.B * w.Nq / (layer_ms * 1e-3),
                   "flops_model": "forward recomputed + data and weight gradients of the four "
                                  "projections + the attention backward"},
-        "gpu_launches_per_step": {"attention": 3, "layer": 26},
+        "gpu_launches_per_step": {"attention": 3, "layer": 25},
     }
 
 
