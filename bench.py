@@ -399,6 +399,20 @@ def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
         vp(t["beta"]), vp(dy), vp(out["dx_q"]), None, vp(out["dW_qkv"]), vp(out["db_qkv"]),
         vp(out["dW_o"]), vp(out["db_o"]), vp(out["dgamma"]), vp(out["dbeta"]), vp(ws),
         ws.numel(), sp), "mha_layer_bwd")
+    # a training step: the forward that keeps its activations, then the backward from them
+    y_tr = torch.empty_like(t["x_q"])
+    lay = (w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16, 0, None, 1e-5, vp(t["x_q"]),
+           None, vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]), vp(t["b_o"]), vp(t["gamma"]),
+           vp(t["beta"]))
+    grads = (vp(out["dx_q"]), None, vp(out["dW_qkv"]), vp(out["db_qkv"]), vp(out["dW_o"]),
+             vp(out["db_o"]), vp(out["dgamma"]), vp(out["dbeta"]))
+
+    def train_step():
+        st = lib.mha_layer_fwd_train(*lay, vp(y_tr), vp(ws), ws.numel(), sp)
+        return st if st != 0 else lib.mha_layer_bwd_saved(*lay, vp(dy), *grads, vp(ws),
+                                                          ws.numel(), sp)
+
+    train_ms = timed(train_step, "mha_layer_fwd_train + mha_layer_bwd_saved")
     fwd = layer_flops(w, "none")
     gemm = fwd - sdpa_flops(w, "none")
     layer_fl = fwd + 2.0 * gemm + attn_fl
@@ -414,7 +428,13 @@ def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
                   "tokens_per_s": w.B * w.Nq / (layer_ms * 1e-3),
                   "flops_model": "forward recomputed + data and weight gradients of the four "
                                  "projections + the attention backward"},
-        "gpu_launches_per_step": {"attention": 3, "layer": 25},
+        "training_step": {"value": layer_fl / (train_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "ms_per_step": train_ms, "flops_per_step": layer_fl,
+                          "tokens_per_s": w.B * w.Nq / (train_ms * 1e-3),
+                          "what": "mha_layer_fwd_train (y, activations kept) then "
+                                  "mha_layer_bwd_saved: the same FLOPs as the recomputing "
+                                  "backward, plus y"},
+        "gpu_launches_per_step": {"attention": 3, "layer": 25, "training_step": 26},
     }
 
 

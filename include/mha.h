@@ -274,6 +274,32 @@ int mha_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
                   void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * mha_layer_fwd_train / mha_layer_bwd_saved -- the same sublayer forward and backward split
+ * the way a training step runs them ([JY] Transformer 训练样例: a forward pass, then the
+ * backward pass), so the backward does not compute the forward a second time.
+ *   mha_layer_fwd_train: arguments as for mha_layer_fwd, but `workspace` must hold
+ *   mha_layer_bwd_workspace_size() bytes (256-byte aligned).  Writes y (the same values as
+ *   mha_layer_fwd) and leaves in the workspace what the backward reads: the projections, the
+ *   head concat C, the W^O output and the attention's log-sum-exp.
+ *   mha_layer_bwd_saved: arguments as for mha_layer_bwd; the workspace must be the one a
+ *   preceding mha_layer_fwd_train filled with the same inputs, parameters, mask and key_len
+ *   (on the same stream, or ordered after it), untouched since.  The gradients equal those of
+ *   mha_layer_bwd (bitwise in the deterministic mode).  Errors as for those two calls.
+ */
+int mha_layer_fwd_train(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps, const void* x_q,
+                        const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                        const void* b_o, const void* gamma, const void* beta, void* y,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+int mha_layer_bwd_saved(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps, const void* x_q,
+                        const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                        const void* b_o, const void* gamma, const void* beta, const void* dy,
+                        void* dx_q, void* dx_kv, void* dW_qkv, void* db_qkv, void* dW_o,
+                        void* db_o, void* dgamma, void* dbeta, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/*
  * mha_layer_fwd_noalloc -- mha_layer_fwd for callers that cannot supply a workspace.
  * The pages have no counterpart: this is a packaging variant, not part of the method.
  *

@@ -374,3 +374,35 @@ def test_layer_backward_validation(lib):
     assert bwd(ws_bytes=self_bytes - 1) == C.MHA_ERR_WORKSPACE
     assert bwd(dx_q=ODD) == C.MHA_ERR_ALIGN
     assert bwd(ws=ctypes.c_void_p(0x10010)) == C.MHA_ERR_ALIGN
+
+
+def test_layer_training_split_validation(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.mha_layer_bwd_workspace_size(2, 2, 100, 100, 128, 64, 64, 1, 1,
+                                            ctypes.byref(n)) == 0
+    need = n.value
+
+    def fwd(**kw):
+        a = dict(y=FAKE, ws=FAKE, ws_bytes=need, x_q=FAKE, D=128)
+        a.update(kw)
+        return lib.mha_layer_fwd_train(2, 2, 100, 100, a["D"], 64, 64, 1, 0, None, 1e-5,
+                                       a["x_q"], None, FAKE, None, FAKE, None, None, None,
+                                       a["y"], a["ws"], a["ws_bytes"], None)
+
+    def bwd(**kw):
+        a = dict(dy=FAKE, ws=FAKE, ws_bytes=need)
+        a.update(kw)
+        return lib.mha_layer_bwd_saved(2, 2, 100, 100, 128, 64, 64, 1, 0, None, 1e-5, FAKE,
+                                       None, FAKE, None, FAKE, None, None, None, a["dy"], FAKE,
+                                       None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["ws"],
+                                       a["ws_bytes"], None)
+
+    assert fwd(y=None) == C.MHA_ERR_INVALID
+    assert fwd(x_q=None) == C.MHA_ERR_INVALID
+    assert fwd(D=96) == C.MHA_ERR_UNSUPPORTED
+    assert fwd(ws_bytes=need - 1) == C.MHA_ERR_WORKSPACE   # the backward's workspace size
+    assert fwd(ws=None) == C.MHA_ERR_WORKSPACE
+    assert fwd(y=ODD) == C.MHA_ERR_ALIGN
+    assert bwd(dy=None) == C.MHA_ERR_INVALID
+    assert bwd(ws_bytes=need - 1) == C.MHA_ERR_WORKSPACE
+    assert bwd(dy=ODD) == C.MHA_ERR_ALIGN

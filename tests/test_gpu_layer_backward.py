@@ -165,3 +165,41 @@ def test_layer_backward_big_long_sampled_batches(mask):
         total = ref if total is None else {k: total[k] + ref[k] for k in PARAMS}
     for k in PARAMS:
         assert_bf16_param_grad_close(got[k], total[k], f"big {mask} {k}")
+
+
+@pytest.mark.parametrize("name", ["enc_self_base_b32_n128", "cross_pad_base_b32_q128_k256"])
+def test_layer_training_split_matches(name):
+    """mha_layer_fwd_train writes the forward's y bitwise, and mha_layer_bwd_saved from the
+    activations it left gives the gradients of mha_layer_bwd bitwise (deterministic mode);
+    in the default mode the saved backward still meets the oracle's bound."""
+    w = si.WORKLOADS[name]
+    inp = si.draw_layer(w, affine=True)
+    dy = draw_dy(w, 86, "bf16")
+    bf = torch.bfloat16
+    t = {k: to_dev(v, bf) for k, v in inp.items() if k != "key_len"}
+    kl = to_dev(inp["key_len"], torch.int32)
+    args = (t["x_q"], t["x_kv"], t["W_qkv"], t["b_qkv"], t["W_o"], t["b_o"], t["gamma"],
+            t["beta"], w.H)
+    kw = dict(mask=w.mask, key_len=kl, d_k=w.d_k, d_v=w.d_v)
+    tdy = to_dev(dy, bf)
+    y_ref = mha.mha_layer(*args, **kw)
+    before = mha.get_deterministic()
+    mha.set_deterministic(True)
+    try:
+        y, ws = mha.mha_layer_forward_train(*args, **kw)
+        assert torch.equal(y, y_ref)
+        full = mha.mha_layer_backward(*args, tdy, **kw)
+        saved = mha.mha_layer_backward(*args, tdy, workspace=ws, saved=True, **kw)
+        for k in PER_TOKEN + PARAMS:
+            if full[k] is None:
+                assert saved[k] is None
+            else:
+                assert torch.equal(full[k], saved[k]), k
+        mha.set_deterministic(False)
+        y2, ws2 = mha.mha_layer_forward_train(*args, **kw)
+        assert torch.equal(y2, y_ref)
+        fast = mha.mha_layer_backward(*args, tdy, workspace=ws2, saved=True, **kw)
+    finally:
+        mha.set_deterministic(before)
+    compare_bf16({k: host(v) for k, v in fast.items()}, run_oracle(inp, dy, w),
+                 f"training split {name}")

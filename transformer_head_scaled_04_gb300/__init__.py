@@ -24,6 +24,7 @@ from .api import (  # noqa: F401
     linear,
     mha_layer,
     mha_layer_backward,
+    mha_layer_forward_train,
     residual_layernorm,
     sdpa,
     sdpa_backward,

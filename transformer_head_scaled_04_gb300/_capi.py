@@ -34,6 +34,8 @@ PROTOTYPES = {
     "mha_layer_fwd": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10 + [_size, _vp]),
     "mha_layer_bwd_workspace_size": (_c_int, [_c_int] * 9 + [ctypes.POINTER(_size)]),
     "mha_layer_bwd": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 18 + [_size, _vp]),
+    "mha_layer_fwd_train": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10 + [_size, _vp]),
+    "mha_layer_bwd_saved": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 18 + [_size, _vp]),
     "mha_layer_fwd_timed": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 10
                             + [_size, _vp, _vp, _c_int]),
     "mha_layer_fwd_noalloc": (_c_int, [_c_int] * 9 + [_vp, _c_float] + [_vp] * 9 + [_vp]),

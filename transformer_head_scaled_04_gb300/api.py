@@ -205,12 +205,41 @@ def layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype, self_attention) -
     return n.value
 
 
+def mha_layer_forward_train(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, mask="none",
+                            key_len=None, eps=1e-5, d_k=None, d_v=None, workspace=None,
+                            out=None):
+    """The training forward (``mha_layer_fwd_train``): y as ``mha_layer`` computes it, with the
+    activations the backward needs left in ``workspace`` (``layer_bwd_workspace_size`` bytes,
+    allocated here if None).  Returns (y, workspace); pass both on to ``mha_layer_backward(...,
+    workspace=workspace, saved=True)``."""
+    _cuda(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, key_len, workspace, out)
+    _contiguous("mha_layer_forward_train", x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta)
+    B, Nq, D = x_q.shape
+    Nk = Nq if x_kv is None else x_kv.shape[1]
+    d_k = D // H if d_k is None else d_k
+    d_v = D // H if d_v is None else d_v
+    ws = layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, x_q.dtype, x_kv is None)
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=x_q.device)
+    if out is None:
+        out = torch.empty_like(x_q)
+    with torch.cuda.device(x_q.device):
+        code = C.load().mha_layer_fwd_train(
+            B, H, Nq, Nk, D, d_k, d_v, _dt(x_q), _mask(mask), _ptr(key_len), float(eps),
+            _ptr(x_q), _ptr(x_kv), _ptr(W_qkv), _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma),
+            _ptr(beta), _ptr(out), _ptr(workspace), workspace.numel(), _stream(x_q.device))
+    C.check(code, "mha_layer_fwd_train")
+    return out, workspace
+
+
 def mha_layer_backward(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, dy, mask="none",
-                       key_len=None, eps=1e-5, d_k=None, d_v=None, workspace=None):
+                       key_len=None, eps=1e-5, d_k=None, d_v=None, workspace=None, saved=False):
     """Gradients of ``mha_layer`` with respect to every input and parameter, given dy = dL/dy,
-    via ``mha_layer_bwd``.  Returns a dict with dx_q, dx_kv (None for self-attention), dW_qkv,
-    db_qkv, dW_o, db_o, dgamma, dbeta -- each shaped like its tensor (the bias, gamma and beta
-    gradients are [D] / [H*(2d_k+d_v)] even where the forward passed None).
+    via ``mha_layer_bwd`` (``mha_layer_bwd_saved`` when ``saved``: the workspace then comes
+    from ``mha_layer_forward_train`` with the same arguments, and the forward is not computed
+    again).  Returns a dict with dx_q, dx_kv (None for self-attention), dW_qkv, db_qkv, dW_o,
+    db_o, dgamma, dbeta -- each shaped like its tensor (the bias, gamma and beta gradients are
+    [D] / [H*(2d_k+d_v)] even where the forward passed None).
     """
     _cuda(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, dy, key_len, workspace)
     _contiguous("mha_layer_backward", x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, dy)
@@ -221,6 +250,8 @@ def mha_layer_backward(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, dy, ma
     if tuple(dy.shape) != (B, Nq, D):
         raise ValueError(f"dy must be [{B},{Nq},{D}]")
     ws = layer_bwd_workspace_size(B, H, Nq, Nk, D, d_k, d_v, x_q.dtype, x_kv is None)
+    if saved and workspace is None:
+        raise ValueError("saved=True needs the workspace mha_layer_forward_train filled")
     if workspace is None:
         workspace = torch.empty(ws, dtype=torch.uint8, device=x_q.device)
     e = lambda *shape: torch.empty(shape, dtype=x_q.dtype, device=x_q.device)  # noqa: E731
@@ -228,14 +259,15 @@ def mha_layer_backward(x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, dy, ma
          "dx_kv": None if x_kv is None else torch.empty_like(x_kv),
          "dW_qkv": torch.empty_like(W_qkv), "db_qkv": e(W_qkv.shape[0]),
          "dW_o": torch.empty_like(W_o), "db_o": e(D), "dgamma": e(D), "dbeta": e(D)}
+    fn = C.load().mha_layer_bwd_saved if saved else C.load().mha_layer_bwd
     with torch.cuda.device(x_q.device):
-        code = C.load().mha_layer_bwd(
+        code = fn(
             B, H, Nq, Nk, D, d_k, d_v, _dt(x_q), _mask(mask), _ptr(key_len), float(eps),
             _ptr(x_q), _ptr(x_kv), _ptr(W_qkv), _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma),
             _ptr(beta), _ptr(dy), _ptr(g["dx_q"]), _ptr(g["dx_kv"]), _ptr(g["dW_qkv"]),
             _ptr(g["db_qkv"]), _ptr(g["dW_o"]), _ptr(g["db_o"]), _ptr(g["dgamma"]),
             _ptr(g["dbeta"]), _ptr(workspace), workspace.numel(), _stream(x_q.device))
-    C.check(code, "mha_layer_bwd")
+    C.check(code, "mha_layer_bwd_saved" if saved else "mha_layer_bwd")
     return g
 
 

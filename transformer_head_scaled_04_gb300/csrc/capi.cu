@@ -1072,27 +1072,38 @@ LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_
   return p;
 }
 
+// phase: kLayerBwdFull (forward recomputed, then the backward), kLayerFwdTrain (the forward
+// alone, y written and the activations the backward needs left in the workspace),
+// kLayerBwdSaved (the backward from those saved activations)
+enum { kLayerBwdFull = 0, kLayerFwdTrain = 1, kLayerBwdSaved = 2 };
+
 int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
                    const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
                    const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
                    const void* gamma, const void* dy, void* dx_q, void* dx_kv, void* dW_qkv,
                    void* db_qkv, void* dW_o, void* db_o, void* dgamma, void* dbeta,
-                   void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                   void* workspace, size_t ws_bytes, cudaStream_t stream,
+                   int phase = kLayerBwdFull, const void* beta = nullptr, void* y = nullptr) {
   int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
   if (st != MHA_OK) return st;
   if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
   const bool self = (x_kv == nullptr);
   if ((self || mask == MHA_MASK_CAUSAL) && Nq != Nk) return MHA_ERR_INVALID;
   if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
-  const void* need[] = {x_q, W_qkv, W_o, dy, dx_q, dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta};
-  for (const void* q : need)
-    if (q == nullptr) return MHA_ERR_INVALID;
-  if (!self && dx_kv == nullptr) return MHA_ERR_INVALID;
+  if (phase == kLayerFwdTrain) {
+    if (x_q == nullptr || W_qkv == nullptr || W_o == nullptr || y == nullptr)
+      return MHA_ERR_INVALID;
+  } else {
+    const void* need[] = {x_q, W_qkv, W_o, dy, dx_q, dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta};
+    for (const void* q : need)
+      if (q == nullptr) return MHA_ERR_INVALID;
+    if (!self && dx_kv == nullptr) return MHA_ERR_INVALID;
+  }
   if (std::isnan(ln_eps) || ln_eps < 0.f) return MHA_ERR_INVALID;
   const LayerBwdPlan pl = plan_layer_bwd(B, H, Nq, Nk, D, d_k, d_v, dtype, self);
   if (workspace == nullptr || ws_bytes < pl.total) return MHA_ERR_WORKSPACE;
-  const void* all[] = {x_q,  x_kv,  W_qkv, b_qkv, W_o,    b_o,  gamma,  dy,   dx_q,
-                       dx_kv, dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta, workspace};
+  const void* all[] = {x_q,  x_kv,  W_qkv, b_qkv, W_o,    b_o,  gamma,  dy,   dx_q, dx_kv,
+                       dW_qkv, db_qkv, dW_o, db_o, dgamma, dbeta, workspace, beta, y};
   for (const void* q : all)
     if (q != nullptr && !aligned(q, 16)) return MHA_ERR_ALIGN;
   if (key_len != nullptr && !aligned(key_len, 4)) return MHA_ERR_ALIGN;
@@ -1123,15 +1134,21 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
   uint8_t* qbuf = ws + pl.off_q;
   uint8_t* kvbuf = ws + pl.off_kv;
+  const bool recompute = phase != kLayerBwdSaved;
   if (self) {
-    MHA_TRY(run_linear(Mq, pl.ld_q, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, pl.ld_q, ctx, stream));
+    if (recompute)
+      MHA_TRY(run_linear(Mq, pl.ld_q, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, pl.ld_q, ctx,
+                         stream));
     a.Q = qbuf;
     a.K = qbuf + nqk * es;
     a.V = qbuf + 2 * nqk * es;
   } else {
-    MHA_TRY(run_linear(Mq, nqk, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, nqk, ctx, stream));
-    MHA_TRY(run_linear(Mk, pl.ld_kv, D, dtype, x_kv, D, Wb + static_cast<size_t>(nqk) * D * es,
-                       bq ? bq + nqk * es : nullptr, kvbuf, pl.ld_kv, ctx, stream));
+    if (recompute) {
+      MHA_TRY(run_linear(Mq, nqk, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, nqk, ctx, stream));
+      MHA_TRY(run_linear(Mk, pl.ld_kv, D, dtype, x_kv, D,
+                         Wb + static_cast<size_t>(nqk) * D * es, bq ? bq + nqk * es : nullptr,
+                         kvbuf, pl.ld_kv, ctx, stream));
+    }
     a.Q = qbuf;
     a.K = kvbuf;
     a.V = kvbuf + nqk * es;
@@ -1148,8 +1165,14 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
   }
   a.O = W(pl.off_c);
   a.lse = static_cast<float*>(W(pl.off_lse));
-  MHA_TRY(run_sdpa(a, dtype, ctx, stream));
-  MHA_TRY(run_linear(Mq, D, nv, dtype, W(pl.off_c), nv, W_o, b_o, W(pl.off_a), D, ctx, stream));
+  if (phase != kLayerBwdSaved) {
+    MHA_TRY(run_sdpa(a, dtype, ctx, stream));
+    MHA_TRY(run_linear(Mq, D, nv, dtype, W(pl.off_c), nv, W_o, b_o, W(pl.off_a), D, ctx,
+                       stream));
+  }
+  if (phase == kLayerFwdTrain)
+    return ok(mha::launch_residual_layernorm(dtype, Mq, D, ln_eps, x_q, W(pl.off_a), gamma, beta,
+                                             y, ctx, stream));
 
   // ---- residual + LayerNorm backward: dr; dgamma, dbeta, db_o from per-chunk partials
   float* part = static_cast<float*>(W(pl.off_part));
@@ -1270,6 +1293,30 @@ int mha_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
   return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
                         W_qkv, b_qkv, W_o, b_o, gamma, dy, dx_q, dx_kv, dW_qkv, db_qkv, dW_o,
                         db_o, dgamma, dbeta, workspace, ws_bytes, stream);
+}
+
+int mha_layer_fwd_train(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps, const void* x_q,
+                        const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                        const void* b_o, const void* gamma, const void* beta, void* y,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
+                        W_qkv, b_qkv, W_o, b_o, gamma, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
+                        kLayerFwdTrain, beta, y);
+}
+
+int mha_layer_bwd_saved(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
+                        int mask, const int32_t* key_len, float ln_eps, const void* x_q,
+                        const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
+                        const void* b_o, const void* gamma, const void* beta, const void* dy,
+                        void* dx_q, void* dx_kv, void* dW_qkv, void* db_qkv, void* dW_o,
+                        void* db_o, void* dgamma, void* dbeta, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream) {
+  (void)beta;
+  return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
+                        W_qkv, b_qkv, W_o, b_o, gamma, dy, dx_q, dx_kv, dW_qkv, db_qkv, dW_o,
+                        db_o, dgamma, dbeta, workspace, ws_bytes, stream, kLayerBwdSaved);
 }
 
 }  // extern "C"
