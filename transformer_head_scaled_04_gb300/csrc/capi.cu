@@ -241,22 +241,34 @@ int wgrad_ksplit(int M, int N, int K, int num_sms) {
   return best;
 }
 
-// dW [M, N] = A [M, K] B [N, K]^T for the weight gradients (K = tokens); bf16 through the
-// split-K GEMM when that fills the GPU better, acc: fp32 scratch of M * N values
-int run_linear_wgrad(int M, int N, int K, int dtype, const void* A, int64_t lda, const void* Bm,
-                     void* Y, int64_t ldy, float* acc, const DevCtx& ctx, cudaStream_t s) {
-  // the split-K partials are added in whatever order the slices finish: not in the
-  // deterministic mode
-  if (dtype != MHA_BF16 || N % 8 != 0 || g_deterministic.load(std::memory_order_relaxed) != 0)
-    return run_linear(M, N, K, dtype, A, lda, Bm, nullptr, Y, ldy, ctx, s);
-  const int ks = wgrad_ksplit(M, N, K, ctx.num_sms);
-  if (ks == 1) return run_linear(M, N, K, dtype, A, lda, Bm, nullptr, Y, ldy, ctx, s);
-  CUtensorMap tmA, tmB, tmAcc;
-  if (!map_2d_bf16(&tmA, A, K, M, lda, 128) || !map_2d_bf16(&tmB, Bm, K, N, K, 128) ||
-      !map_2d_f32_acc(&tmAcc, acc, N, M))
+// dW [M, N] = A^T B for the weight gradients, from the row-major activations A_st [K, M]
+// (row pitch lda) and B_st [K, N] (row pitch ldb), K = tokens.  bf16: both read MN-major by
+// the tensor-core GEMM, split over K when that fills the GPU better (fp32 scratch acc of M * N
+// values; not in the deterministic mode).  fp32: transposed into At [M, Kpad] and Bt [N, Kpad]
+// (zero-padded to Kpad, a multiple of 64) for the SIMT GEMM.
+int run_linear_wgrad(int M, int N, int K, int dtype, const void* A_st, int64_t lda,
+                     const void* B_st, int64_t ldb, void* Y, int64_t ldy, float* acc, void* At,
+                     void* Bt, int Kpad, const DevCtx& ctx, cudaStream_t s) {
+  if (dtype != MHA_BF16) {
+    if (mha::launch_transpose(dtype, A_st, lda, K, M, At, Kpad, Kpad, s) != cudaSuccess ||
+        mha::launch_transpose(dtype, B_st, ldb, K, N, Bt, Kpad, Kpad, s) != cudaSuccess)
+      return MHA_ERR_CUDA;
+    return run_linear(M, N, Kpad, dtype, At, Kpad, Bt, nullptr, Y, ldy, ctx, s);
+  }
+  CUtensorMap tmA, tmB, tmY;
+  if (!map_2d_bf16(&tmA, A_st, M, K, lda, 64) || !map_2d_bf16(&tmB, B_st, N, K, ldb, 64))
     return MHA_ERR_CUDA;
-  const cudaError_t e =
-      mha::launch_gemm_bf16_splitk(tmA, tmB, tmAcc, acc, ks, Y, M, N, K, ldy, ctx, s);
+  const int ks = g_deterministic.load(std::memory_order_relaxed) != 0
+                     ? 1
+                     : wgrad_ksplit(M, N, (K + 63) / 64 * 64, ctx.num_sms);
+  cudaError_t e;
+  if (ks > 1 && N % 8 == 0) {
+    if (!map_2d_f32_acc(&tmY, acc, N, M)) return MHA_ERR_CUDA;
+    e = mha::launch_gemm_bf16_splitk(tmA, tmB, tmY, acc, ks, Y, M, N, K, ldy, ctx, s);
+  } else {
+    if (!map_2d_bf16(&tmY, Y, N, M, ldy, 32)) return MHA_ERR_CUDA;
+    e = mha::launch_gemm_bf16_mn(tmA, tmB, tmY, Y, M, N, K, ldy, ctx, s);
+  }
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
@@ -1058,12 +1070,14 @@ LayerBwdPlan plan_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_
   p.off_wot = take(static_cast<size_t>(p.nv) * D * es);
   p.off_wqt = take(static_cast<size_t>(D) * p.ld_q * es);
   p.off_wkvt = self ? p.off_wqt : take(static_cast<size_t>(D) * p.ld_kv * es);
-  p.off_drt = take(static_cast<size_t>(D) * p.Mq_pad * es);
-  p.off_ct = take(static_cast<size_t>(p.nv) * p.Mq_pad * es);
-  p.off_dqt = take(static_cast<size_t>(p.ld_q) * p.Mq_pad * es);
-  p.off_dkvt = self ? p.off_dqt : take(static_cast<size_t>(p.ld_kv) * p.Mk_pad * es);
-  p.off_xqt = take(static_cast<size_t>(D) * p.Mq_pad * es);
-  p.off_xkvt = self ? p.off_xqt : take(static_cast<size_t>(D) * p.Mk_pad * es);
+  // transposed activations for the fp32 weight gradients (bf16 reads them MN-major in place)
+  const size_t tes = dtype == MHA_BF16 ? 0 : es;
+  p.off_drt = take(static_cast<size_t>(D) * p.Mq_pad * tes);
+  p.off_ct = take(static_cast<size_t>(p.nv) * p.Mq_pad * tes);
+  p.off_dqt = take(static_cast<size_t>(p.ld_q) * p.Mq_pad * tes);
+  p.off_dkvt = self ? p.off_dqt : take(static_cast<size_t>(p.ld_kv) * p.Mk_pad * tes);
+  p.off_xqt = take(static_cast<size_t>(D) * p.Mq_pad * tes);
+  p.off_xkvt = self ? p.off_xqt : take(static_cast<size_t>(D) * p.Mk_pad * tes);
   // fp32 accumulator of the split-K weight-gradient GEMMs (the largest dW)
   const size_t wmax = static_cast<size_t>(D) *
                       std::max(std::max(p.ld_q, p.ld_kv), std::max(p.nv, p.nqk + p.nv));
@@ -1188,13 +1202,9 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
   MHA_TRY(ok(mha::launch_transpose(dtype, W_o, nv, D, nv, W(pl.off_wot), D, D, stream)));
   MHA_TRY(run_linear(Mq, nv, D, dtype, W(pl.off_dr), D, W(pl.off_wot), nullptr, W(pl.off_dc),
                      nv, ctx, stream));
-  MHA_TRY(ok(mha::launch_transpose(dtype, W(pl.off_dr), D, Mq, D, W(pl.off_drt), pl.Mq_pad,
-                                   pl.Mq_pad, stream)));
-  MHA_TRY(ok(mha::launch_transpose(dtype, W(pl.off_c), nv, Mq, nv, W(pl.off_ct), pl.Mq_pad,
-                                   pl.Mq_pad, stream)));
   float* wacc = static_cast<float*>(W(pl.off_wacc));
-  MHA_TRY(run_linear_wgrad(D, nv, pl.Mq_pad, dtype, W(pl.off_drt), pl.Mq_pad, W(pl.off_ct),
-                           dW_o, nv, wacc, ctx, stream));
+  MHA_TRY(run_linear_wgrad(D, nv, Mq, dtype, W(pl.off_dr), D, W(pl.off_c), nv, dW_o, nv, wacc,
+                           W(pl.off_drt), W(pl.off_ct), pl.Mq_pad, ctx, stream));
 
   // ---- attention backward: dQ, dK, dV into buffers laid out like the projections
   mha::SdpaBwdArgs g;
@@ -1222,12 +1232,8 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      pl.ld_q, stream)));
     MHA_TRY(run_linear(Mq, D, pl.ld_q, dtype, dqbuf, pl.ld_q, W(pl.off_wqt), nullptr, dx_q, D,
                        ctx, stream, false, W(pl.off_dr)));
-    MHA_TRY(ok(mha::launch_transpose(dtype, dqbuf, pl.ld_q, Mq, pl.ld_q, W(pl.off_dqt),
-                                     pl.Mq_pad, pl.Mq_pad, stream)));
-    MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
-                                     stream)));
-    MHA_TRY(run_linear_wgrad(pl.ld_q, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad,
-                             W(pl.off_xqt), dW_qkv, D, wacc, ctx, stream));
+    MHA_TRY(run_linear_wgrad(pl.ld_q, D, Mq, dtype, dqbuf, pl.ld_q, x_q, D, dW_qkv, D, wacc,
+                             W(pl.off_dqt), W(pl.off_xqt), pl.Mq_pad, ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, pl.ld_q, Mq, pl.ld_q, part, stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, pl.ld_q, pl.ld_q, db_qkv,
                                            stream)));
@@ -1239,12 +1245,8 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      stream)));
     MHA_TRY(run_linear(Mq, D, nqk, dtype, dqbuf, nqk, W(pl.off_wqt), nullptr, dx_q, D, ctx,
                        stream, false, W(pl.off_dr)));
-    MHA_TRY(ok(mha::launch_transpose(dtype, dqbuf, nqk, Mq, nqk, W(pl.off_dqt), pl.Mq_pad,
-                                     pl.Mq_pad, stream)));
-    MHA_TRY(ok(mha::launch_transpose(dtype, x_q, D, Mq, D, W(pl.off_xqt), pl.Mq_pad, pl.Mq_pad,
-                                     stream)));
-    MHA_TRY(run_linear_wgrad(nqk, D, pl.Mq_pad, dtype, W(pl.off_dqt), pl.Mq_pad, W(pl.off_xqt),
-                             dWb, D, wacc, ctx, stream));
+    MHA_TRY(run_linear_wgrad(nqk, D, Mq, dtype, dqbuf, nqk, x_q, D, dWb, D, wacc,
+                             W(pl.off_dqt), W(pl.off_xqt), pl.Mq_pad, ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dqbuf, nqk, Mq, nqk, part, stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, nqk, nqk, dbb, stream)));
     // key/value side
@@ -1253,13 +1255,9 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                      pl.ld_kv, D, W(pl.off_wkvt), pl.ld_kv, pl.ld_kv, stream)));
     MHA_TRY(run_linear(Mk, D, pl.ld_kv, dtype, dkvbuf, pl.ld_kv, W(pl.off_wkvt), nullptr, dx_kv,
                        D, ctx, stream));
-    MHA_TRY(ok(mha::launch_transpose(dtype, dkvbuf, pl.ld_kv, Mk, pl.ld_kv, W(pl.off_dkvt),
-                                     pl.Mk_pad, pl.Mk_pad, stream)));
-    MHA_TRY(ok(mha::launch_transpose(dtype, src_kv, D, Mk, D, W(pl.off_xkvt), pl.Mk_pad,
-                                     pl.Mk_pad, stream)));
-    MHA_TRY(run_linear_wgrad(pl.ld_kv, D, pl.Mk_pad, dtype, W(pl.off_dkvt), pl.Mk_pad,
-                             W(pl.off_xkvt), dWb + static_cast<size_t>(nqk) * D * es, D, wacc,
-                             ctx, stream));
+    MHA_TRY(run_linear_wgrad(pl.ld_kv, D, Mk, dtype, dkvbuf, pl.ld_kv, src_kv, D,
+                             dWb + static_cast<size_t>(nqk) * D * es, D, wacc, W(pl.off_dkvt),
+                             W(pl.off_xkvt), pl.Mk_pad, ctx, stream));
     MHA_TRY(ok(mha::launch_colsum_partials(dtype, dkvbuf, pl.ld_kv, Mk, pl.ld_kv, part,
                                            stream)));
     MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_k, pl.ld_kv, pl.ld_kv,

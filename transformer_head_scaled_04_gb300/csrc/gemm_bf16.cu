@@ -22,6 +22,11 @@
 // output tiles would leave SMs idle): the work units are (K slice, tile) pairs, each unit's
 // fp32 partial goes through the same staging boxes as 32 x 32 fp32 boxes and is added into a
 // zeroed fp32 [M, N] buffer by bulk tensor reductions; a separate launch rounds it to bf16.
+// MN-major operands (kMN, the weight gradients dW = dOut^T In straight from the row-major
+// activations, no transposed copies): X and W are then stored [K, M] and [K, N]; each stage
+// loads 64 x 64 boxes (64 K rows of 64 M or N columns, 128-byte swizzle) side by side, and the
+// MMA reads them MN-major (the 64-column chunks 8 KB apart as the leading-dimension step); K
+// need not be a multiple of 64 (rows past K load as zeros).
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -52,7 +57,7 @@ struct GemmShape {
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
-template <int BN, bool kRelu, bool kAcc>
+template <int BN, bool kRelu, bool kAcc, bool kMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_kb = K / kBK;
+  const int num_kb = kMN ? (K + kBK - 1) / kBK : K / kBK;
   const int tiles_n = (N + BN - 1) / BN;
   const int tiles = tiles_n * ((M + kBM - 1) / kBM);
   // work unit u: tile u % tiles, K slice u / tiles (units running together share K slices)
@@ -128,8 +133,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(full_bar(s), S::kStageBytes);
-        tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
-        tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
+        if constexpr (kMN) {
+#pragma unroll
+          for (int c = 0; c < kBM / 64; ++c)
+            tma_load_2d(smem_u32(sA + s * S::kABytes + c * 8192), &tmX, full_bar(s), m0 + c * 64,
+                        kb * kBK);
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(smem_u32(sB + s * S::kBBytes + c * 8192), &tmW, full_bar(s), n0 + c * 64,
+                        kb * kBK);
+        } else {
+          tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
+          tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
+        }
       }
     }
     // let every copy this thread started land before the CTA can exit
@@ -137,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (void)mbar_wait(full_bar(i % S::kStages), (i / S::kStages) & 1, timeout_ns);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, false, false);
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, kMN, kMN);
     int it = 0, tcount = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++tcount) {
@@ -160,8 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b0 = smem_u32(sB + s * S::kBBytes);
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
-          const uint64_t ad = smem_desc_sw128(a0 + k * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(b0 + k * 32, 16, 1024);
+          // K-major: 16 K values are 32 bytes along the swizzled row; MN-major: 16 K rows
+          const uint64_t ad = kMN ? smem_desc_sw128(a0 + k * 2048, 8192, 1024)
+                                  : smem_desc_sw128(a0 + k * 32, 16, 1024);
+          const uint64_t bd = kMN ? smem_desc_sw128(b0 + k * 2048, 8192, 1024)
+                                  : smem_desc_sw128(b0 + k * 32, 16, 1024);
           mma_bf16_ss(d, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
         }
         mma_commit(empty_bar(s));
@@ -312,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool kRelu, bool kAcc>
+template <int BN, bool kRelu, bool kAcc, bool kMN = false>
 cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
                       const void* bias, void* Y,
                       int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                       const void* R, int ksplit) {
   using S = GemmShape<BN>;
-  auto kern = gemm_bias_bf16_kernel<BN, kRelu, kAcc>;
+  auto kern = gemm_bias_bf16_kernel<BN, kRelu, kAcc, kMN>;
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), S::kSmemBytes, nullptr);
   if (e != cudaSuccess) return e;
   const int64_t units =
@@ -369,14 +388,21 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
   return launch_bn<128, false, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
 }
 
+cudaError_t launch_gemm_bf16_mn(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                const CUtensorMap& tmY, void* Y, int M, int N, int K,
+                                int64_t ldy, const DevCtx& ctx, cudaStream_t s) {
+  return launch_bn<128, false, false, true>(tmX, tmW, tmY, nullptr, Y, M, N, K, ldy, ctx, s,
+                                            nullptr, 1);
+}
+
 cudaError_t launch_gemm_bf16_splitk(const CUtensorMap& tmX, const CUtensorMap& tmW,
                                     const CUtensorMap& tmAcc, float* acc, int ksplit, void* Y,
                                     int M, int N, int K, int64_t ldy, const DevCtx& ctx,
                                     cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(acc, 0, static_cast<size_t>(M) * N * 4, s);
   if (e != cudaSuccess) return e;
-  e = launch_bn<128, false, true>(tmX, tmW, tmAcc, nullptr, nullptr, M, N, K, N, ctx, s, nullptr,
-                                  ksplit);
+  e = launch_bn<128, false, true, true>(tmX, tmW, tmAcc, nullptr, nullptr, M, N, K, N, ctx, s,
+                                        nullptr, ksplit);
   if (e != cudaSuccess) return e;
   const int64_t total = static_cast<int64_t>(M) * (N / 8);
   const int64_t want = (total + 255) / 256;

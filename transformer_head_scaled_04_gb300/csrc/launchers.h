@@ -50,10 +50,15 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                              const void* residual = nullptr);
-// Split-K form for weight gradients (no bias, no activation): acc [M, N] fp32 scratch is
-// zeroed, each of ksplit K slices of every 128 x 128 tile is added into it by bulk tensor
-// reductions through tmAcc (fp32 {N, M}, box {32, 32}, 128-byte swizzle), then Y = bf16(acc).
-// K / 64 must be at least ksplit.
+// Weight-gradient forms (no bias, no activation), both operands MN-major: X stored [K, M] and
+// W stored [K, N] (row-major activations, tokens = K), maps {M or N, K} with box {64, 64};
+// 128 x 128 tiles.  launch_gemm_bf16_mn writes Y directly.  The split-K form zeroes acc
+// [M, N] fp32 scratch, adds each of ksplit K slices of every tile into it by bulk tensor
+// reductions through tmAcc (fp32 {N, M}, box {32, 32}, 128-byte swizzle), then Y = bf16(acc);
+// ceil(K / 64) must be at least ksplit.
+cudaError_t launch_gemm_bf16_mn(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                const CUtensorMap& tmY, void* Y, int M, int N, int K,
+                                int64_t ldy, const DevCtx& ctx, cudaStream_t s);
 cudaError_t launch_gemm_bf16_splitk(const CUtensorMap& tmX, const CUtensorMap& tmW,
                                     const CUtensorMap& tmAcc, float* acc, int ksplit, void* Y,
                                     int M, int N, int K, int64_t ldy, const DevCtx& ctx,
