@@ -955,9 +955,28 @@ def run_profile_case(args):
         C.check(lib.mha_residual_layernorm_fwd(B * N, Dm, C.MHA_BF16, 1e-5, vp(x), vp(a_ln), None,
                                                None, vp(y_ln), sp), "mha_residual_layernorm_fwd")
 
-    fwd()
-    fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv,
-          "layernorm": layernorm}[args.profile_case]
+    def layer_bwd_case():
+        # the whole sublayer backward of the big model at this batch (self-attention, no mask)
+        import transformer_head_scaled_04_gb300 as mha_pkg
+
+        g2 = torch.Generator(device=dev).manual_seed(20260012)
+        xs = torch.randn((B, N, Dm), device=dev, generator=g2).to(bf)
+        Wl = (torch.randn((3 * Dm, Dm), device=dev, generator=g2) * 0.03).to(bf)
+        Wol = (torch.randn((Dm, Dm), device=dev, generator=g2) * 0.03).to(bf)
+        dyl = torch.randn((B, N, Dm), device=dev, generator=g2).to(bf)
+        zq, zo = torch.zeros(3 * Dm, dtype=bf, device=dev), torch.zeros(Dm, dtype=bf, device=dev)
+        ones = torch.ones(Dm, dtype=bf, device=dev)
+        wsl = torch.empty(mha_pkg.layer_bwd_workspace_size(B, H, N, N, Dm, d, d, bf, True),
+                          dtype=torch.uint8, device=dev)
+        return lambda: mha_pkg.mha_layer_backward(xs, None, Wl, zq, Wol, zo, ones, zo, H, dyl,
+                                                  "none", workspace=wsl)
+
+    if args.profile_case == "layer_bwd":
+        fn = layer_bwd_case()
+    else:
+        fwd()
+        fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv,
+              "layernorm": layernorm}[args.profile_case]
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -982,7 +1001,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
-    ap.add_argument("--profile-case", choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm"], default=None,
+    ap.add_argument("--profile-case",
+                    choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm", "layer_bwd"],
+                    default=None,
                     help="run only this kernel family (for ncu captures), no bench line")
     ap.add_argument("--batch", type=int, default=4, help="batch of --profile-case")
     args = ap.parse_args()
