@@ -234,8 +234,10 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
 /*
  * mha_layer_bwd_workspace_size -- bytes of device workspace mha_layer_bwd needs for these
  * sizes (self_attention != 0: x_kv is NULL and Nk == Nq).  It holds the recomputed forward
- * intermediates, the gradients between the steps and the transposed operands of the
- * weight-gradient products.
+ * intermediates (the activations mha_layer_fwd_train leaves), the gradients between the
+ * steps, the attention backward's scratch (with its fp32 dQ accumulator), and for MHA_BF16
+ * the fp32 accumulator of the split-K weight-gradient products, for MHA_F32 their transposed
+ * operands.
  */
 int mha_layer_bwd_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d_v,
                                  int dtype, int self_attention, size_t* bytes);
