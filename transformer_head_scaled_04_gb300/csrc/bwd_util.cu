@@ -281,20 +281,19 @@ __global__ void __launch_bounds__(kRows * 32)
 }
 
 // Column partial sums over a chunk of rows for bf16, 8 consecutive columns per thread:
-// blockDim (128, kRowGroups); row group y takes rows r0 + y, r0 + y + kRowGroups, ...; the
+// blockDim (kCols, kGroups); row group y takes rows r0 + y, r0 + y + kGroups, ...; the
 // groups' sums are added in group order (deterministic).  kTerms = 3: dy * rhat, dy and dr
 // (LayerNorm parameters and db_o); kTerms = 1: the column sums of X (a bias gradient).
-constexpr int kRowGroups = 4;
-template <int kTerms>
-__global__ void __launch_bounds__(128 * kRowGroups)
+template <int kTerms, int kCols, int kGroups>
+__global__ void __launch_bounds__(kCols * kGroups)
     colsum_v8_kernel(const __nv_bfloat16* __restrict__ X, int64_t ld,
                      const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ a,
                      const __nv_bfloat16* __restrict__ dr, const float2* __restrict__ stats,
                      int M, int N, int rows_per_chunk, float* __restrict__ part) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
-  __shared__ float red[kRowGroups - 1][kTerms][128 * 8];
-  const int col = (blockIdx.x * 128 + threadIdx.x) * 8;
+  __shared__ float red[kGroups - 1][kTerms][kCols * 8];
+  const int col = (blockIdx.x * kCols + threadIdx.x) * 8;
   const int chunk = blockIdx.y, grp = threadIdx.y;
   const int r0 = chunk * rows_per_chunk, r1 = min(r0 + rows_per_chunk, M);
   float acc[kTerms][8];
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(128 * kRowGroups)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
   if (col < N) {
-    for (int r = r0 + grp; r < r1; r += kRowGroups) {
+    for (int r = r0 + grp; r < r1; r += kGroups) {
       float d[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(X + static_cast<int64_t>(r) * ld + col), d);
       if (kTerms == 1) {
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(128 * kRowGroups)
       for (int e = 0; e < 8; ++e) {
         float v = acc[k][e];
 #pragma unroll
-        for (int q = 0; q < kRowGroups - 1; ++q) v += red[q][k][threadIdx.x * 8 + e];
+        for (int q = 0; q < kGroups - 1; ++q) v += red[q][k][threadIdx.x * 8 + e];
         o[e] = v;
       }
       float4* dst = reinterpret_cast<float4*>(part + (static_cast<int64_t>(chunk) * kTerms + k) * N + col);
@@ -424,9 +423,11 @@ cudaError_t launch_layernorm_bwd(int dtype, int M, int D, float eps, const void*
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const dim3 g8((D + 1023) / 1024, bwd_row_chunks(M));
-    (void)launch_pdl(colsum_v8_kernel<3>, dim3(g8), dim3(dim3(128, kRowGroups)), 0, s, dyb, D, xb, ab, drb, stats, M, D,
-                                                             kChunkRows, part);
+    // 512 columns and eight row groups per block: a d_model of 1024 gives two blocks per
+    // 256-row chunk, so every SM has work
+    const dim3 g8((D + 511) / 512, bwd_row_chunks(M));
+    (void)launch_pdl(colsum_v8_kernel<3, 64, 8>, dim3(g8), dim3(64, 8), 0, s, dyb,
+                     static_cast<int64_t>(D), xb, ab, drb, stats, M, D, kChunkRows, part);
     return cudaGetLastError();
   }
 #define MHA_LN_BWD(T, N)                                                                    \
@@ -460,8 +461,9 @@ cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, 
                                    float* part, cudaStream_t s) {
   if (dtype == 1 && N % 8 == 0 && ld % 8 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0) {
     const dim3 g8((N + 1023) / 1024, bwd_row_chunks(M));
-    (void)launch_pdl(colsum_v8_kernel<1>, dim3(g8), dim3(dim3(128, kRowGroups)), 0, s, static_cast<const __nv_bfloat16*>(X), ld, nullptr, nullptr, nullptr, nullptr, M, N,
-        kChunkRows, part);
+    (void)launch_pdl(colsum_v8_kernel<1, 128, 4>, dim3(g8), dim3(128, 4), 0, s,
+                     static_cast<const __nv_bfloat16*>(X), ld, nullptr, nullptr, nullptr,
+                     nullptr, M, N, kChunkRows, part);
     return cudaGetLastError();
   }
   const dim3 grid((N + 255) / 256, bwd_row_chunks(M));
