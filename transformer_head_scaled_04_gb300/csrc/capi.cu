@@ -1026,8 +1026,11 @@ namespace {
 // Scratch of one sublayer backward (offsets into the caller's workspace, 256-byte aligned).
 // Forward intermediates: the projections (self: Q|K|V interleaved per token; cross: Q, then
 // K|V), the head-concat C, the W^O output A, the log-sum-exp; then the gradients dr, dC and
-// the projections' gradients (same layouts), the transposed operands of the weight-gradient
-// GEMMs (token axis padded to a multiple of 64) and the fp32 partial column sums.
+// the projections' gradients (same layouts), the transposed weights of the data-gradient
+// GEMMs, the fp32 partial column sums, and for the weight-gradient GEMMs either (bf16) the
+// fp32 split-K accumulator -- their operands are read in place -- or (fp32) the transposed
+// token-axis operands, padded to a multiple of 64 tokens.  mha_layer_fwd_train fills the
+// forward part; mha_layer_bwd_saved reads it.
 struct LayerBwdPlan {
   int Mq, Mk, Mq_pad, Mk_pad, nqk, nv, ld_q, ld_kv;  // ld_q: row pitch of the Q projection
   size_t off_q, off_kv, off_c, off_a, off_lse, off_dvec, off_stats, off_part, off_dr, off_dc,
