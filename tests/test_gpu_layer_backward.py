@@ -89,6 +89,10 @@ def test_layer_backward_base_workloads(name):
     ("key_padding", True, 130, 200),
     ("none", True, 64, 257),
     ("key_padding", False, 1, 1),
+    # enough tokens (3 x 700, 3 x 1500) for the split-K weight gradients, with a ragged last
+    # K slice (2100 and 4500 are not multiples of 64)
+    ("none", False, 700, 700),
+    ("key_padding", True, 130, 1500),
 ])
 def test_layer_backward_bf16_ragged(mask, cross, Nq, Nk):
     w = si.Workload("t", "layer", "bf16", B=3, H=4, Nq=Nq, Nk=Nk, mask=mask, cross=cross,
