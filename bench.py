@@ -434,7 +434,7 @@ def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
                           "what": "mha_layer_fwd_train (y, activations kept) then "
                                   "mha_layer_bwd_saved: the same FLOPs as the recomputing "
                                   "backward, plus y"},
-        "gpu_launches_per_step": {"attention": 3, "layer": 21, "training_step": 22},
+        "gpu_launches_per_step": {"attention": 3, "layer": 19, "training_step": 20},
     }
 
 

@@ -144,18 +144,29 @@ __global__ void __launch_bounds__(256)
   part[static_cast<int64_t>(chunk) * N + col] = s;
 }
 
-// out[col] = sum over chunks, in chunk order, of part[chunk * chunk_stride + col]
+// out_t[col] = sum over chunks of part[t * term_stride + chunk * chunk_stride + col] for the
+// term t = blockIdx.y (up to three outputs per launch); chunk c goes to partial sum c % 4 and
+// the four are added in a fixed order (deterministic)
 template <typename T>
 __global__ void __launch_bounds__(256)
     reduce_partials_kernel(const float* __restrict__ part, int nchunk, int64_t chunk_stride,
-                           int N, T* __restrict__ out) {
+                           int N, int64_t term_stride, T* __restrict__ out0,
+                           T* __restrict__ out1, T* __restrict__ out2) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   const int col = blockIdx.x * 256 + threadIdx.x;
   if (col >= N) return;
-  float s = 0.f;
-  for (int c = 0; c < nchunk; ++c) s += part[static_cast<int64_t>(c) * chunk_stride + col];
-  out[col] = stf<T>(s);
+  const int t = blockIdx.y;
+  T* out = t == 0 ? out0 : (t == 1 ? out1 : out2);
+  const float* p = part + t * term_stride + col;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  int c = 0;
+  for (; c + 4 <= nchunk; c += 4) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s4[q] += p[static_cast<int64_t>(c + q) * chunk_stride];
+  }
+  for (int q = 0; c < nchunk; ++c, ++q) s4[q] += p[static_cast<int64_t>(c) * chunk_stride];
+  out[col] = stf<T>((s4[0] + s4[1]) + (s4[2] + s4[3]));
 }
 
 // Y[c * ldy + r] = X[r * ldx + c] for r < R, c < C; rows R <= r < R_pad of Y's columns are 0
@@ -477,12 +488,23 @@ cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, 
 
 cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
                                    int64_t chunk_stride, int N, void* out, cudaStream_t s) {
-  const dim3 grid((N + 255) / 256);
+  return launch_reduce_partials3(dtype, part, nchunk, chunk_stride, N, 0, 1, out, nullptr,
+                                 nullptr, s);
+}
+
+cudaError_t launch_reduce_partials3(int dtype, const float* part, int nchunk,
+                                    int64_t chunk_stride, int N, int64_t term_stride,
+                                    int nterm, void* out0, void* out1, void* out2,
+                                    cudaStream_t s) {
+  const dim3 grid((N + 255) / 256, nterm);
   if (dtype == 1)
-    (void)launch_pdl(reduce_partials_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, part, nchunk, chunk_stride, N, static_cast<__nv_bfloat16*>(out));
+    (void)launch_pdl(reduce_partials_kernel<__nv_bfloat16>, grid, dim3(256), 0, s, part, nchunk,
+                     chunk_stride, N, term_stride, static_cast<__nv_bfloat16*>(out0),
+                     static_cast<__nv_bfloat16*>(out1), static_cast<__nv_bfloat16*>(out2));
   else
-    (void)launch_pdl(reduce_partials_kernel<float>, dim3(grid), dim3(256), 0, s, part, nchunk, chunk_stride, N,
-                                                       static_cast<float*>(out));
+    (void)launch_pdl(reduce_partials_kernel<float>, grid, dim3(256), 0, s, part, nchunk,
+                     chunk_stride, N, term_stride, static_cast<float*>(out0),
+                     static_cast<float*>(out1), static_cast<float*>(out2));
   return cudaGetLastError();
 }
 

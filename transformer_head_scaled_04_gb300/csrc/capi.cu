@@ -1197,9 +1197,8 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
                                        W(pl.off_dr), static_cast<float2*>(W(pl.off_stats)),
                                        part, stream)));
   const int nch_q = mha::bwd_row_chunks(Mq);
-  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part, nch_q, 3 * D, D, dgamma, stream)));
-  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part + D, nch_q, 3 * D, D, dbeta, stream)));
-  MHA_TRY(ok(mha::launch_reduce_partials(dtype, part + 2 * D, nch_q, 3 * D, D, db_o, stream)));
+  MHA_TRY(ok(mha::launch_reduce_partials3(dtype, part, nch_q, 3 * D, D, D, 3, dgamma, dbeta,
+                                          db_o, stream)));
 
   // ---- W^O: dC = dr W^O (via W^O^T), dW^O = dr^T C
   MHA_TRY(ok(mha::launch_transpose(dtype, W_o, nv, D, nv, W(pl.off_wot), D, D, stream)));

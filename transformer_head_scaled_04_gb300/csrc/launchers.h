@@ -173,6 +173,11 @@ cudaError_t launch_colsum_partials(int dtype, const void* X, int64_t ld, int M, 
 // out[col] = sum over chunks of part[chunk * chunk_stride + col], in chunk order
 cudaError_t launch_reduce_partials(int dtype, const float* part, int nchunk,
                                    int64_t chunk_stride, int N, void* out, cudaStream_t s);
+// nterm (<= 3) such sums in one launch: out_t from part + t * term_stride
+cudaError_t launch_reduce_partials3(int dtype, const float* part, int nchunk,
+                                    int64_t chunk_stride, int N, int64_t term_stride,
+                                    int nterm, void* out0, void* out1, void* out2,
+                                    cudaStream_t s);
 // Y [C, R_pad] (row pitch ldy) = X [R, C]^T (row pitch ldx), zero for rows R..R_pad
 cudaError_t launch_transpose(int dtype, const void* X, int64_t ldx, int R, int C, void* Y,
                              int64_t ldy, int R_pad, cudaStream_t s);
