@@ -312,9 +312,12 @@ int mha_layer_bwd_saved(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
  * file-scope __device__ array that stays resident on every GPU that loads the library until
  * the process exits).  It calls no cudaMalloc, cudaFree or other allocating routine.
  *
- * Arguments, results and errors are those of mha_layer_fwd without workspace/ws_bytes.
+ * Arguments, results and errors are those of mha_layer_fwd without workspace/ws_bytes: it
+ * makes the same checks in the same order (the current device's last, so a device other
+ * than sm_103 gives MHA_ERR_UNSUPPORTED) before it touches the scratch area.
  * Sizes whose mha_layer_workspace_size() exceeds 48 MiB (50331648 bytes) return
- * MHA_ERR_WORKSPACE before anything is launched.
+ * MHA_ERR_WORKSPACE before anything is launched.  At d_model 512 (h = 8, d_k = d_v = 64)
+ * that is up to 9830 self-attention tokens (B * n) per call in bf16 and 4915 in fp32.
  * The first call on each device looks up the scratch area's device address with that
  * device current (cudaGetSymbolAddress) and caches it; make that first call before any
  * stream capture.

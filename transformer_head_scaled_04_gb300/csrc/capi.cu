@@ -687,6 +687,33 @@ int mha_layer_workspace_size(int B, int H, int Nq, int Nk, int D, int d_k, int d
 
 }  // extern "C"
 
+namespace mha {
+int check_layer_call(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                     const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                     const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                     const void* gamma, const void* beta, const void* y, const void* workspace,
+                     size_t ws_bytes, bool builtin_workspace, DevCtx* ctx) {
+  int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
+  if (st != MHA_OK) return st;
+  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
+  const bool self = (x_kv == nullptr);
+  if ((self || mask == MHA_MASK_CAUSAL) && Nq != Nk) return MHA_ERR_INVALID;
+  if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
+  if (x_q == nullptr || W_qkv == nullptr || W_o == nullptr || y == nullptr)
+    return MHA_ERR_INVALID;
+  if (std::isnan(ln_eps) || ln_eps < 0.f) return MHA_ERR_INVALID;
+  const LayerPlan plan = plan_layer(B, H, Nq, Nk, D, d_k, d_v, dtype);
+  if ((!builtin_workspace && workspace == nullptr) || ws_bytes < plan.total)
+    return MHA_ERR_WORKSPACE;
+  const void* all[] = {x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, y};
+  for (const void* p : all)
+    if (p != nullptr && !aligned(p, 16)) return MHA_ERR_ALIGN;
+  if (key_len != nullptr && !aligned(key_len, 4)) return MHA_ERR_ALIGN;
+  if (!builtin_workspace && !aligned(workspace, 256)) return MHA_ERR_ALIGN;
+  return device_ctx(ctx);
+}
+}  // namespace mha
+
 namespace {
 // ev: null, or 5 events recorded on `stream` at the step boundaries (before the projections,
 // before attention, before the output projection, before the residual LayerNorm, after it).
@@ -698,26 +725,13 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   auto mark = [&](int i) {
     if (ev != nullptr) cudaEventRecord(ev[i], stream);
   };
-  int st = check_layer_shape(B, H, Nq, Nk, D, d_k, d_v, dtype);
-  if (st != MHA_OK) return st;
-  if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
-  const bool self = (x_kv == nullptr);
-  if ((self || mask == MHA_MASK_CAUSAL) && Nq != Nk) return MHA_ERR_INVALID;
-  if (mask == MHA_MASK_KEY_PADDING && key_len == nullptr) return MHA_ERR_INVALID;
-  if (x_q == nullptr || W_qkv == nullptr || W_o == nullptr || y == nullptr)
-    return MHA_ERR_INVALID;
-  if (std::isnan(ln_eps) || ln_eps < 0.f) return MHA_ERR_INVALID;
-  const LayerPlan plan = plan_layer(B, H, Nq, Nk, D, d_k, d_v, dtype);
-  if (workspace == nullptr || ws_bytes < plan.total) return MHA_ERR_WORKSPACE;
-  const void* all[] = {x_q, x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, y, workspace};
-  for (const void* p : all)
-    if (p != nullptr && !aligned(p, 16)) return MHA_ERR_ALIGN;
-  if (key_len != nullptr && !aligned(key_len, 4)) return MHA_ERR_ALIGN;
-  if (!aligned(workspace, 256)) return MHA_ERR_ALIGN;
-
   DevCtx ctx;
-  st = device_ctx(&ctx);
+  int st = mha::check_layer_call(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q,
+                                 x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, y, workspace,
+                                 ws_bytes, false, &ctx);
   if (st != MHA_OK) return st;
+  const bool self = (x_kv == nullptr);
+  const LayerPlan plan = plan_layer(B, H, Nq, Nk, D, d_k, d_v, dtype);
 
   const size_t es = elem_size(dtype);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -17,6 +17,16 @@ struct DevCtx {
   int num_sms;
 };
 
+// ---- every check mha_layer_fwd makes before it launches anything, in its order: shapes,
+// mask, required pointers, eps, workspace size, alignment, then the current device (which
+// fills ctx).  builtin_workspace: the workspace is the library's own scratch area, whose
+// address is looked up only after these checks pass (workspace is then ignored).
+int check_layer_call(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype, int mask,
+                     const int32_t* key_len, float ln_eps, const void* x_q, const void* x_kv,
+                     const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                     const void* gamma, const void* beta, const void* y, const void* workspace,
+                     size_t ws_bytes, bool builtin_workspace, DevCtx* ctx);
+
 // ---- per-kernel launch preparation: raises the kernel's dynamic shared-memory limit to
 // smem_bytes and reports its register count (num_regs may be null), once per (kernel, device);
 // later calls return the cached result without driver calls.

@@ -10,16 +10,20 @@
 // CUDA runtime places in device memory when it loads this module on a device.  It stays
 // there, on every GPU that loads the library, until the process exits.
 //
-// Nothing here calls cudaMalloc, cudaFree or any allocating routine.  The entry point only
-// looks up the array's device address (once per device) and forwards to mha_layer_fwd.
+// Nothing here calls cudaMalloc, cudaFree or any allocating routine.  The entry point runs
+// every check mha_layer_fwd makes (the current device's included), then looks up the
+// array's device address (once per device) and forwards to mha_layer_fwd.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
+#include "launchers.h"
 #include "mha.h"
 
-// Largest workspace the no-alloc entry point can serve: 48 MiB, enough for every base-model
-// workload (d_model 512, up to 8192 query tokens of self-attention per call).
+// Largest workspace the no-alloc entry point can serve: 48 MiB.  Self-attention at
+// d_model 512 (h = 8, d_k = d_v = 64) keeps 5120 bytes per token in bf16 and 10240 in fp32,
+// so one call serves up to 9830 tokens (B * n) in bf16 and 4915 in fp32; cross-attention
+// keeps 3072 bytes per query token and 2048 per key token in bf16 (twice that in fp32).
 static constexpr size_t kLayerScratchBytes = static_cast<size_t>(48) << 20;
 
 // The scratch itself.  Host code must not use this name as a pointer: on the host it is only
@@ -61,10 +65,14 @@ extern "C" int mha_layer_fwd_noalloc(int B, int H, int Nq, int Nk, int D, int d_
                                      const void* b_qkv, const void* W_o, const void* b_o,
                                      const void* gamma, const void* beta, void* y,
                                      cudaStream_t stream) {
-  size_t need = 0;
-  int st = mha_layer_workspace_size(B, H, Nq, Nk, D, d_k, d_v, dtype, &need);
+  // The same checks, in the same order, as mha_layer_fwd with a 48 MiB workspace, so this
+  // entry point returns the codes that one would (MHA_ERR_WORKSPACE beyond 48 MiB,
+  // MHA_ERR_UNSUPPORTED on a device other than sm_103) before it touches the scratch symbol.
+  mha::DevCtx ctx;
+  int st = mha::check_layer_call(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q,
+                                 x_kv, W_qkv, b_qkv, W_o, b_o, gamma, beta, y, nullptr,
+                                 kLayerScratchBytes, true, &ctx);
   if (st != MHA_OK) return st;
-  if (need > kLayerScratchBytes) return MHA_ERR_WORKSPACE;  // beyond the built-in 48 MiB
   void* ws = nullptr;
   st = scratch_address(&ws);
   if (st != MHA_OK) return st;
