@@ -73,17 +73,40 @@ def window_pairs(B: int, H: int, N: int, window: int) -> int:
     return int(B * H * per_row.sum())
 
 
-def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
+def tstats(ts) -> dict:
+    """Mean, median, min and 90th percentile of a list of times (ms)."""
+    a = np.asarray(ts, dtype=np.float64)
+    return {"mean": float(a.mean()), "median": float(np.median(a)), "min": float(a.min()),
+            "p90": float(np.percentile(a, 90))}
+
+
+def sdpa_hbm_bytes(w: si.Workload, key_len=None) -> float:
+    """Fewest bytes the attention step can move: every query row of Q read and of O written
+    once, and the K and V rows some query may attend read once (bf16).  Under key padding only
+    the first key_len[b] rows of K and V are ever needed."""
+    es = 2.0
+    q_o = 2.0 * w.B * w.H * w.Nq * w.d_k * es
+    if w.mask == "key_padding":
+        keys = float(np.clip(key_len, 0, w.Nk).sum())
+    else:
+        keys = float(w.B * w.Nk)
+    return q_o + 2.0 * w.H * keys * w.d_k * es
+
+
+def measure_base_configs(lib, C, dev, stream, flush, steps, warmup, peaks):
     """The base model's sublayer workloads (d_model=512, h=8) and the small fp32 attention
     call: one mha_layer_fwd (mha_sdpa_fwd) per step, L2 flushed before each, CUDA events.
-    These are launch- and latency-bound sizes; the big workload is the throughput case."""
+    These are launch- and latency-bound sizes; the big workload is the throughput case.
+    Each step of the sublayer is also launched alone through its own entry point (L2 flushed
+    before every launch) and set against its roofline: attention and LayerNorm against HBM,
+    the projections against the bf16 tensor peak."""
     import torch
 
     sp = ctypes.c_void_p(stream.cuda_stream)
     vp = lambda x: None if x is None else ctypes.c_void_p(x.data_ptr())  # noqa: E731
     out = {}
 
-    def timeit(fn):
+    def timeit_all(fn):
         for _ in range(warmup):
             fn()
         ts = []
@@ -95,7 +118,24 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
             e1.record(stream)
             e1.synchronize()
             ts.append(e0.elapsed_time(e1))
-        return float(np.median(ts))
+        return tstats(ts)
+
+    def timeit(fn):
+        return timeit_all(fn)["median"]
+
+    hbm = float(peaks["hbm_gbs"])
+    tensor = float(peaks["bf16_tflops"])
+
+    def hbm_line(kernel, nbytes, st):
+        gbs = nbytes / (st["median"] * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gbs / hbm, "algorithmic_bytes_per_launch": nbytes, "ms": st}
+
+    def tensor_line(kernel, flops, st):
+        tf = flops / (st["median"] * 1e-3) / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": tf, "peak": tensor,
+                "unit": "TFLOP/s", "frac": tf / tensor, "algorithmic_flops_per_launch": flops,
+                "ms": st}
 
     for name in ("enc_self_base_b32_n128", "dec_causal_base_b32_n256",
                  "cross_pad_base_b32_q128_k256"):
@@ -112,8 +152,11 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
         a = (w.B, w.H, w.Nq, w.Nk, w.D, w.d_k, w.d_v, C.MHA_BF16, C.MASKS[w.mask], vp(kl), 1e-5,
              vp(t["x_q"]), vp(t["x_kv"]), vp(t["W_qkv"]), vp(t["b_qkv"]), vp(t["W_o"]),
              vp(t["b_o"]), vp(t["gamma"]), vp(t["beta"]), vp(y), vp(ws), ws.numel(), sp)
-        ms = timeit(lambda: C.check(lib.mha_layer_fwd(*a), "mha_layer_fwd"))
+        st_layer = timeit_all(lambda: C.check(lib.mha_layer_fwd(*a), "mha_layer_fwd"))
+        ms = st_layer["median"]
         fl = layer_flops(w, w.mask, inp["key_len"])
+        roof = base_step_rooflines(lib, C, dev, sp, vp, w, t, kl, inp["key_len"], timeit_all,
+                                   hbm_line, tensor_line)
         # where the time goes: events at the step boundaries (median over the steps)
         per = []
         for _ in range(steps):
@@ -127,11 +170,14 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
             evs[4].synchronize()
             per.append([evs[k].elapsed_time(evs[k + 1]) for k in range(4)])
         med = np.median(np.array(per), axis=0)
-        out[name] = {"ms": ms, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
+        out[name] = {"ms": ms, "ms_stats": st_layer, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
                      "tokens_per_s": w.B * w.Nq / (ms * 1e-3), "flops_per_step": fl,
                      "step_breakdown_ms": {"qkv_proj": float(med[0]), "sdpa": float(med[1]),
                                            "out_proj": float(med[2]),
-                                           "residual_layernorm": float(med[3])}}
+                                           "residual_layernorm": float(med[3])},
+                     "step_breakdown_note": "events recorded between the launches of one "
+                                            "mha_layer_fwd_timed call (median over steps)",
+                     "roofline": roof}
     # the small fp32 attention call (B=1, h=8, n=32, d=64): latency
     w = si.WORKLOADS["sdpa_f32_b1_h8_n32"]
     Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="f32", seed=w.seed)
@@ -140,9 +186,70 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup):
     O = torch.empty_like(tq)
     a = (w.B, w.H, w.Nq, w.Nk, 64, 64, C.MHA_F32, 0, None, 0.0, vp(tq), vp(tk), vp(tv), vp(O),
          None, sp)
-    ms = timeit(lambda: C.check(lib.mha_sdpa_fwd(*a), "mha_sdpa_fwd"))
-    out["sdpa_f32_b1_h8_n32"] = {"us": ms * 1e3, "flops_per_call": sdpa_flops(w, "none")}
+    st = timeit_all(lambda: C.check(lib.mha_sdpa_fwd(*a), "mha_sdpa_fwd"))
+    out["sdpa_f32_b1_h8_n32"] = {"us": st["median"] * 1e3,
+                                 "us_stats": {k: v * 1e3 for k, v in st.items()},
+                                 "flops_per_call": sdpa_flops(w, "none")}
     return out
+
+
+def base_step_rooflines(lib, C, dev, sp, vp, w, t, kl, key_len, timeit_all, hbm_line,
+                        tensor_line):
+    """Each step of one base-model sublayer launched alone through its entry point (the
+    projections through mha_linear_fwd, attention through mha_sdpa_fwd on the projection
+    buffer's strided layout, residual + LayerNorm through mha_residual_layernorm_fwd), timed
+    and set against its roofline."""
+    import torch
+
+    bf = torch.bfloat16
+    D, H, d = w.D, w.H, w.d_k
+    Mq, Mk = w.B * w.Nq, w.B * w.Nk
+    res = {}
+    if not w.cross:
+        qkv = torch.empty((Mq, 3 * D), dtype=bf, device=dev)
+        st = timeit_all(lambda: C.check(lib.mha_linear_fwd(
+            Mq, 3 * D, D, C.MHA_BF16, vp(t["x_q"]), D, vp(t["W_qkv"]), vp(t["b_qkv"]), vp(qkv),
+            3 * D, sp), "mha_linear_fwd"))
+        res["qkv_proj"] = tensor_line("gemm_bias_bf16_kernel", 2.0 * Mq * D * 3 * D, st)
+        qp, kp, vp_ = qkv.data_ptr(), qkv.data_ptr() + 2 * D, qkv.data_ptr() + 4 * D
+        sq = [w.Nq * 3 * D, d, 3 * D, 1]
+        skv = sq
+    else:
+        qb = torch.empty((Mq, D), dtype=bf, device=dev)
+        kvb = torch.empty((Mk, 2 * D), dtype=bf, device=dev)
+        wq, wkv = t["W_qkv"][:D], t["W_qkv"][D:]
+        bq, bkv = t["b_qkv"][:D], t["b_qkv"][D:]
+
+        def proj():
+            C.check(lib.mha_linear_fwd(Mq, D, D, C.MHA_BF16, vp(t["x_q"]), D, vp(wq), vp(bq),
+                                       vp(qb), D, sp), "mha_linear_fwd")
+            C.check(lib.mha_linear_fwd(Mk, 2 * D, D, C.MHA_BF16, vp(t["x_kv"]), D, vp(wkv),
+                                       vp(bkv), vp(kvb), 2 * D, sp), "mha_linear_fwd")
+        st = timeit_all(proj)
+        res["qkv_proj"] = tensor_line("gemm_bias_bf16_kernel (Q, then K|V: two launches)",
+                                      2.0 * Mq * D * D + 2.0 * Mk * D * 2 * D, st)
+        qp, kp, vp_ = qb.data_ptr(), kvb.data_ptr(), kvb.data_ptr() + 2 * D
+        sq = [w.Nq * D, d, D, 1]
+        skv = [w.Nk * 2 * D, d, 2 * D, 1]
+    c = torch.empty((Mq, D), dtype=bf, device=dev)
+    strides = (ctypes.c_int64 * 16)(*(sq + skv + skv + [w.Nq * D, d, D, 1]))
+    st = timeit_all(lambda: C.check(lib.mha_sdpa_fwd(
+        w.B, H, w.Nq, w.Nk, d, d, C.MHA_BF16, C.MASKS[w.mask], vp(kl), 0.0, ctypes.c_void_p(qp),
+        ctypes.c_void_p(kp), ctypes.c_void_p(vp_), vp(c), ctypes.cast(strides, ctypes.c_void_p),
+        sp), "mha_sdpa_fwd"))
+    res["sdpa"] = hbm_line("sdpa_fwd_bf16_kernel", sdpa_hbm_bytes(w, key_len), st)
+    res["sdpa"]["tflops"] = sdpa_flops(w, w.mask, key_len) / (st["median"] * 1e-3) / 1e12
+    a_out = torch.empty((Mq, D), dtype=bf, device=dev)
+    st = timeit_all(lambda: C.check(lib.mha_linear_fwd(
+        Mq, D, D, C.MHA_BF16, vp(c), D, vp(t["W_o"]), vp(t["b_o"]), vp(a_out), D, sp),
+        "mha_linear_fwd"))
+    res["out_proj"] = tensor_line("gemm_bias_bf16_kernel", 2.0 * Mq * D * D, st)
+    y = torch.empty((Mq, D), dtype=bf, device=dev)
+    st = timeit_all(lambda: C.check(lib.mha_residual_layernorm_fwd(
+        Mq, D, C.MHA_BF16, 1e-5, vp(t["x_q"]), vp(a_out), vp(t["gamma"]), vp(t["beta"]), vp(y),
+        sp), "mha_residual_layernorm_fwd"))
+    res["residual_layernorm"] = hbm_line("residual_layernorm_stream_kernel", 6.0 * Mq * D, st)
+    return res
 
 
 def measure_window(lib, C, dev, stream, flush, steps, warmup, peak, window=WINDOW):
@@ -567,21 +674,65 @@ def oracle_sample(inp, w, mask, b, rows):
     return proj + 2.0 * (w.d_k + w.d_v) * pairs + 2.0 * n * w.H * w.d_v * D
 
 
+def oracle_batch_element(inp, w, mask, b):
+    """One sample of the CPU oracle legs (cpu_baseline and --impl reference alike): the whole
+    sublayer for every query row of batch element b.  Returns its algorithmic FLOPs."""
+    return oracle_sample(inp, w, mask, b, np.arange(w.Nq))
+
+
+def cpu_fields() -> dict:
+    """Threads the oracle used (numpy's BLAS pool; the rest of the oracle is one Python
+    thread) and the host's core count, reported separately."""
+    return {"cores": blas_threads(), "blas_threads": blas_threads(),
+            "host_cpu_count": os.cpu_count()}
+
+
 def cpu_baseline(inp, w, mask, budget_s=12.0):
     """The oracle as it stands, timed on this host on whole batch elements (all 4096 query
     rows each) until about `budget_s` seconds of work have run."""
     flops, t0, done = 0.0, time.perf_counter(), 0
-    rows = np.arange(w.Nq)
     while done < w.B:
-        flops += oracle_sample(inp, w, mask, done, rows)
+        flops += oracle_batch_element(inp, w, mask, done)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
-    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": f"{done} of {w.B} batch elements (all {w.Nq} query rows, {mask} mask) of "
-                      f"the same workload, float64 NumPy, {el:.1f} s"}
+    out = {"value": flops / el / 1e12, "unit": "TFLOP/s", "kind": "oracle",
+           "sample": f"{done} of {w.B} batch elements (all {w.Nq} query rows, {mask} mask) of "
+                     f"the same workload, float64 NumPy, {el:.1f} s"}
+    out.update(cpu_fields())
+    return out
+
+
+def cpu_oracle_configs(min_s=1.0):
+    """The full oracle (no sampling) on the small fp32 attention call and the three base-model
+    sublayers, each repeated until min_s seconds have run; median time per call."""
+    import oracle
+
+    res = {}
+    w = si.WORKLOADS["sdpa_f32_b1_h8_n32"]
+    Q, K, V, _ = si.draw_sdpa(w.B, w.H, w.Nq, w.Nk, dtype="f32", seed=w.seed)
+    jobs = [(w.name, lambda: oracle.sdpa_ref(Q, K, V), sdpa_flops(w, "none"), w.B * w.Nq)]
+    for name in ("enc_self_base_b32_n128", "dec_causal_base_b32_n256",
+                 "cross_pad_base_b32_q128_k256"):
+        wl = si.WORKLOADS[name]
+        inp = si.draw_layer(wl)
+        jobs.append((name, (lambda inp=inp, wl=wl: oracle.mha_layer_ref(
+            inp["x_q"], inp["x_kv"], inp["W_qkv"], inp["b_qkv"], inp["W_o"], inp["b_o"],
+            inp["gamma"], inp["beta"], wl.H, wl.mask, inp["key_len"])),
+            layer_flops(wl, wl.mask, inp["key_len"]), wl.B * wl.Nq))
+    for name, fn, fl, tokens in jobs:
+        ts, t0 = [], time.perf_counter()
+        while not ts or time.perf_counter() - t0 < min_s:
+            t1 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t1)
+        med = float(np.median(ts))
+        res[name] = {"ms": med * 1e3, "calls": len(ts), "GFLOP/s": fl / med / 1e9,
+                     "tokens_per_s": tokens / med, "flops_per_call": fl}
+    res.update(cpu_fields())
+    res["what"] = "the whole float64 NumPy oracle per call (no sampling), median over calls"
+    return res
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -638,13 +789,9 @@ def run_reference(args):
         return 0
     w = si.WORKLOADS[WORKLOAD]
     inp = si.draw_layer(w)
-    g = np.random.Generator(np.random.PCG64(1234))
-    n_rows = 256
 
-    def step(i):
-        b = i % w.B
-        rows = np.sort(g.choice(w.Nq, n_rows, replace=False))
-        return oracle_sample(inp, w, "none", b, rows)
+    def step(i):  # the same sample as cpu_baseline: one whole batch element per step
+        return oracle_batch_element(inp, w, "none", i % w.B)
 
     for i in range(args.warmup):
         step(i)
@@ -660,10 +807,9 @@ def run_reference(args):
         "unit": "TFLOP/s",
         "ms_per_step": el / args.steps * 1e3,
         "dtype": "f64",
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
-                         "kind": "oracle",
-                         "sample": f"per step: {n_rows} random query rows of one batch element "
-                                   f"(K/V projected in full), float64 NumPy oracle"},
+        "cpu_baseline": dict({"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                              "sample": f"per step: one whole batch element (all {w.Nq} query "
+                                        f"rows, no mask), float64 NumPy oracle"}, **cpu_fields()),
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     })
@@ -768,7 +914,7 @@ def run_ours(args):
     # the feed-forward sublayer and the whole encoder layer on the same tokens
     ffn = measure_ffn(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
     window = measure_window(lib, C, dev, stream, flush, args.steps, args.warmup, peak)
-    base = measure_base_configs(lib, C, dev, stream, flush, args.steps, args.warmup)
+    base = measure_base_configs(lib, C, dev, stream, flush, args.steps, args.warmup, peaks)
     window["speedup_vs_full_attention_time"] = sdpa_ms / window["ms"]
     decode = measure_decode(lib, C, dev, stream, flush, args.steps, args.warmup,
                             float(peaks["hbm_gbs"]))
@@ -859,6 +1005,12 @@ def run_ours(args):
         "step_breakdown_ms": {"qkv_proj": float(per[:, 0].mean()), "sdpa": sdpa_ms,
                               "out_proj": float(per[:, 2].mean()),
                               "residual_layernorm": float(per[:, 3].mean())},
+        "timing_ms": {"step": tstats(per.sum(axis=1)), "qkv_proj": tstats(per[:, 0]),
+                      "sdpa": tstats(per[:, 1]), "out_proj": tstats(per[:, 2]),
+                      "residual_layernorm": tstats(per[:, 3]),
+                      "causal_step": tstats(per_c.sum(axis=1)),
+                      "causal_sdpa": tstats(per_c[:, 1]),
+                      "note": "value, ms_per_step and the roofline use the means"},
         "roofline": {"kernel": "sdpa_fwd_bf16_kernel", "bound": "tensor", "achieved": sdpa_tf,
                      "peak": peak, "unit": "TFLOP/s", "frac": sdpa_tf / peak,
                      "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)"
@@ -891,6 +1043,7 @@ def run_ours(args):
     })
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(inp, w, "none")
+        out["cpu_oracle_configs"] = cpu_oracle_configs()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg:

@@ -35,6 +35,16 @@ Tolerances (stated for the sublayer's outputs):
 """
 import numpy as np
 
+# Every comparison below records what it reached: (what, bound kind, measured values, ratio of
+# the measured value to its bound for each bound).  conftest.py prints the worst ratios at the
+# end of the session and writes them all to $MHA_PARITY_REPORT (JSON) when that is set.
+ACHIEVED: list[dict] = []
+
+
+def _record(what, kind, **vals):
+    ACHIEVED.append(dict(what=what, kind=kind, **{k: float(v) for k, v in vals.items()}))
+
+
 BF16_MAX_ABS = 2e-2
 BF16_REL_L2 = 5e-3
 BF16_TWO_SUBLAYER_MAX_ABS = 4e-2
@@ -54,6 +64,8 @@ def errors(got, ref):
 def assert_bf16_close(got, ref, what="", max_abs_bound=BF16_MAX_ABS):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     max_abs, rel = errors(got, ref)
+    _record(what, "bf16", max_abs=max_abs, rel_l2=rel, max_abs_ratio=max_abs / max_abs_bound,
+            rel_l2_ratio=rel / BF16_REL_L2)
     assert max_abs <= max_abs_bound and rel <= BF16_REL_L2, \
         f"{what}: max|d|={max_abs:.3e} (<= {max_abs_bound}), relL2={rel:.3e} (<= {BF16_REL_L2})"
     return max_abs, rel
@@ -66,6 +78,7 @@ def assert_f32_close(got, ref, what=""):
     _, rel = errors(got, ref)
     bound = F32_REL * np.maximum(1.0, np.abs(ref))
     worst = float((np.abs(got - ref) / bound).max())
+    _record(what, "f32", rel_l2=rel, elem_ratio=worst, rel_l2_ratio=rel / F32_REL)
     assert rel <= F32_REL and worst <= 1.0, f"{what}: relL2={rel:.3e}, worst elem ratio={worst:.3f}"
     return worst, rel
 
@@ -81,6 +94,7 @@ def assert_bf16_grad_close(got, ref, what=""):
     _, rel = errors(got, ref)
     bound = BF16_GRAD_ABS + BF16_GRAD_REL * np.abs(ref)
     worst = float((np.abs(got - ref) / bound).max()) if got.size else 0.0
+    _record(what, "bf16_grad", rel_l2=rel, elem_ratio=worst, rel_l2_ratio=rel / BF16_REL_L2)
     assert worst <= 1.0 and rel <= BF16_REL_L2, \
         f"{what}: worst |d| / (2e-2 + 2^-7 |ref|) = {worst:.3f}, relL2={rel:.3e}"
     return worst, rel
@@ -100,6 +114,8 @@ def assert_bf16_token_grad_close(got, ref, what=""):
     row_rms = np.sqrt(np.mean(r2 * r2, axis=1, keepdims=True))
     bound = BF16_GRAD_ABS * np.maximum(1.0, row_rms) + BF16_GRAD_REL * np.abs(r2)
     worst = float((np.abs(got.reshape(r2.shape) - r2) / bound).max()) if got.size else 0.0
+    _record(what, "bf16_token_grad", rel_l2=rel, elem_ratio=worst,
+            rel_l2_ratio=rel / BF16_LAYER_GRAD_REL_L2)
     assert worst <= 1.0 and rel <= BF16_LAYER_GRAD_REL_L2, \
         f"{what}: worst |d| / (2e-2 max(1, row rms) + 2^-7 |ref|) = {worst:.3f}, " \
         f"relL2={rel:.3e}"
@@ -115,6 +131,12 @@ def assert_bf16_param_grad_close(got, ref, what=""):
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     bound = BF16_PARAM_GRAD_ABS * max(1.0, rms) + BF16_GRAD_REL * np.abs(ref)
     worst = float((np.abs(got - ref) / bound).max()) if got.size else 0.0
+    # the same error against the per-token bound's 2e-2 scale, to show how much of the
+    # parameter bound's extra room is used
+    tight = BF16_GRAD_ABS * max(1.0, rms) + BF16_GRAD_REL * np.abs(ref)
+    worst_tight = float((np.abs(got - ref) / tight).max()) if got.size else 0.0
+    _record(what, "bf16_param_grad", rel_l2=rel, elem_ratio=worst,
+            elem_ratio_at_2e2=worst_tight, rel_l2_ratio=rel / BF16_LAYER_GRAD_REL_L2)
     assert worst <= 1.0 and rel <= BF16_LAYER_GRAD_REL_L2, \
         f"{what}: worst |d| / (5e-2 max(1, rms) + 2^-7 |ref|) = {worst:.3f} (rms {rms:.3g}), " \
         f"relL2={rel:.3e}"
