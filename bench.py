@@ -39,6 +39,9 @@ WORKLOAD = "big_long_b8_n4096"
 FFN_WORKLOAD = "ffn_big_b8_n4096"
 WINDOW = 256
 DECODE_B, DECODE_L = 64, 4096
+# one sublayer call: the Q|K|V projection, the fused attention, and the W^O projection fused
+# with the residual LayerNorm
+LAYER_LAUNCHES = 3
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -173,8 +176,7 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup, peaks):
         out[name] = {"ms": ms, "ms_stats": st_layer, "TFLOP/s": fl / (ms * 1e-3) / 1e12,
                      "tokens_per_s": w.B * w.Nq / (ms * 1e-3), "flops_per_step": fl,
                      "step_breakdown_ms": {"qkv_proj": float(med[0]), "sdpa": float(med[1]),
-                                           "out_proj": float(med[2]),
-                                           "residual_layernorm": float(med[3])},
+                                           "out_proj_layernorm": float(med[2] + med[3])},
                      "step_breakdown_note": "events recorded between the launches of one "
                                             "mha_layer_fwd_timed call (median over steps)",
                      "roofline": roof}
@@ -191,6 +193,10 @@ def measure_base_configs(lib, C, dev, stream, flush, steps, warmup, peaks):
                                  "us_stats": {k: v * 1e3 for k, v in st.items()},
                                  "flops_per_call": sdpa_flops(w, "none")}
     return out
+
+
+def hbm_peak() -> float:
+    return float(load_peaks()[0]["hbm_gbs"])
 
 
 def base_step_rooflines(lib, C, dev, sp, vp, w, t, kl, key_len, timeit_all, hbm_line,
@@ -239,16 +245,17 @@ def base_step_rooflines(lib, C, dev, sp, vp, w, t, kl, key_len, timeit_all, hbm_
         sp), "mha_sdpa_fwd"))
     res["sdpa"] = hbm_line("sdpa_fwd_bf16_kernel", sdpa_hbm_bytes(w, key_len), st)
     res["sdpa"]["tflops"] = sdpa_flops(w, w.mask, key_len) / (st["median"] * 1e-3) / 1e12
-    a_out = torch.empty((Mq, D), dtype=bf, device=dev)
-    st = timeit_all(lambda: C.check(lib.mha_linear_fwd(
-        Mq, D, D, C.MHA_BF16, vp(c), D, vp(t["W_o"]), vp(t["b_o"]), vp(a_out), D, sp),
-        "mha_linear_fwd"))
-    res["out_proj"] = tensor_line("gemm_bias_bf16_kernel", 2.0 * Mq * D * D, st)
     y = torch.empty((Mq, D), dtype=bf, device=dev)
-    st = timeit_all(lambda: C.check(lib.mha_residual_layernorm_fwd(
-        Mq, D, C.MHA_BF16, 1e-5, vp(t["x_q"]), vp(a_out), vp(t["gamma"]), vp(t["beta"]), vp(y),
-        sp), "mha_residual_layernorm_fwd"))
-    res["residual_layernorm"] = hbm_line("residual_layernorm_stream_kernel", 6.0 * Mq * D, st)
+    st = timeit_all(lambda: C.check(lib.mha_out_proj_layernorm_fwd(
+        Mq, D, D, C.MHA_BF16, 1e-5, vp(c), vp(t["W_o"]), vp(t["b_o"]), vp(t["x_q"]),
+        vp(t["gamma"]), vp(t["beta"]), vp(y), sp), "mha_out_proj_layernorm_fwd"))
+    res["out_proj_layernorm"] = tensor_line("gemm_ln_bf16_kernel (W^O + residual LayerNorm)",
+                                            2.0 * Mq * D * D, st)
+    # the same launch against HBM: C and x read, y written (bf16), W^O read once
+    nbytes = 2.0 * (3 * Mq * D + D * D)
+    res["out_proj_layernorm"]["hbm"] = {"achieved": nbytes / (st["median"] * 1e-3) / 1e9,
+                                        "frac": nbytes / (st["median"] * 1e-3) / 1e9 / hbm_peak(),
+                                        "algorithmic_bytes_per_launch": nbytes}
     return res
 
 
@@ -385,12 +392,12 @@ def measure_ffn(lib, C, dev, stream, flush, steps, warmup, peak):
                     f"tokens={M}, d_model={w.D}, d_ff={w.d_ff}",
         "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
         "flops_per_step": fl, "tokens_per_s": M / (ms * 1e-3),
-        "step_breakdown_ms": {"linear1_relu": g1, "linear2": float(per[:, 1].mean()),
-                              "residual_layernorm": float(per[:, 2].mean())},
+        "step_breakdown_ms": {"linear1_relu": g1,
+                              "linear2_layernorm": float(per[:, 1:3].sum(axis=1).mean())},
         "roofline": {"kernel": "gemm_bias_bf16_kernel (ReLU epilogue, first linear map)",
                      "bound": "tensor", "achieved": g1_tf, "peak": peak, "unit": "TFLOP/s",
                      "frac": g1_tf / peak, "algorithmic_flops_per_launch": fl / 2},
-        "gpu_launches_per_step": 3,
+        "gpu_launches_per_step": 2,
     }
 
 
@@ -438,7 +445,7 @@ def measure_encoder(lib, C, dev, stream, flush, steps, warmup):
                     f"sublayer, B={w.B}, n={w.Nq}, d_model={w.D}, h={w.H}, d_ff={wf.d_ff}",
         "value": fl / (step * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": step,
         "flops_per_step": fl, "tokens_per_s": w.B * w.Nq / (step * 1e-3),
-        "gpu_launches_per_step": 7,
+        "gpu_launches_per_step": 5,
     }
 
 
@@ -541,7 +548,7 @@ def measure_backward(lib, C, dev, stream, flush, steps, warmup, peak):
                           "what": "mha_layer_fwd_train (y, activations kept) then "
                                   "mha_layer_bwd_saved: the same FLOPs as the recomputing "
                                   "backward, plus y"},
-        "gpu_launches_per_step": {"attention": 3, "layer": 19, "training_step": 20},
+        "gpu_launches_per_step": {"attention": 3, "layer": 19, "training_step": 19},
     }
 
 
@@ -1003,11 +1010,10 @@ def run_ours(args):
         "pct_of_bf16_peak": 100.0 * value / world / peak,
         "layer_flops_per_step": fl_layer,
         "step_breakdown_ms": {"qkv_proj": float(per[:, 0].mean()), "sdpa": sdpa_ms,
-                              "out_proj": float(per[:, 2].mean()),
-                              "residual_layernorm": float(per[:, 3].mean())},
+                              "out_proj_layernorm": float(per[:, 2:4].sum(axis=1).mean())},
         "timing_ms": {"step": tstats(per.sum(axis=1)), "qkv_proj": tstats(per[:, 0]),
-                      "sdpa": tstats(per[:, 1]), "out_proj": tstats(per[:, 2]),
-                      "residual_layernorm": tstats(per[:, 3]),
+                      "sdpa": tstats(per[:, 1]),
+                      "out_proj_layernorm": tstats(per[:, 2:4].sum(axis=1)),
                       "causal_step": tstats(per_c.sum(axis=1)),
                       "causal_sdpa": tstats(per_c[:, 1]),
                       "note": "value, ms_per_step and the roofline use the means"},
@@ -1032,7 +1038,7 @@ def run_ours(args):
                            "ms_per_step": e2e_serial_ms},
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size()},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": LAYER_LAUNCHES * args.steps,
         "clocks": clocks,
         "ffn": ffn,
         "encoder_layer": encoder,
@@ -1108,6 +1114,15 @@ def run_profile_case(args):
         C.check(lib.mha_residual_layernorm_fwd(B * N, Dm, C.MHA_BF16, 1e-5, vp(x), vp(a_ln), None,
                                                None, vp(y_ln), sp), "mha_residual_layernorm_fwd")
 
+    # the W^O projection fused with the residual LayerNorm on the same rows
+    wo = (torch.randn((Dm, Dm), device=dev, generator=g) * 0.03).to(bf)
+    y_o = torch.empty_like(a_ln)
+
+    def out_proj_ln():
+        C.check(lib.mha_out_proj_layernorm_fwd(B * N, Dm, Dm, C.MHA_BF16, 1e-5, vp(a_ln), vp(wo),
+                                               None, vp(x), None, None, vp(y_o), sp),
+                "mha_out_proj_layernorm_fwd")
+
     def layer_bwd_case():
         # the whole sublayer backward of the big model at this batch (self-attention, no mask)
         import transformer_head_scaled_04_gb300 as mha_pkg
@@ -1128,8 +1143,8 @@ def run_profile_case(args):
         fn = layer_bwd_case()
     else:
         fwd()
-        fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv,
-              "layernorm": layernorm}[args.profile_case]
+        fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv, "layernorm": layernorm,
+              "out_proj_ln": out_proj_ln}[args.profile_case]
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -1155,7 +1170,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
     ap.add_argument("--profile-case",
-                    choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm", "layer_bwd"],
+                    choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm", "layer_bwd",
+                             "out_proj_ln"],
                     default=None,
                     help="run only this kernel family (for ncu captures), no bench line")
     ap.add_argument("--batch", type=int, default=4, help="batch of --profile-case")

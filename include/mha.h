@@ -425,6 +425,25 @@ int mha_encoder_layer_fwd(int B, int N, int H, int D, int d_ff, int dtype, int m
 int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x, const void* a,
                                const void* gamma, const void* beta, void* y, cudaStream_t stream);
 
+/*
+ * mha_out_proj_layernorm_fwd -- y = LayerNorm(x + C W_o^T + b_o) * gamma + beta: the W^O
+ * projection of the sublayer and its residual + post-norm step in one call ([LT] 3.2.2:
+ * MultiHead = Concat(head_1..head_h) W^O; [LT] 3.1: LayerNorm(x + Sublayer(x))).  This is what
+ * mha_layer_fwd runs after the attention step.
+ *   C [M,K] (the head concat), W_o [D,K] ([out,in]), b_o [D] or NULL, x and y [M,D], gamma /
+ *   beta [D] or NULL; all dense row-major, 16-byte aligned.
+ *   bf16 with D a multiple of 256 (at most 2048) and K a multiple of 64: one kernel, the
+ *   projection output never written to memory and never rounded (the residual sum is formed
+ *   in fp32; the two-step path rounds the projection to bf16 when it stores it).  Otherwise (fp32, or other widths with D a multiple of 8 up to 2048 and,
+ *   for bf16, D and K multiples of 64): the projection into y, then the LayerNorm in place.
+ *   Errors: MHA_ERR_INVALID (sizes < 1, NULL C / W_o / x / y, eps < 0 or NaN),
+ *   MHA_ERR_UNSUPPORTED (limits above, or not sm_103), MHA_ERR_ALIGN, MHA_ERR_CUDA.
+ */
+int mha_out_proj_layernorm_fwd(int M, int D, int K, int dtype, float eps, const void* C,
+                               const void* W_o, const void* b_o, const void* x,
+                               const void* gamma, const void* beta, void* y,
+                               cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mha_status_string(int status);
 

@@ -406,3 +406,23 @@ def test_layer_training_split_validation(lib):
     assert bwd(dy=None) == C.MHA_ERR_INVALID
     assert bwd(ws_bytes=need - 1) == C.MHA_ERR_WORKSPACE
     assert bwd(dy=ODD) == C.MHA_ERR_ALIGN
+
+
+def out_proj_ln(lib, M=4, D=256, K=256, dt=1, eps=1e-5, c=FAKE, w=FAKE, b=None, x=FAKE, y=FAKE):
+    return lib.mha_out_proj_layernorm_fwd(M, D, K, dt, eps, c, w, b, x, None, None, y, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=0), C.MHA_ERR_INVALID),
+    (dict(K=-1), C.MHA_ERR_INVALID),
+    (dict(dt=5), C.MHA_ERR_INVALID),
+    (dict(c=None), C.MHA_ERR_INVALID),
+    (dict(x=None), C.MHA_ERR_INVALID),
+    (dict(eps=float("nan")), C.MHA_ERR_INVALID),
+    (dict(D=2304), C.MHA_ERR_UNSUPPORTED),          # wider than 2048
+    (dict(D=100, dt=0), C.MHA_ERR_UNSUPPORTED),      # not a multiple of 8
+    (dict(K=96), C.MHA_ERR_UNSUPPORTED),             # bf16 K multiple of 64
+    (dict(b=ODD), C.MHA_ERR_ALIGN),
+])
+def test_out_proj_layernorm_validation(lib, kw, code):
+    assert out_proj_ln(lib, **kw) == code

@@ -6,6 +6,8 @@ Per-token gradients (dx_q, dx_kv) are held to the bf16 gradient bound at each to
 scale; parameter gradients, sums over all B*N tokens, to a bound that scales with the
 tensor's RMS (both derived in ``parity_util``).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -207,3 +209,34 @@ def test_layer_training_split_matches(name):
         mha.set_deterministic(before)
     compare_bf16({k: host(v) for k, v in fast.items()}, run_oracle(inp, dy, w),
                  f"training split {name}")
+
+
+def test_layer_training_split_big_model_rows():
+    """The big model's heads at 16384 rows, where the training forward computes y with the W^O
+    projection and the LayerNorm in one kernel that also keeps the projection for the
+    backward: y equals mha_layer_fwd's bitwise, and the backward from the saved activations
+    equals the recomputing backward bitwise (deterministic mode).  The recomputing backward
+    itself is held to the oracle by test_layer_backward_big_long_sampled_batches."""
+    w = dataclasses.replace(si.WORKLOADS["big_long_b8_n4096"], B=4)
+    inp = si.draw_layer(w, affine=True)
+    dy = draw_dy(w, 87, "bf16")
+    bf = torch.bfloat16
+    t = {k: to_dev(v, bf) for k, v in inp.items() if k != "key_len"}
+    args = (t["x_q"], t["x_kv"], t["W_qkv"], t["b_qkv"], t["W_o"], t["b_o"], t["gamma"],
+            t["beta"], w.H)
+    kw = dict(mask="none", key_len=None, d_k=w.d_k, d_v=w.d_v)
+    tdy = to_dev(dy, bf)
+    y_ref = mha.mha_layer(*args, **kw)
+    before = mha.get_deterministic()
+    mha.set_deterministic(True)
+    try:
+        y, ws = mha.mha_layer_forward_train(*args, **kw)
+        assert torch.equal(y, y_ref)
+        full = mha.mha_layer_backward(*args, tdy, **kw)
+        saved = mha.mha_layer_backward(*args, tdy, workspace=ws, saved=True, **kw)
+        for k in PER_TOKEN + PARAMS:
+            if full[k] is not None:
+                assert torch.equal(full[k], saved[k]), k
+    finally:
+        mha.set_deterministic(before)
+    assert mha.device_status() == 0

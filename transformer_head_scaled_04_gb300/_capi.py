@@ -49,6 +49,7 @@ PROTOTYPES = {
     "mha_encoder_layer_fwd": (_c_int, [_c_int] * 7 + [_vp, _c_float] + [_vp] * 15
                               + [_size, _vp]),
     "mha_residual_layernorm_fwd": (_c_int, [_c_int] * 3 + [_c_float] + [_vp] * 6),
+    "mha_out_proj_layernorm_fwd": (_c_int, [_c_int] * 4 + [_c_float] + [_vp] * 8),
     "mha_status_string": (ctypes.c_char_p, [_c_int]),
     "mha_set_deterministic": (_c_int, [_c_int]),
     "mha_get_deterministic": (_c_int, []),

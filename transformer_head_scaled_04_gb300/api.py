@@ -403,3 +403,19 @@ def wait_selftest(timeout_ns: int = 1_000_000) -> int:
     C.check(C.load().mha_debug_wait_selftest(int(timeout_ns), _stream(torch.cuda.current_device())),
             "mha_debug_wait_selftest")
     return device_status()
+
+
+def out_proj_layernorm(c, W_o, b_o, x, gamma=None, beta=None, eps=1e-5, out=None):
+    """y = LayerNorm(x + c W_o^T + b_o) * gamma + beta over the last axis via
+    ``mha_out_proj_layernorm_fwd`` (c [..., K], W_o [D, K], x [..., D])."""
+    _cuda(c, W_o, b_o, x, gamma, beta, out)
+    D, K = W_o.shape
+    M = x.numel() // D
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        code = C.load().mha_out_proj_layernorm_fwd(M, D, K, _dt(x), float(eps), _ptr(c),
+                                                   _ptr(W_o), _ptr(b_o), _ptr(x), _ptr(gamma),
+                                                   _ptr(beta), _ptr(out), _stream(x.device))
+    C.check(code, "mha_out_proj_layernorm_fwd")
+    return out

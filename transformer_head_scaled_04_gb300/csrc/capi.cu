@@ -196,6 +196,16 @@ bool map_dq_acc_f32(CUtensorMap* m, const void* base, int B, int H, int rows) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The sublayer's last two steps as one kernel (W^O fused with the residual LayerNorm) pay off
+// only when each cluster of the fused kernel gets several 128-row tiles and the projection is
+// short: on the big model's attention sublayer (32768 rows, K = 1024) the whole sublayer is
+// ~1% faster, on the base model's (4096 rows, K = 512; one tile per cluster) 10% slower, and
+// on the feed-forward sublayer's second map (K = 4096) no faster; elsewhere the projection
+// and the LayerNorm run as two launches.
+bool use_fused_out_ln(int dtype, int M, int D, int K) {
+  return dtype == MHA_BF16 && mha::gemm_ln_bf16_supported(D, K) && M >= 16384 && K <= 2048;
+}
+
 // mha_set_deterministic: the bf16 attention backward's dQ by its own kernel (bitwise
 // reproducible) instead of fp32 bulk reductions in whatever order the key tiles finish
 std::atomic<int> g_deterministic{0};
@@ -790,9 +800,20 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   mark(1);
   st = run_sdpa(a, dtype, ctx, stream);
   if (st != MHA_OK) return st;
+  mark(2);
+  if (use_fused_out_ln(dtype, Mq, D, nv)) {
+    // y = LayerNorm(x_q + C W_o^T + b_o) in one kernel: A stays on chip
+    CUtensorMap tmC, tmWo;
+    if (!map_2d_bf16(&tmC, C, nv, Mq, nv, 128) || !map_2d_bf16(&tmWo, W_o, nv, D, nv, 256))
+      return MHA_ERR_CUDA;
+    const cudaError_t e = mha::launch_gemm_ln_bf16(tmC, tmWo, b_o, x_q, gamma, beta, y, Mq, D,
+                                                   nv, ln_eps, ctx, stream);
+    mark(3);
+    mark(4);
+    return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
   // A = C W_o^T + b_o
   uint8_t* A = ws + plan.off_a;
-  mark(2);
   st = run_linear(Mq, D, nv, dtype, C, nv, W_o, b_o, A, D, ctx, stream);
   if (st != MHA_OK) return st;
   // y = LayerNorm(x_q + A)
@@ -835,6 +856,17 @@ int ffn_impl(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, con
   st = run_linear(M, d_ff, D, dtype, x, D, W1, b1, Hb, d_ff, ctx, stream, /*relu=*/true);
   if (st != MHA_OK) return st;
   mark(1);
+  if (use_fused_out_ln(dtype, M, D, d_ff)) {
+    // y = LayerNorm(x + H W2^T + b2) in one kernel: FFN(x) stays on chip
+    CUtensorMap tmH, tmW2;
+    if (!map_2d_bf16(&tmH, Hb, d_ff, M, d_ff, 128) || !map_2d_bf16(&tmW2, W2, d_ff, D, d_ff, 256))
+      return MHA_ERR_CUDA;
+    const cudaError_t e = mha::launch_gemm_ln_bf16(tmH, tmW2, b2, x, gamma, beta, y, M, D, d_ff,
+                                                   ln_eps, ctx, stream);
+    mark(2);
+    mark(3);
+    return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
   // F = H W2^T + b2
   st = run_linear(M, D, d_ff, dtype, Hb, d_ff, W2, b2, F, D, ctx, stream);
   if (st != MHA_OK) return st;
@@ -997,6 +1029,38 @@ int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x
   const int st = device_ctx(&ctx);
   if (st != MHA_OK) return st;
   cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, eps, x, a, gamma, beta, y, ctx, stream);
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+int mha_out_proj_layernorm_fwd(int M, int D, int K, int dtype, float eps, const void* C,
+                               const void* W_o, const void* b_o, const void* x,
+                               const void* gamma, const void* beta, void* y,
+                               cudaStream_t stream) {
+  if (M < 1 || D < 1 || K < 1 || !valid_dtype(dtype)) return MHA_ERR_INVALID;
+  if (C == nullptr || W_o == nullptr || x == nullptr || y == nullptr) return MHA_ERR_INVALID;
+  if (std::isnan(eps) || eps < 0.f) return MHA_ERR_INVALID;
+  if (D % 8 != 0 || D > 2048 || M > (1 << 24)) return MHA_ERR_UNSUPPORTED;
+  if (dtype == MHA_BF16 && (D % 64 != 0 || K % 64 != 0)) return MHA_ERR_UNSUPPORTED;
+  const void* all[] = {C, W_o, b_o, x, gamma, beta, y};
+  for (const void* p : all)
+    if (p != nullptr && !aligned(p, 16)) return MHA_ERR_ALIGN;
+  DevCtx ctx;
+  int st = device_ctx(&ctx);
+  if (st != MHA_OK) return st;
+  if (dtype == MHA_BF16 && mha::gemm_ln_bf16_supported(D, K)) {
+    CUtensorMap tmC, tmWo;
+    if (!map_2d_bf16(&tmC, C, K, M, K, 128) || !map_2d_bf16(&tmWo, W_o, K, D, K, 256))
+      return MHA_ERR_CUDA;
+    const cudaError_t e = mha::launch_gemm_ln_bf16(tmC, tmWo, b_o, x, gamma, beta, y, M, D, K,
+                                                   eps, ctx, stream);
+    return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
+  // two launches: the projection into y, then the LayerNorm reads it back in place (each row
+  // is read whole before it is written)
+  st = run_linear(M, D, K, dtype, C, K, W_o, b_o, y, D, ctx, stream);
+  if (st != MHA_OK) return st;
+  const cudaError_t e =
+      mha::launch_residual_layernorm(dtype, M, D, eps, x, y, gamma, beta, y, ctx, stream);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
@@ -1196,6 +1260,17 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
   }
   a.O = W(pl.off_c);
   a.lse = static_cast<float*>(W(pl.off_lse));
+  if (phase == kLayerFwdTrain && use_fused_out_ln(dtype, Mq, D, nv)) {
+    // y exactly as mha_layer_fwd computes it (W^O and LayerNorm in one kernel), which also
+    // keeps the projection output A in bf16 for the backward
+    MHA_TRY(run_sdpa(a, dtype, ctx, stream));
+    CUtensorMap tmC, tmWo;
+    if (!map_2d_bf16(&tmC, W(pl.off_c), nv, Mq, nv, 128) ||
+        !map_2d_bf16(&tmWo, W_o, nv, D, nv, 256))
+      return MHA_ERR_CUDA;
+    return ok(mha::launch_gemm_ln_bf16(tmC, tmWo, b_o, x_q, gamma, beta, y, Mq, D, nv, ln_eps,
+                                       ctx, stream, W(pl.off_a)));
+  }
   if (phase != kLayerBwdSaved) {
     MHA_TRY(run_sdpa(a, dtype, ctx, stream));
     MHA_TRY(run_linear(Mq, D, nv, dtype, W(pl.off_c), nv, W_o, b_o, W(pl.off_a), D, ctx,

@@ -131,6 +131,10 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
+// Ask L2 to fetch the 128-byte line holding `addr` ahead of use.
+__device__ __forceinline__ void prefetch_global_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(addr)) : "memory");
+}
 // Ask L2 to fetch `bytes` (a multiple of 16; 16-byte aligned) from global memory ahead of use.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
@@ -234,6 +238,86 @@ __device__ __forceinline__ int launch_cancel_result(uint32_t resp) {
       : "memory");
   if (!ok) return -1;
   return static_cast<int>(cx + gridDim.x * (cy + gridDim.y * cz));
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+// This CTA's rank in its cluster, the cluster's index in the grid and the number of clusters
+// (x dimension; the kernels here use 1-D clusters and grids).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// The address in the cluster's shared window of the same variable in CTA `rank`'s memory.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b)
+               : "memory");
+}
+__device__ __forceinline__ float2 ld_shared_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+// Asynchronous store of two floats into the shared memory of a CTA of the cluster (addresses
+// from mapa_shared); the write completes 8 bytes of the transaction count of `bar`, an
+// mbarrier in that same CTA.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+      ::"r"(addr), "f"(a), "f"(b), "r"(bar)
+      : "memory");
+}
+// Named barrier among `count` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Arrive on an mbarrier of any CTA of the cluster (address from mapa_shared), releasing this
+// thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+// Bounded wait on a local mbarrier whose arrivals come from other CTAs of the cluster
+// (acquire at cluster scope, so their writes before the arrival are visible afterwards).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+  auto test = [&]() {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+  };
+  if (test()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (test()) return true;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+// Every thread of every CTA of the cluster arrives and waits (all threads must execute it;
+// the non-.aligned forms let the lanes of a warp arrive at different times).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 / TMEM

@@ -73,6 +73,17 @@ cudaError_t launch_gemm_bf16_splitk(const CUtensorMap& tmX, const CUtensorMap& t
                                     const CUtensorMap& tmAcc, float* acc, int ksplit, void* Y,
                                     int M, int N, int K, int64_t ldy, const DevCtx& ctx,
                                     cudaStream_t s);
+// ---- W^O projection fused with the residual + LayerNorm of the sublayer (bf16):
+// y = LayerNorm(x + C W^T + bias) * gamma + beta for C [M, K], W [D, K], x and y [M, D]
+// (row pitch D).  tmX: 2-D map over C {K, M}, box {64, 128}; tmW: over W {K, D}, box {64, 256};
+// both 128-byte swizzled.  Needs D a multiple of 256 up to 2048 and K a multiple of 64
+// (gemm_ln_bf16_supported).  a_out: optional [M, D] (row pitch D) that also receives the
+// projection output bf16(C W^T + bias).
+bool gemm_ln_bf16_supported(int D, int K);
+cudaError_t launch_gemm_ln_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                const void* bias, const void* x, const void* gamma,
+                                const void* beta, void* y, int M, int D, int K, float eps,
+                                const DevCtx& ctx, cudaStream_t s, void* a_out = nullptr);
 cudaError_t launch_gemm_f32(const float* X, int64_t ldx, const float* W, const float* bias,
                             bool relu, float* Y, int64_t ldy, int M, int N, int K,
                             cudaStream_t s, const float* residual = nullptr);
