@@ -91,6 +91,49 @@ def test_sdpa_bf16(B, H, Nq, Nk, mask, kl):
                 assert np.all(host(O)[b] == 0.0)
 
 
+# Query sequences of at most 128 rows (a single query tile per head; the base model's encoder
+# and cross-attention shapes), over odd numbers of heads, with every mask; with key padding
+# some batch elements see no key at all next to ones that see many, and the log-sum-exp is
+# checked too (+inf exactly where a row sees no key).
+SHORT_Q_CASES = [
+    (3, 5, 128, 128, "none", None),
+    (1, 7, 128, 128, "causal", None),
+    (5, 3, 128, 256, "key_padding", [0, 256, 1, 129, 0]),
+    (2, 3, 77, 300, "none", None),
+    (3, 1, 100, 100, "causal", None),
+    (4, 1, 1, 5, "key_padding", [5, 0, 3, 1]),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,mask,kl", SHORT_Q_CASES)
+def test_sdpa_bf16_short_queries(B, H, Nq, Nk, mask, kl):
+    Q, K, V, _ = si.draw_sdpa(B, H, Nq, Nk, dtype="bf16", seed=500 + B * H + Nq + Nk)
+    key_len = np.array(kl, np.int32) if kl is not None else None
+    O, lse = mha.sdpa_with_lse(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16),
+                               to_dev(V, torch.bfloat16), mask, to_dev(key_len, torch.int32))
+    ref = oracle.sdpa_ref(Q, K, V, mask, key_len)
+    assert_bf16_close(host(O), ref, f"sdpa bf16 short queries {B}x{H} {Nq}x{Nk} {mask}")
+    lse_ref = oracle.sdpa_lse_ref(Q, K, mask, key_len)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(host(lse)), fin)
+    assert np.allclose(host(lse)[fin], lse_ref[fin], rtol=0, atol=2e-3)
+    if key_len is not None:
+        for b, L in enumerate(kl):
+            if L == 0:
+                assert np.all(host(O)[b] == 0.0)
+
+
+def test_sdpa_bf16_short_queries_more_heads_than_sms():
+    """More (b, h) than SMs with a single ragged query tile each (persistent blocks take over
+    blocks that have not started)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, H, N = 2, sms + 5, 90
+    Q, K, V, _ = si.draw_sdpa(B, H, N, N, dtype="bf16", seed=4343)
+    O = mha.sdpa(to_dev(Q, torch.bfloat16), to_dev(K, torch.bfloat16), to_dev(V, torch.bfloat16),
+                 "none")
+    assert_bf16_close(host(O), oracle.sdpa_ref(Q, K, V, "none"), f"sdpa bf16 short queries {H} heads")
+
+
 @pytest.mark.parametrize("mask", ["none", "causal"])
 def test_sdpa_bf16_more_blocks_than_sms(mask):
     """More 256-row query blocks than SMs, with a short last round, so that persistent blocks
