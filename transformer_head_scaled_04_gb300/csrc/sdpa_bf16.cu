@@ -636,7 +636,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[(static_cast<int64_t>(w.b) * p.H + w.h) * p.Nq + row] =
             (ok && l > 0.f) ? (m_used * c + log2f(l)) * 0.6931471805599453f : INFINITY;
       const int wrow0 = w.q0 + t * kBQ + quarter * 32;
-      if (w.nmax() > 0) {
+      if (w.nmax() > 0 && w.q0 + t * kBQ >= p.Nq) {
+        // This query tile has no rows (a sequence of at most 128 queries, or the last block of
+        // a ragged one): nothing to store.  Its warps wait on nothing else of the unit, so they
+        // could run two units ahead of the other tile and release the Q buffer into its
+        // previous use, which the other tile may still be staging O in.  Waiting for this
+        // unit's Q to land first puts the release into this unit's use: the producer loads
+        // that Q only once the buffer's previous use has been released.
+        const int qb = it & 1;
+        if (lane == 0) {
+          if (!mbar_wait(bar(kBarQ + qb), (it >> 1) & 1, p.timeout_ns)) {
+            record_error(p.status, kErrTimeout, kSiteEpilogue);
+            ok = false;
+          }
+          mbar_arrive(bar(kBarQEmpty + qb));
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        ++it;
+      } else if (w.nmax() > 0) {
         // O / l in bf16 -> this warp's 32 rows of the unit's Q buffer, which every S product
         // of the unit has read by now (128-byte swizzle: 16-byte chunk c of row r at chunk
         // c ^ (r % 8), conflict-free) -> one bulk tensor store per warp, which writes only the
