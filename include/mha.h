@@ -50,7 +50,9 @@ typedef enum {
   MHA_ERR_ALIGN = -3,          /* pointer or stride not aligned as the kernel requires */
   MHA_ERR_WORKSPACE = -4,      /* workspace missing or smaller than the matching *_workspace_size() */
   MHA_ERR_CUDA = -5,           /* a CUDA runtime/driver call or a launch failed */
-  MHA_ERR_DEVICE_TIMEOUT = -6  /* a device-side bounded wait ran out (see mha_debug_*) */
+  MHA_ERR_DEVICE_TIMEOUT = -6, /* a device-side bounded wait ran out (see mha_debug_*) */
+  MHA_ERR_DEVICE_BOUNDS = -7   /* a kernel of the MHA_DEBUG_BOUNDS build (libmha_debug.so)
+                                  computed an index outside a buffer; the access was skipped */
 } mha_status;
 
 typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;

@@ -5,6 +5,8 @@ import ctypes
 import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmha.so")
+# the same ABI with the kernels' index checks compiled in (built by build(debug_bounds=True))
+DEBUG_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmha_debug.so")
 
 # mirrors of the enums in include/mha.h
 MHA_OK = 0
@@ -14,6 +16,7 @@ MHA_ERR_ALIGN = -3
 MHA_ERR_WORKSPACE = -4
 MHA_ERR_CUDA = -5
 MHA_ERR_DEVICE_TIMEOUT = -6
+MHA_ERR_DEVICE_BOUNDS = -7
 MHA_F32 = 0
 MHA_BF16 = 1
 MASKS = {"none": 0, "causal": 1, "key_padding": 2}
@@ -77,6 +80,26 @@ def load() -> ctypes.CDLL:
             fn.argtypes = args
         _lib = lib
     return _lib
+
+
+_debug_lib = None
+
+
+def load_debug() -> ctypes.CDLL:
+    """Load libmha_debug.so, the index-checking build of the same ABI (fails loudly if it was
+    never built)."""
+    global _debug_lib
+    if _debug_lib is None:
+        if not os.path.exists(DEBUG_LIB_PATH):
+            raise RuntimeError(f"{DEBUG_LIB_PATH} is missing: build it first with "
+                               "`python -m transformer_head_scaled_04_gb300.build --debug-bounds`")
+        lib = ctypes.CDLL(DEBUG_LIB_PATH)
+        for name, (res, args) in PROTOTYPES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _debug_lib = lib
+    return _debug_lib
 
 
 def status_string(code: int) -> str:

@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmha.so")
+# the same library with the kernels' index checks compiled in (-DMHA_DEBUG_BOUNDS)
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libmha_debug.so")
 
 SOURCES = ["capi.cu", "gemm_bf16.cu", "gemm_f32.cu", "sdpa_bf16.cu", "sdpa_f32.cu",
            "sdpa_decode.cu", "sdpa_bwd_f32.cu", "sdpa_bwd_bf16.cu", "bwd_util.cu", "layernorm.cu",
@@ -44,23 +47,29 @@ def _inputs() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every translation unit and link libmha.so; returns the library path."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          debug_bounds: bool = False) -> str:
+    """Compile every translation unit and link libmha.so (libmha_debug.so, the kernels' index
+    checks compiled in, with debug_bounds); returns the library path."""
+    lib_path = DEBUG_LIB_PATH if debug_bounds else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug_bounds else BUILD_DIR
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH + NVCC_FLAGS + list(extra_flags or [])
+    if debug_bounds:
+        flags.append("-DMHA_DEBUG_BOUNDS")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -73,14 +82,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -12,9 +12,26 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "mha.h"
 #include "device_common.cuh"
 #include "launchers.h"
+
+// An NVTX range over the rest of the scope: every public entry point that launches work and
+// every step inside it (projection, attention, ...) shows up by name in a profiler's timeline;
+// without a profiler attached the calls return at once.
+namespace {
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
+#define MHA_NVTX_CAT2(a, b) a##b
+#define MHA_NVTX_CAT(a, b) MHA_NVTX_CAT2(a, b)
+#define MHA_NVTX_RANGE(name) NvtxRange MHA_NVTX_CAT(nvtx_range_, __LINE__)(name)
 
 namespace {
 
@@ -214,6 +231,7 @@ std::atomic<int> g_deterministic{0};
 int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
                const void* bias, void* Y, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                bool relu = false, const void* residual = nullptr) {
+  MHA_NVTX_RANGE("linear");
   cudaError_t e;
   if (dtype == MHA_BF16) {
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);
@@ -259,6 +277,7 @@ int wgrad_ksplit(int M, int N, int K, int num_sms) {
 int run_linear_wgrad(int M, int N, int K, int dtype, const void* A_st, int64_t lda,
                      const void* B_st, int64_t ldb, void* Y, int64_t ldy, float* acc, void* At,
                      void* Bt, int Kpad, const DevCtx& ctx, cudaStream_t s) {
+  MHA_NVTX_RANGE("linear_weight_gradient");
   if (dtype != MHA_BF16) {
     if (mha::launch_transpose(dtype, A_st, lda, K, M, At, Kpad, Kpad, s) != cudaSuccess ||
         mha::launch_transpose(dtype, B_st, ldb, K, N, Bt, Kpad, Kpad, s) != cudaSuccess)
@@ -283,6 +302,7 @@ int run_linear_wgrad(int M, int N, int K, int dtype, const void* A_st, int64_t l
 }
 
 int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t s) {
+  MHA_NVTX_RANGE("attention");
   cudaError_t e;
   if (dtype == MHA_BF16) {
     CUtensorMap tq, tk, tv, to;
@@ -293,13 +313,16 @@ int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t 
       return MHA_ERR_CUDA;
     e = mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
   } else {
-    e = mha::launch_sdpa_f32(a, s);
+    mha::SdpaArgs af = a;
+    af.status = ctx.status;
+    e = mha::launch_sdpa_f32(af, s);
   }
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
 // rowdot (D) and the gradient kernels of one attention backward; a.Dv is the caller's scratch
 int run_sdpa_bwd(mha::SdpaBwdArgs a, int dtype, const DevCtx& ctx, cudaStream_t s) {
+  MHA_NVTX_RANGE("attention_backward");
   a.deterministic = g_deterministic.load(std::memory_order_relaxed) != 0;
   cudaError_t e = mha::launch_sdpa_bwd_rowdot(a, dtype, s);
   if (e != cudaSuccess) return MHA_ERR_CUDA;
@@ -433,6 +456,8 @@ const char* mha_status_string(int st) {
     case MHA_ERR_WORKSPACE: return "MHA_ERR_WORKSPACE: workspace missing or too small";
     case MHA_ERR_CUDA: return "MHA_ERR_CUDA: CUDA call or launch failed";
     case MHA_ERR_DEVICE_TIMEOUT: return "MHA_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+    case MHA_ERR_DEVICE_BOUNDS:
+      return "MHA_ERR_DEVICE_BOUNDS: a kernel index fell outside its buffer (debug build)";
     default: return "unknown mha status";
   }
 }
@@ -505,6 +530,7 @@ extern "C" {
 int mha_sdpa_fwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int mask,
                  const int32_t* key_len, float scale, const void* Q, const void* K, const void* V,
                  void* O, const int64_t* strides, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_sdpa_fwd");
   if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
   return sdpa_entry(B, H, Nq, Nk, d_k, d_v, dtype, mask, key_len, 0, scale, Q, K, V, O, strides,
                     stream);
@@ -525,6 +551,7 @@ int mha_sdpa_decode_fwd(int B, int H, int Nq, int Lmax, int d_k, int d_v, int dt
                         const int32_t* cache_len, float scale, const void* Q, const void* K,
                         const void* V, void* O, const int64_t* strides, void* workspace,
                         size_t ws_bytes, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_sdpa_decode_fwd");
   if (B < 1 || H < 1 || Nq < 1 || Lmax < 1 || d_k < 1 || d_v < 1 || !valid_dtype(dtype))
     return MHA_ERR_INVALID;
   if ((causal != 0 && causal != 1) || Nq > Lmax) return MHA_ERR_INVALID;
@@ -602,6 +629,7 @@ int mha_sdpa_fwd_lse(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, 
                      const int32_t* key_len, float scale, const void* Q, const void* K,
                      const void* V, void* O, const int64_t* strides, float* lse,
                      cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_sdpa_fwd_lse");
   if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING || lse == nullptr)
     return MHA_ERR_INVALID;
   return sdpa_entry(B, H, Nq, Nk, d_k, d_v, dtype, mask, key_len, 0, scale, Q, K, V, O, strides,
@@ -620,6 +648,7 @@ int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
                  const void* V, const void* O, const void* dO, const float* lse, void* dQ,
                  void* dK, void* dV, const int64_t* strides, void* workspace, size_t ws_bytes,
                  cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_sdpa_bwd");
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d_k < 1 || d_v < 1 || !valid_dtype(dtype))
     return MHA_ERR_INVALID;
   if (mask < MHA_MASK_NONE || mask > MHA_MASK_KEY_PADDING) return MHA_ERR_INVALID;
@@ -682,6 +711,7 @@ int mha_sdpa_bwd(int B, int H, int Nq, int Nk, int d_k, int d_v, int dtype, int 
 int mha_sdpa_window_fwd(int B, int H, int N, int d_k, int d_v, int dtype, int window,
                         float scale, const void* Q, const void* K, const void* V, void* O,
                         const int64_t* strides, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_sdpa_window_fwd");
   return sdpa_entry(B, H, N, N, d_k, d_v, dtype, mha::kMaskWindow, nullptr, window, scale, Q, K,
                     V, O, strides, stream);
 }
@@ -803,6 +833,7 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   mark(2);
   if (use_fused_out_ln(dtype, Mq, D, nv)) {
     // y = LayerNorm(x_q + C W_o^T + b_o) in one kernel: A stays on chip
+    MHA_NVTX_RANGE("out_projection_layernorm");
     CUtensorMap tmC, tmWo;
     if (!map_2d_bf16(&tmC, C, nv, Mq, nv, 128) || !map_2d_bf16(&tmWo, W_o, nv, D, nv, 256))
       return MHA_ERR_CUDA;
@@ -818,6 +849,7 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   if (st != MHA_OK) return st;
   // y = LayerNorm(x_q + A)
   mark(3);
+  MHA_NVTX_RANGE("residual_layernorm");
   cudaError_t e =
       mha::launch_residual_layernorm(dtype, Mq, D, ln_eps, x_q, A, gamma, beta, y, ctx, stream);
   mark(4);
@@ -858,6 +890,7 @@ int ffn_impl(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, con
   mark(1);
   if (use_fused_out_ln(dtype, M, D, d_ff)) {
     // y = LayerNorm(x + H W2^T + b2) in one kernel: FFN(x) stays on chip
+    MHA_NVTX_RANGE("linear2_layernorm");
     CUtensorMap tmH, tmW2;
     if (!map_2d_bf16(&tmH, Hb, d_ff, M, d_ff, 128) || !map_2d_bf16(&tmW2, W2, d_ff, D, d_ff, 256))
       return MHA_ERR_CUDA;
@@ -872,6 +905,7 @@ int ffn_impl(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, con
   if (st != MHA_OK) return st;
   mark(2);
   // y = LayerNorm(x + F)
+  MHA_NVTX_RANGE("residual_layernorm");
   cudaError_t e = mha::launch_residual_layernorm(dtype, M, D, ln_eps, x, F, gamma, beta, y, ctx, stream);
   mark(3);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
@@ -885,6 +919,7 @@ int mha_layer_fwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
                   const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
                   const void* gamma, const void* beta, void* y, void* workspace,
                   size_t ws_bytes, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_layer_fwd");
   return layer_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv, W_qkv,
                     b_qkv, W_o, b_o, gamma, beta, y, workspace, ws_bytes, stream, nullptr);
 }
@@ -895,6 +930,7 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         const void* b_o, const void* gamma, const void* beta, void* y,
                         void* workspace, size_t ws_bytes, cudaStream_t stream,
                         const cudaEvent_t* events, int n_events) {
+  MHA_NVTX_RANGE("mha_layer_fwd_timed");
   if (events == nullptr || n_events < 5) return MHA_ERR_INVALID;
   for (int i = 0; i < 5; ++i)
     if (events[i] == nullptr) return MHA_ERR_INVALID;
@@ -904,6 +940,7 @@ int mha_layer_fwd_timed(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
 
 int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, const void* W,
                    const void* bias, void* Y, int64_t ldy, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_linear_fwd");
   const int st = check_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy);
   if (st != MHA_OK) return st;
   DevCtx ctx;
@@ -941,6 +978,7 @@ extern "C" {
 int mha_linear_relu_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx,
                         const void* W, const void* bias, void* Y, int64_t ldy,
                         cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_linear_relu_fwd");
   const int st = check_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy);
   if (st != MHA_OK) return st;
   DevCtx ctx;
@@ -961,6 +999,7 @@ int mha_ffn_fwd(int M, int D, int d_ff, int dtype, float ln_eps, const void* x, 
                 const void* b1, const void* W2, const void* b2, const void* gamma,
                 const void* beta, void* y, void* workspace, size_t ws_bytes,
                 cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_ffn_fwd");
   return ffn_impl(M, D, d_ff, dtype, ln_eps, x, W1, b1, W2, b2, gamma, beta, y, workspace,
                   ws_bytes, stream, nullptr);
 }
@@ -970,6 +1009,7 @@ int mha_ffn_fwd_timed(int M, int D, int d_ff, int dtype, float ln_eps, const voi
                       const void* gamma, const void* beta, void* y, void* workspace,
                       size_t ws_bytes, cudaStream_t stream, const cudaEvent_t* events,
                       int n_events) {
+  MHA_NVTX_RANGE("mha_ffn_fwd_timed");
   if (events == nullptr || n_events < 4) return MHA_ERR_INVALID;
   for (int i = 0; i < 4; ++i)
     if (events[i] == nullptr) return MHA_ERR_INVALID;
@@ -996,6 +1036,7 @@ int mha_encoder_layer_fwd(int B, int N, int H, int D, int d_ff, int dtype, int m
                           const void* W1, const void* b1, const void* W2, const void* b2,
                           const void* gamma2, const void* beta2, void* y, void* workspace,
                           size_t ws_bytes, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_encoder_layer_fwd");
   size_t need = 0;
   int st = mha_encoder_layer_workspace_size(B, N, H, D, d_ff, dtype, &need);
   if (st != MHA_OK) return st;
@@ -1018,6 +1059,7 @@ int mha_encoder_layer_fwd(int B, int N, int H, int D, int d_ff, int dtype, int m
 int mha_residual_layernorm_fwd(int M, int D, int dtype, float eps, const void* x, const void* a,
                                const void* gamma, const void* beta, void* y,
                                cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_residual_layernorm_fwd");
   if (M < 1 || D < 1 || !valid_dtype(dtype)) return MHA_ERR_INVALID;
   if (x == nullptr || a == nullptr || y == nullptr) return MHA_ERR_INVALID;
   if (std::isnan(eps) || eps < 0.f) return MHA_ERR_INVALID;
@@ -1036,6 +1078,7 @@ int mha_out_proj_layernorm_fwd(int M, int D, int K, int dtype, float eps, const 
                                const void* W_o, const void* b_o, const void* x,
                                const void* gamma, const void* beta, void* y,
                                cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_out_proj_layernorm_fwd");
   if (M < 1 || D < 1 || K < 1 || !valid_dtype(dtype)) return MHA_ERR_INVALID;
   if (C == nullptr || W_o == nullptr || x == nullptr || y == nullptr) return MHA_ERR_INVALID;
   if (std::isnan(eps) || eps < 0.f) return MHA_ERR_INVALID;
@@ -1087,6 +1130,7 @@ int mha_debug_last_device_status(cudaStream_t stream) {
 }
 
 int mha_debug_wait_selftest(int64_t timeout_ns, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_debug_wait_selftest");
   DevCtx ctx;
   const int st = device_ctx(&ctx);
   if (st != MHA_OK) return st;
@@ -1378,6 +1422,7 @@ int mha_layer_bwd(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dty
                   const void* gamma, const void* beta, const void* dy, void* dx_q, void* dx_kv,
                   void* dW_qkv, void* db_qkv, void* dW_o, void* db_o, void* dgamma, void* dbeta,
                   void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_layer_bwd");
   (void)beta;  // the output shift does not enter any gradient
   return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
                         W_qkv, b_qkv, W_o, b_o, gamma, dy, dx_q, dx_kv, dW_qkv, db_qkv, dW_o,
@@ -1389,6 +1434,7 @@ int mha_layer_fwd_train(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         const void* x_kv, const void* W_qkv, const void* b_qkv, const void* W_o,
                         const void* b_o, const void* gamma, const void* beta, void* y,
                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_layer_fwd_train");
   return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
                         W_qkv, b_qkv, W_o, b_o, gamma, nullptr, nullptr, nullptr, nullptr,
                         nullptr, nullptr, nullptr, nullptr, nullptr, workspace, ws_bytes, stream,
@@ -1402,6 +1448,7 @@ int mha_layer_bwd_saved(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         void* dx_q, void* dx_kv, void* dW_qkv, void* db_qkv, void* dW_o,
                         void* db_o, void* dgamma, void* dbeta, void* workspace, size_t ws_bytes,
                         cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_layer_bwd_saved");
   (void)beta;
   return layer_bwd_impl(B, H, Nq, Nk, D, d_k, d_v, dtype, mask, key_len, ln_eps, x_q, x_kv,
                         W_qkv, b_qkv, W_o, b_o, gamma, dy, dx_q, dx_kv, dW_qkv, db_qkv, dW_o,

@@ -24,6 +24,40 @@ __device__ __forceinline__ void record_error(int* status, int code, int site) {
   }
 }
 
+// ------------------------------------------------------------------ index checks
+// A build with MHA_DEBUG_BOUNDS defined checks the index of every plain (non-TMA) global load
+// and store the kernels make against the extent the kernel's own size arguments give that
+// buffer: an index outside records MHA_ERR_DEVICE_BOUNDS (-7) with the access's site id in
+// the status word and the access is skipped.  Nothing traps.  The normal build compiles the
+// checks away.  (Tensor-map copies need no check: the hardware clips them to the map.)
+#ifdef MHA_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+constexpr int kErrDeviceBounds = -7;
+
+__device__ __forceinline__ bool bounds_ok(int64_t i, int64_t n, int* status, int site) {
+  if constexpr (kDebugBounds) {
+    if (i < 0 || i >= n) {
+      record_error(status, kErrDeviceBounds, site);
+      return false;
+    }
+  }
+  return true;
+}
+// [i, i + len) inside [0, n)
+__device__ __forceinline__ bool span_ok(int64_t i, int64_t len, int64_t n, int* status,
+                                        int site) {
+  if constexpr (kDebugBounds) {
+    if (i < 0 || len < 0 || i + len > n) {
+      record_error(status, kErrDeviceBounds, site);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

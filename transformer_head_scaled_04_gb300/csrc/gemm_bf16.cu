@@ -42,7 +42,13 @@ constexpr int kBK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kThreads = 192;
 constexpr int kErrTimeout = -6;
 
-enum : int { kSiteGemmProducer = 11, kSiteGemmMma = 12, kSiteGemmEpilogue = 13 };
+enum : int {
+  kSiteGemmProducer = 11,
+  kSiteGemmMma = 12,
+  kSiteGemmEpilogue = 13,
+  kSiteGemmBias = 14,      // index checks (MHA_DEBUG_BOUNDS builds)
+  kSiteGemmResidual = 15
+};
 
 template <int BN>
 struct GemmShape {
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         float bv[64];
-        if (bias != nullptr) {
+        if (bias != nullptr && span_ok(col, 64, N, status, kSiteGemmBias)) {
           const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
@@ -272,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 64; ++i) bv[i] = 0.f;
         }
-        if (R != nullptr && row < M) {  // a residual matrix with Y's layout joins the bias
+        if (R != nullptr && row < M && span_ok(col, 64, N, status, kSiteGemmResidual)) {
+          // a residual matrix with Y's layout joins the bias
           const uint4* rp = reinterpret_cast<const uint4*>(R + static_cast<int64_t>(row) * ldy + col);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {

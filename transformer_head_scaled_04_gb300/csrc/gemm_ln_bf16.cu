@@ -57,7 +57,15 @@ constexpr int kBarBytes = 256;
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kMaxCluster = 8;
 
-enum : int { kSiteProducer = 41, kSiteMma = 42, kSiteEpilogue = 43, kSiteStats = 44 };
+enum : int {
+  kSiteProducer = 41,
+  kSiteMma = 42,
+  kSiteEpilogue = 43,
+  kSiteStats = 44,
+  kSiteVectors = 45,  // index checks (MHA_DEBUG_BOUNDS builds): b_o / gamma / beta
+  kSiteX = 46,        // x
+  kSiteOut = 47       // y and the optional projection output
+};
 
 // (sum, squared deviations) per row for each of the two accumulators in flight and each of the
 // 2 * CS column halves of the cluster; then b_o, gamma, beta for the CTA's columns (fp32)
@@ -234,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // b_o, gamma and beta of the CTA's 256 columns, once, as fp32
     for (int i = threadIdx.x - 64; i < kBN; i += kEpiWarps * 32) {
       const int col = n0 + i;
-      sVec[i] = p.bias ? __bfloat162float(p.bias[col]) : 0.f;
-      sVec[kBN + i] = p.gamma ? __bfloat162float(p.gamma[col]) : 1.f;
-      sVec[2 * kBN + i] = p.beta ? __bfloat162float(p.beta[col]) : 0.f;
+      const bool ok_col = bounds_ok(col, p.D, p.status, kSiteVectors);
+      sVec[i] = (p.bias && ok_col) ? __bfloat162float(p.bias[col]) : 0.f;
+      sVec[kBN + i] = (p.gamma && ok_col) ? __bfloat162float(p.gamma[col]) : 1.f;
+      sVec[2 * kBN + i] = (p.beta && ok_col) ? __bfloat162float(p.beta[col]) : 0.f;
     }
     named_bar_sync(1, kEpiWarps * 32);
     // ask L2 for this thread's 256 bytes of x in a tile (two 128-byte lines of its row)
@@ -269,8 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 1. r = x + (acc + b_o), back into TMEM; sum.  x is loaded two chunks ahead.
       uint4 xa[4], xb[4];
       auto load_x = [&](int c, uint4 (&dst)[4]) {
+        const bool ok_x = in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteX);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = in ? __ldg(xrow + c * 4 + v) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < 4; ++v) dst[v] = ok_x ? __ldg(xrow + c * 4 + v) : make_uint4(0, 0, 0, 0);
       };
       load_x(0, xa);
       load_x(1, xb);
@@ -289,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* bvec = sVec + c0 + c * 32;
         tmem_wait_ld();
         reg_fence(a);
-        if (p.a_out != nullptr && in) {
+        if (p.a_out != nullptr && in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteOut)) {
           uint4* ap = reinterpret_cast<uint4*>(p.a_out + static_cast<int64_t>(row) * p.D + n0 +
                                                c0 + c * 32);
 #pragma unroll
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty(buf));
         }
-        if (in) {
+        if (in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteOut)) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint32_t o[4];

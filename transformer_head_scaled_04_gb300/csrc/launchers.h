@@ -109,6 +109,7 @@ struct SdpaArgs {
   // optional: natural log of each row's softmax denominator, log sum_j exp(q.k_j * scale)
   // over the allowed keys (+inf for a row with none), fp32 [B, H, Nq] contiguous
   float* lse = nullptr;
+  int* status = nullptr;     // device status word (the f32 kernel's index checks)
 };
 // bf16: Q/K/V through 4-D TMA maps {d, n, h, b} with box {64, 128, 1, 1}, 128-byte swizzle;
 // O written through the same kind of map with box {64, 32, 1, 1} (one 32-row box per warp).

@@ -17,6 +17,7 @@ namespace mha {
 namespace {
 
 constexpr int kRowsPerBlock = 8;
+constexpr int kSiteLnCols = 31;  // index check (MHA_DEBUG_BOUNDS builds): a row's 8-column span
 
 template <typename T>
 struct Vec8;
@@ -58,7 +59,7 @@ template <typename T, int NIT>
 __global__ void __launch_bounds__(kRowsPerBlock * 32)
     residual_layernorm_kernel(const T* __restrict__ x, const T* __restrict__ a,
                               const T* __restrict__ gamma, const T* __restrict__ beta,
-                              T* __restrict__ y, int M, int D, float eps) {
+                              T* __restrict__ y, int M, int D, float eps, int* status) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   const int warp = threadIdx.x >> 5;
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
     const int col = (it * 32 + lane) * 8;
-    if (col < D) {
+    if (col < D && span_ok(col, 8, D, status, kSiteLnCols)) {
       float xv[8], av[8];
       Vec8<T>::load(x + base + col, xv);
       Vec8<T>::load(a + base + col, av);
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
     const int col = (it * 32 + lane) * 8;
-    if (col < D) {
+    if (col < D && span_ok(col, 8, D, status, kSiteLnCols)) {
       float g[8], bt[8], out[8];
       if (gamma) {
         Vec8<T>::load(gamma + col, g);
@@ -134,7 +135,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
                                      const __nv_bfloat16* __restrict__ a,
                                      const __nv_bfloat16* __restrict__ gamma,
                                      const __nv_bfloat16* __restrict__ beta,
-                                     __nv_bfloat16* __restrict__ y, int M, int D, float eps) {
+                                     __nv_bfloat16* __restrict__ y, int M, int D, float eps,
+                                     int* status) {
   const int lane = threadIdx.x & 31;
   const int W = gridDim.x * kRowsPerBlock;
   pdl_launch_dependents();
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int col = (it * 32 + lane) * 8;
-      if (col < D) {
+      if (col < D && span_ok(col, 8, D, status, kSiteLnCols)) {
         float xv[8], av[8];
         Vec8<__nv_bfloat16>::load(x + base + col, xv);
         Vec8<__nv_bfloat16>::load(a + base + col, av);
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int col = (it * 32 + lane) * 8;
-      if (col < D) {
+      if (col < D && span_ok(col, 8, D, status, kSiteLnCols)) {
         float g[8], bt[8], out[8];
         if (gamma) {
           Vec8<__nv_bfloat16>::load(gamma + col, g);
@@ -221,7 +223,7 @@ cudaError_t launch_stream(int M, int D, float eps, const void* x, const void* a,
                       static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(a),
                       static_cast<const __nv_bfloat16*>(gamma),
                       static_cast<const __nv_bfloat16*>(beta), static_cast<__nv_bfloat16*>(y),
-                      M, D, eps);
+                      M, D, eps, ctx.status);
   };
   switch ((D + 255) / 256) {
     case 1: return go(residual_layernorm_stream_kernel<1>);
@@ -237,14 +239,14 @@ cudaError_t launch_stream(int M, int D, float eps, const void* x, const void* a,
 
 template <typename T>
 cudaError_t launch_t(int M, int D, float eps, const void* x, const void* a, const void* gamma,
-                     const void* beta, void* y, cudaStream_t s) {
+                     const void* beta, void* y, int* status, cudaStream_t s) {
   const int nit = (D + 255) / 256;
   dim3 grid((M + kRowsPerBlock - 1) / kRowsPerBlock);
   dim3 block(kRowsPerBlock * 32);
   auto args = [&](auto kern) {
     (void)launch_pdl(kern, dim3(grid), dim3(block), 0, s, static_cast<const T*>(x), static_cast<const T*>(a),
                                 static_cast<const T*>(gamma), static_cast<const T*>(beta),
-                                static_cast<T*>(y), M, D, eps);
+                                static_cast<T*>(y), M, D, eps, status);
   };
   switch (nit) {
     case 1: args(residual_layernorm_kernel<T, 1>); break;
@@ -265,7 +267,7 @@ cudaError_t launch_residual_layernorm(int dtype, int M, int D, float eps, const 
                                       const void* a, const void* gamma, const void* beta,
                                       void* y, const DevCtx& ctx, cudaStream_t s) {
   if (dtype == 1) return launch_stream(M, D, eps, x, a, gamma, beta, y, ctx, s);
-  return launch_t<float>(M, D, eps, x, a, gamma, beta, y, s);
+  return launch_t<float>(M, D, eps, x, a, gamma, beta, y, ctx.status, s);
 }
 
 }  // namespace mha

@@ -93,7 +93,10 @@ enum : int {
   kSiteMma = 22,
   kSiteSoftmaxS = 23,
   kSiteSoftmaxO = 24,
-  kSiteEpilogue = 25
+  kSiteEpilogue = 25,
+  kSiteKeyLen = 26,    // index checks (MHA_DEBUG_BOUNDS builds)
+  kSiteLse = 27,
+  kSiteZeroRows = 28
 };
 
 // barrier indices
@@ -157,7 +160,8 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int lin) {
   }
   w.q0 = qblk * (2 * kBQ);
   w.L = p.Nk;
-  if (p.mask == 2) w.L = min(max(__ldg(p.key_len + w.b), 0), p.Nk);
+  if (p.mask == 2 && bounds_ok(w.b, p.B, p.status, kSiteKeyLen))
+    w.L = min(max(__ldg(p.key_len + w.b), 0), p.Nk);
   // Restricted attention: both query tiles walk the key tiles that the block's whole band
   // [q0 - window, last row + window] touches, starting at key tile kt0; rows mask the keys
   // outside their own band, so a tile can be fully masked for one of the two query tiles.
@@ -632,8 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (p.lse != nullptr && row < p.Nq)
-        p.lse[(static_cast<int64_t>(w.b) * p.H + w.h) * p.Nq + row] =
+      const int64_t lse_i = (static_cast<int64_t>(w.b) * p.H + w.h) * p.Nq + row;
+      if (p.lse != nullptr && row < p.Nq &&
+          bounds_ok(lse_i, static_cast<int64_t>(p.B) * p.H * p.Nq, p.status, kSiteLse))
+        p.lse[lse_i] =
             (ok && l > 0.f) ? (m_used * c + log2f(l)) * 0.6931471805599453f : INFINITY;
       const int wrow0 = w.q0 + t * kBQ + quarter * 32;
       if (w.nmax() > 0 && w.q0 + t * kBQ >= p.Nq) {
@@ -680,7 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(kBarQEmpty + qb));
         }
         ++it;
-      } else if (row < p.Nq) {  // a unit that sees no key: zero rows, stored directly
+      } else if (row < p.Nq && bounds_ok(w.b, p.B, p.status, kSiteZeroRows) &&
+                 bounds_ok(w.h, p.H, p.status, kSiteZeroRows)) {
+        // a unit that sees no key: zero rows, stored directly
         uint4* d4 = reinterpret_cast<uint4*>(p.O + static_cast<int64_t>(w.b) * p.so_b +
                                              static_cast<int64_t>(w.h) * p.so_h +
                                              static_cast<int64_t>(row) * p.so_n);

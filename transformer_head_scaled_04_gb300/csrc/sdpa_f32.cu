@@ -25,6 +25,8 @@ constexpr int kMaxD = 128;
 constexpr int kWarps = 8;
 constexpr int kChunk = 32;             // keys per shared-memory chunk
 constexpr int kPitch = kMaxD + 1;      // padded row pitch of a staged K / V row
+// index checks (MHA_DEBUG_BOUNDS builds)
+enum : int { kSiteF32KeyLen = 51, kSiteF32KV = 52, kSiteF32Lse = 53 };
 
 __global__ void __launch_bounds__(kWarps * 32)
     sdpa_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
@@ -33,7 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                     float scale, float* __restrict__ lse,
                     int64_t qb, int64_t qh, int64_t qn, int64_t qd, int64_t kb, int64_t kh,
                     int64_t kn, int64_t kd, int64_t vb, int64_t vh, int64_t vn, int64_t vd,
-                    int64_t ob, int64_t oh, int64_t on, int64_t od) {
+                    int64_t ob, int64_t oh, int64_t on, int64_t od, int* status) {
   pdl_launch_dependents();
   pdl_wait();  // the previous kernel's output is complete from here on
   __shared__ float sq[kWarps][kMaxD];
@@ -57,13 +59,15 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (mask == 1) {
       limit = r;
     } else if (mask == 2) {
-      limit = min(max(key_len[b], 0), Nk) - 1;
+      limit = bounds_ok(b, gridDim.z, status, kSiteF32KeyLen) ? min(max(key_len[b], 0), Nk) - 1
+                                                               : -1;
     } else if (mask == kMaskWindow) {
       limit = min(r + window, Nk - 1);
       first = max(r - window, 0);
     } else if (mask == kMaskCausalCache) {
       // the Nq queries are the newest of L cached positions: row r sits at L - Nq + r
-      const int L = min(max(key_len[b], 0), Nk);
+      const int L = bounds_ok(b, gridDim.z, status, kSiteF32KeyLen) ? min(max(key_len[b], 0), Nk)
+                                                                    : 0;
       limit = min(L - Nq + r, L - 1);
     } else {
       limit = Nk - 1;
@@ -91,11 +95,13 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int nj = min(kChunk, blk_limit + 1 - j0);
     for (int e = threadIdx.x; e < nj * d_k; e += kWarps * 32) {
       const int jj = e / d_k, t = e - jj * d_k;
-      sk[jj * kPitch + t] = kbase[static_cast<int64_t>(j0 + jj) * kn + t * kd];
+      if (bounds_ok(j0 + jj, Nk, status, kSiteF32KV))
+        sk[jj * kPitch + t] = kbase[static_cast<int64_t>(j0 + jj) * kn + t * kd];
     }
     for (int e = threadIdx.x; e < nj * d_v; e += kWarps * 32) {
       const int jj = e / d_v, t = e - jj * d_v;
-      sv[jj * kPitch + t] = vbase[static_cast<int64_t>(j0 + jj) * vn + t * vd];
+      if (bounds_ok(j0 + jj, Nk, status, kSiteF32KV))
+        sv[jj * kPitch + t] = vbase[static_cast<int64_t>(j0 + jj) * vn + t * vd];
     }
     __syncthreads();
     if (!live) continue;
@@ -130,8 +136,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   const bool any = m != -INFINITY && l > 0.f;
   const float inv = any ? 1.f / l : 0.f;  // no allowed key: zeros
-  if (lse != nullptr && lane == 0)
-    lse[(static_cast<int64_t>(b) * gridDim.y + h) * Nq + row] = any ? m + logf(l) : INFINITY;
+  const int64_t lse_i = (static_cast<int64_t>(b) * gridDim.y + h) * Nq + row;
+  if (lse != nullptr && lane == 0 &&
+      bounds_ok(lse_i, static_cast<int64_t>(gridDim.z) * gridDim.y * Nq, status, kSiteF32Lse))
+    lse[lse_i] = any ? m + logf(l) : INFINITY;
   float* o = O + b * ob + h * oh + static_cast<int64_t>(row) * on;
 #pragma unroll
   for (int i = 0; i < kMaxD / 32; ++i)
@@ -145,7 +153,7 @@ cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s) {
   (void)launch_pdl(sdpa_f32_kernel, dim3(grid), dim3(kWarps * 32), 0, s, static_cast<const float*>(a.Q), static_cast<const float*>(a.K),
       static_cast<const float*>(a.V), static_cast<float*>(a.O), a.Nq, a.Nk, a.d_k, a.d_v,
       a.mask, a.window, a.key_len, a.scale, a.lse, a.sq[0], a.sq[1], a.sq[2], a.sq[3], a.sk[0], a.sk[1], a.sk[2],
-      a.sk[3], a.sv[0], a.sv[1], a.sv[2], a.sv[3], a.so[0], a.so[1], a.so[2], a.so[3]);
+      a.sk[3], a.sv[0], a.sv[1], a.sv[2], a.sv[3], a.so[0], a.so[1], a.so[2], a.so[3], a.status);
   return cudaGetLastError();
 }
 
