@@ -304,6 +304,39 @@ int mha_layer_bwd_saved(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, i
                         cudaStream_t stream);
 
 /*
+ * mha_layer_host_workspace_size -- device workspace bytes mha_layer_fwd_host needs: two
+ * device buffers each for a slice's x and y, and mha_layer_fwd's workspace for one slice.
+ */
+int mha_layer_host_workspace_size(int B, int H, int N, int D, int d_k, int d_v, int dtype,
+                                  int chunks, size_t* bytes);
+
+/*
+ * mha_layer_fwd_host -- the self-attention sublayer y = LayerNorm(x + MultiHead(x, x, x))
+ * ([LT] 3.1, 3.2.2) with x and y in HOST memory (pinned memory lets the copies run
+ * asynchronously; pageable memory makes them synchronous).  The weights, biases, gamma, beta and
+ * key_len are device memory as for mha_layer_fwd.
+ *   x_host, y_host: [B, N, D] dense, row-major.  chunks: the batch is processed in
+ *   min(chunks, B) slices of ceil(B / chunks) sequences; slice i's x is copied in while slice
+ *   i-1 is computed on `stream` and slice i-2's y is copied back, so the copies hide behind
+ *   the computation except for the first slice's x and the last slice's y.
+ *   workspace: device, at least mha_layer_host_workspace_size(...) bytes, 256-byte aligned.
+ *   Each slice runs exactly as mha_layer_fwd on that slice (the results equal a per-slice
+ *   mha_layer_fwd bit for bit; a whole-batch call may round differently where it fuses the
+ *   W^O projection with the LayerNorm, which mha_layer_fwd does from 16384 rows on).
+ *   The call is asynchronous on `stream`: y_host is complete once `stream` has finished
+ *   everything queued up to this call.  The first call on a device creates two copy streams
+ *   and a few events for that device, kept until the process exits; calls for one device
+ *   from several host threads are serialised.  Errors: those of mha_layer_fwd for one slice
+ *   (checked before anything is queued), MHA_ERR_INVALID for NULL host pointers or chunks < 1,
+ *   MHA_ERR_WORKSPACE, MHA_ERR_ALIGN (workspace not 256-byte aligned), MHA_ERR_CUDA.
+ */
+int mha_layer_fwd_host(int B, int H, int N, int D, int d_k, int d_v, int dtype, int mask,
+                       const int32_t* key_len, float ln_eps, const void* x_host,
+                       const void* W_qkv, const void* b_qkv, const void* W_o, const void* b_o,
+                       const void* gamma, const void* beta, void* y_host, int chunks,
+                       void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * mha_layer_fwd_noalloc -- mha_layer_fwd for callers that cannot supply a workspace.
  * The pages have no counterpart: this is a packaging variant, not part of the method.
  *

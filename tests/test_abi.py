@@ -426,3 +426,39 @@ def out_proj_ln(lib, M=4, D=256, K=256, dt=1, eps=1e-5, c=FAKE, w=FAKE, b=None, 
 ])
 def test_out_proj_layernorm_validation(lib, kw, code):
     assert out_proj_ln(lib, **kw) == code
+
+
+def layer_host(lib, B=2, H=8, N=16, D=512, dt=1, mask=0, x=FAKE, y=FAKE, chunks=2, ws=FAKE,
+               ws_bytes=1 << 30, W_qkv=FAKE, W_o=FAKE):
+    return lib.mha_layer_fwd_host(B, H, N, D, 64, 64, dt, mask, None, 1e-5, x, W_qkv, None,
+                                  W_o, None, None, None, y, chunks, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), C.MHA_ERR_INVALID),
+    (dict(y=None), C.MHA_ERR_INVALID),
+    (dict(chunks=0), C.MHA_ERR_INVALID),
+    (dict(B=0), C.MHA_ERR_INVALID),
+    (dict(mask=2), C.MHA_ERR_INVALID),            # key padding needs key_len
+    (dict(W_o=None), C.MHA_ERR_INVALID),
+    (dict(D=520), C.MHA_ERR_UNSUPPORTED),
+    (dict(ws=None), C.MHA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), C.MHA_ERR_WORKSPACE),
+    (dict(ws=ctypes.c_void_p(0x10010)), C.MHA_ERR_ALIGN),   # 16- but not 256-byte aligned
+])
+def test_layer_host_validation(lib, kw, code):
+    assert layer_host(lib, **kw) == code
+
+
+def test_layer_host_workspace_size(lib):
+    n = ctypes.c_size_t(0)
+    # 8 sequences in 3 slices of 3: four slice buffers of 3 x 4096 x 1024 bf16 + the layer
+    # workspace of 3 sequences
+    assert lib.mha_layer_host_workspace_size(8, 16, 4096, 1024, 64, 64, 1, 3,
+                                             ctypes.byref(n)) == 0
+    slot = 3 * 4096 * 1024 * 2
+    m = ctypes.c_size_t(0)
+    assert lib.mha_layer_workspace_size(3, 16, 4096, 4096, 1024, 64, 64, 1, ctypes.byref(m)) == 0
+    assert n.value == 4 * slot + m.value
+    assert lib.mha_layer_host_workspace_size(8, 16, 4096, 1024, 64, 64, 1, 0,
+                                             ctypes.byref(n)) == C.MHA_ERR_INVALID

@@ -25,6 +25,7 @@ from .api import (  # noqa: F401
     mha_layer,
     mha_layer_backward,
     mha_layer_forward_train,
+    mha_layer_host,
     out_proj_layernorm,
     residual_layernorm,
     sdpa,

@@ -419,3 +419,35 @@ def out_proj_layernorm(c, W_o, b_o, x, gamma=None, beta=None, eps=1e-5, out=None
                                                    _ptr(beta), _ptr(out), _stream(x.device))
     C.check(code, "mha_out_proj_layernorm_fwd")
     return out
+
+
+def mha_layer_host(x_host, W_qkv, b_qkv, W_o, b_o, gamma, beta, H, mask="none", key_len=None,
+                   eps=1e-5, chunks=4, workspace=None, out=None, device=None):
+    """Self-attention sublayer on host tensors via ``mha_layer_fwd_host``: x_host [B,N,D] (CPU,
+    ideally pinned), weights on the CUDA device; returns y on the host (``out``, pinned, is
+    allocated if not given).  The copies in and out overlap the computation slice by slice;
+    the call returns once y is complete."""
+    _cuda(W_qkv, b_qkv, W_o, b_o, gamma, beta, key_len, workspace)
+    if x_host.is_cuda:
+        raise ValueError("x_host must be a host tensor")
+    dev = W_qkv.device if device is None else device
+    B, N, D = x_host.shape
+    x_host = x_host.contiguous()
+    if out is None:
+        out = torch.empty_like(x_host).pin_memory()
+    dt = _dt(x_host)
+    lib = C.load()
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        C.check(lib.mha_layer_host_workspace_size(B, H, N, D, D // H, D // H, dt, chunks,
+                                                  ctypes.byref(n)), "mha_layer_host_workspace_size")
+        workspace = torch.empty(max(n.value, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        code = lib.mha_layer_fwd_host(B, H, N, D, D // H, D // H, dt, C.MASKS[mask],
+                                      _ptr(key_len), float(eps), _ptr(x_host), _ptr(W_qkv),
+                                      _ptr(b_qkv), _ptr(W_o), _ptr(b_o), _ptr(gamma), _ptr(beta),
+                                      _ptr(out), int(chunks), _ptr(workspace), workspace.numel(),
+                                      _stream(dev))
+        C.check(code, "mha_layer_fwd_host")
+        torch.cuda.current_stream(dev).synchronize()
+    return out
