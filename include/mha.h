@@ -322,7 +322,7 @@ int mha_layer_host_workspace_size(int B, int H, int N, int D, int d_k, int d_v, 
  *   workspace: device, at least mha_layer_host_workspace_size(...) bytes, 256-byte aligned.
  *   Each slice runs exactly as mha_layer_fwd on that slice (the results equal a per-slice
  *   mha_layer_fwd bit for bit; a whole-batch call may round differently where it fuses the
- *   W^O projection with the LayerNorm, which mha_layer_fwd does from 16384 rows on).
+ *   W^O projection with the LayerNorm, which mha_layer_fwd does from 8192 rows on).
  *   The call is asynchronous on `stream`: y_host is complete once `stream` has finished
  *   everything queued up to this call.  The first call on a device creates two copy streams
  *   and a few events for that device, kept until the process exits; calls for one device

@@ -212,9 +212,10 @@ def test_layer_training_split_matches(name):
 
 
 def test_layer_training_split_big_model_rows():
-    """The big model's heads at 16384 rows, where the training forward computes y with the W^O
-    projection and the LayerNorm in one kernel that also keeps the projection for the
-    backward: y equals mha_layer_fwd's bitwise, and the backward from the saved activations
+    """The big model's heads at 16384 rows (the fused path starts at 8192), where the training
+    forward computes y with the W^O projection and the LayerNorm in one kernel that also keeps
+    the projection for the backward: y equals mha_layer_fwd's bitwise, and the backward from
+    the saved activations
     equals the recomputing backward bitwise (deterministic mode).  The recomputing backward
     itself is held to the oracle by test_layer_backward_big_long_sampled_batches."""
     w = dataclasses.replace(si.WORKLOADS["big_long_b8_n4096"], B=4)

@@ -72,7 +72,7 @@ def test_out_proj_layernorm_f32():
 
 @pytest.mark.gpu
 def test_out_proj_layernorm_matches_the_sublayer_path_bitwise():
-    """At 16384 rows and more, mha_layer_fwd runs this same kernel on its head-concat buffer:
+    """From 8192 rows on, mha_layer_fwd runs this same kernel on its head-concat buffer:
     the fused call on the sublayer's own concat (recomputed by the attention entry point)
     gives the same bits.  The big model's heads at half its batch."""
     w = dataclasses.replace(si.WORKLOADS["big_long_b8_n4096"], B=4)

@@ -214,13 +214,14 @@ bool map_dq_acc_f32(CUtensorMap* m, const void* base, int B, int H, int rows) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The sublayer's last two steps as one kernel (W^O fused with the residual LayerNorm) pay off
-// only when each cluster of the fused kernel gets several 128-row tiles and the projection is
-// short: on the big model's attention sublayer (32768 rows, K = 1024) the whole sublayer is
-// ~1% faster, on the base model's (4096 rows, K = 512; one tile per cluster) 10% slower, and
-// on the feed-forward sublayer's second map (K = 4096) no faster; elsewhere the projection
-// and the LayerNorm run as two launches.
+// once there are enough 128-row tiles for each cluster of the fused kernel to work through
+// several: same-box A/B of whole sublayers, 8192 rows (base model, causal, n = 256) 51.8 ->
+// 48.8 us, the big model's 32768 rows 0.703 -> 0.689 ms, the big FFN sublayer (K = 4096)
+// 375 -> 373 us; at 4096 rows (base model, n = 128) the fused launch is slower (38.6 -> 40.6
+// us sublayer, 33.4 -> 36.5 us FFN sublayer), so the projection and the LayerNorm stay two
+// launches there.
 bool use_fused_out_ln(int dtype, int M, int D, int K) {
-  return dtype == MHA_BF16 && mha::gemm_ln_bf16_supported(D, K) && M >= 16384 && K <= 2048;
+  return dtype == MHA_BF16 && mha::gemm_ln_bf16_supported(D, K) && M >= 8192;
 }
 
 // mha_set_deterministic: the bf16 attention backward's dQ by its own kernel (bitwise

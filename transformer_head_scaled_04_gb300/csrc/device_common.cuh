@@ -231,6 +231,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

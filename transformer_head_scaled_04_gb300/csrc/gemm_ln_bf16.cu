@@ -25,10 +25,15 @@
 //              3. mean and biased variance of the whole row by the exact combination of the
 //                 partial results (n = 128 values each: M2 = sum_i M2_i + n (mean_i - mean)^2),
 //                 then y = (r - mean) / sqrt(var + eps) * gamma + beta from r in TMEM, rounded
-//                 to bf16 and stored from registers (64 contiguous bytes of the row per thread
-//                 and chunk).  x for the next tile is requested into L2 at the start of a tile
-//                 and read two 32-column chunks ahead; b_o, gamma and beta sit in shared
-//                 memory as fp32; the elementwise arithmetic runs on fp32 pairs.
+//                 to bf16.  x and y move between global memory and the row-per-thread
+//                 registers through a 32-row x 32-column staging tile per warp, so that the
+//                 global accesses are coalesced (four lanes per 64-byte piece of a row, eight
+//                 rows per instruction); with each thread reading and writing its own row
+//                 directly, every 16-byte access of a warp touched 32 rows, and those accesses
+//                 took ~2.6 us (x) and ~3 us (y) of a tile's epilogue.  x for the next tile is
+//                 requested into L2 at the start of a tile and loaded two 32-column chunks
+//                 ahead; b_o, gamma and beta sit in shared memory as bf16; the elementwise
+//                 arithmetic runs on fp32 pairs.
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
 // in-flight copies and MMAs land, frees TMEM and returns.  All CTAs of a cluster meet at a
 // cluster barrier before they exit, so no CTA leaves while a peer may still write to it.
@@ -68,14 +73,17 @@ enum : int {
 };
 
 // (sum, squared deviations) per row for each of the two accumulators in flight and each of the
-// 2 * CS column halves of the cluster; then b_o, gamma, beta for the CTA's columns (fp32)
+// 2 * CS column halves of the cluster; then b_o, gamma, beta for the CTA's columns (bf16); then
+// a 32-row x 32-column bf16 staging tile per epilogue warp (x in, y out)
 // (4 ring stages where they fit in the 227 KB a CTA may have, else 3)
+constexpr int kStageTileBytes = 32 * 64;
 template <int CS>
 struct LnShape {
   static constexpr int kParts = 2 * CS;
   static constexpr int kStatBytes = 2 * kParts * kBM * 8;
-  static constexpr int kVecBytes = 3 * kBN * 4;
-  static constexpr int kRest = 1024 + kBarBytes + kStatBytes + kVecBytes;
+  static constexpr int kVecBytes = 3 * kBN * 2;
+  static constexpr int kStageBytesEpi = kEpiWarps * kStageTileBytes;
+  static constexpr int kRest = 1024 + kBarBytes + kStatBytes + kVecBytes + kStageBytesEpi;
   static constexpr int kStages = (kRest + 4 * kStageBytes <= 227 * 1024) ? 4 : 3;
   static constexpr int kSmemBytes = kRest + kStages * kStageBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -127,8 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [0,ST) full, [ST,2ST) empty, acc_full[2], acc_empty[2], stats[2], drain; tmem slot after
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 7);
   const uint32_t sStat = smem_u32(smem + S::kStages * kStageBytes + kBarBytes);
-  float* sVec = reinterpret_cast<float*>(smem + S::kStages * kStageBytes + kBarBytes +
-                                         S::kStatBytes);  // b_o | gamma | beta
+  __nv_bfloat16* sVec = reinterpret_cast<__nv_bfloat16*>(
+      smem + S::kStages * kStageBytes + kBarBytes + S::kStatBytes);  // b_o | gamma | beta
+  const uint32_t sStage =
+      smem_u32(smem + S::kStages * kStageBytes + kBarBytes + S::kStatBytes + S::kVecBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -243,9 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = threadIdx.x - 64; i < kBN; i += kEpiWarps * 32) {
       const int col = n0 + i;
       const bool ok_col = bounds_ok(col, p.D, p.status, kSiteVectors);
-      sVec[i] = (p.bias && ok_col) ? __bfloat162float(p.bias[col]) : 0.f;
-      sVec[kBN + i] = (p.gamma && ok_col) ? __bfloat162float(p.gamma[col]) : 1.f;
-      sVec[2 * kBN + i] = (p.beta && ok_col) ? __bfloat162float(p.beta[col]) : 0.f;
+      sVec[i] = (p.bias && ok_col) ? p.bias[col] : __float2bfloat16(0.f);
+      sVec[kBN + i] = (p.gamma && ok_col) ? p.gamma[col] : __float2bfloat16(1.f);
+      sVec[2 * kBN + i] = (p.beta && ok_col) ? p.beta[col] : __float2bfloat16(0.f);
     }
     named_bar_sync(1, kEpiWarps * 32);
     // ask L2 for this thread's 256 bytes of x in a tile (two 128-byte lines of its row)
@@ -273,14 +283,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tb =
           tmem + buf * kBN + c0 + (static_cast<uint32_t>(quarter * 32) << 16);
-      const uint4* xrow = reinterpret_cast<const uint4*>(
-          p.x + static_cast<int64_t>(in ? row : 0) * p.D + n0 + c0);
-      // 1. r = x + (acc + b_o), back into TMEM; sum.  x is loaded two chunks ahead.
+      // this warp's 32 x 64-byte staging tile: 16-byte chunk j of row r sits in slot
+      // j ^ ((r >> 1) & 3), so both the row-per-lane reads and the 8-rows-per-instruction
+      // writes hit all 32 banks once
+      const uint32_t stg = sStage + (warp - 2) * kStageTileBytes;
+      const int rr = lane >> 2, jj = lane & 3;  // coalesced side: rows rr + 8k, chunk jj
+      const int wrow = m0 + quarter * 32;       // the warp's first row
+      const uint32_t slot_w = stg + rr * 64 + ((jj ^ ((rr >> 1) & 3)) << 4);  // + k * 512
+      const uint32_t slot_r = stg + lane * 64;                                 // + (j ^ sw) * 16
+      const int sw_r = (lane >> 1) & 3;
+      // 1. r = x + (acc + b_o), back into TMEM; sum.  x comes in coalesced (four lanes per
+      // 64-byte row piece, eight rows per instruction), two 32-column chunks ahead, and goes
+      // through the staging tile to the thread that owns the row.
       uint4 xa[4], xb[4];
       auto load_x = [&](int c, uint4 (&dst)[4]) {
-        const bool ok_x = in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteX);
+        const int col = n0 + c0 + c * 32 + jj * 8;
+        const bool ok_x = span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteX);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = ok_x ? __ldg(xrow + c * 4 + v) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < 4; ++k) {
+          const int r = wrow + rr + 8 * k;
+          dst[k] = (ok_x && r < p.M)
+                       ? __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(r) * p.D +
+                                                              col))
+                       : make_uint4(0, 0, 0, 0);
+        }
       };
       load_x(0, xa);
       load_x(1, xb);
@@ -289,14 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(tb + c * 32, a);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) st_shared_v4(slot_w + k * 512, xa[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) xa[k] = xb[k];
+        if (c + 2 < kHalf / 32) load_x(c + 2, xb);
+        __syncwarp();
         uint4 xc[4];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          xc[v] = xa[v];
-          xa[v] = xb[v];
-        }
-        if (c + 2 < kHalf / 32) load_x(c + 2, xb);
-        const float* bvec = sVec + c0 + c * 32;
+        for (int j = 0; j < 4; ++j) xc[j] = ld_shared_v4(slot_r + ((j ^ sw_r) << 4));
+        __syncwarp();  // the tile is free for the next chunk
+        float bvec[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          unpack8_bf16(ld_shared_v4(smem_u32(sVec + c0 + c * 32 + 8 * j)), bvec + 8 * j);
         tmem_wait_ld();
         reg_fence(a);
         if (p.a_out != nullptr && in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteOut)) {
@@ -379,15 +411,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rstd = 1.0f / sqrtf(M2 * inv_d + p.eps);
       const float2 nmean = make_float2(-mean, -mean);
       const float2 rstd2 = make_float2(rstd, rstd);
-      // y for this thread's row, 32 columns at a time, straight from registers
-      uint4* yrow = reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(in ? row : 0) * p.D +
-                                             n0 + c0);
+      // y, 32 columns at a time: each thread's row into the staging tile, then out coalesced
+      // (four lanes per 64-byte row piece, eight rows per instruction)
 #pragma unroll 1
       for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t a[32];
         tmem_ld32(tb + c * 32, a);
-        const float* g = sVec + kBN + c0 + c * 32;
-        const float* bt = sVec + 2 * kBN + c0 + c * 32;
+        float g[32], bt[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          unpack8_bf16(ld_shared_v4(smem_u32(sVec + kBN + c0 + c * 32 + 8 * j)), g + 8 * j);
+          unpack8_bf16(ld_shared_v4(smem_u32(sVec + 2 * kBN + c0 + c * 32 + 8 * j)), bt + 8 * j);
+        }
         tmem_wait_ld();
         reg_fence(a);
         if (c == kHalf / 32 - 1) {  // accumulator read: hand it back to the MMA issuer
@@ -395,22 +430,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty(buf));
         }
-        if (in && span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteOut)) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t o[4];
+        for (int v = 0; v < 4; ++v) {
+          uint32_t o[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = v * 8 + 2 * e;
-              float2 z = fadd2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
-                               nmean);
-              z = fmul2(z, rstd2);
-              z = ffma2(z, make_float2(g[i], g[i + 1]), make_float2(bt[i], bt[i + 1]));
-              o[e] = pack_bf16x2(z.x, z.y);
-            }
-            yrow[c * 4 + v] = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int i = v * 8 + 2 * e;
+            float2 z = fadd2(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                             nmean);
+            z = fmul2(z, rstd2);
+            z = ffma2(z, make_float2(g[i], g[i + 1]), make_float2(bt[i], bt[i + 1]));
+            o[e] = pack_bf16x2(z.x, z.y);
           }
+          st_shared_v4(slot_r + ((v ^ sw_r) << 4), make_uint4(o[0], o[1], o[2], o[3]));
         }
+        __syncwarp();
+        const bool ok_y = span_ok(n0 + c0 + c * 32, 32, p.D, p.status, kSiteOut);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int r = wrow + rr + 8 * k;
+          const uint4 v = ld_shared_v4(slot_w + k * 512);
+          if (ok_y && r < p.M)
+            *reinterpret_cast<uint4*>(p.y + static_cast<int64_t>(r) * p.D + n0 + c0 + c * 32 +
+                                      jj * 8) = v;
+        }
+        __syncwarp();  // the tile is free for the next chunk
       }
     }
   }
