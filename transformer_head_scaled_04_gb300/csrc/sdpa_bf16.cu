@@ -190,6 +190,12 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int lin) {
   return w;
 }
 
+// kBandMask selects how a diagonal / edge tile excludes keys (the launcher takes it for causal,
+// key-padding and restricted attention): one compare and select per key against per-row
+// bounds, one-sided where the warp's rows allow it.  Unmasked attention keeps a per-key
+// position test: its only masked tile is a ragged last one, and any other form there changed
+// how the compiler scheduled the unmasked exponential loop (3% slower in A/B).
+template <bool kBandMask>
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
@@ -463,6 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         : (p.mask == kMaskWindow) ? min(row + p.window, p.Nk - 1)
                                                   : w.L - 1;
       const int first = (p.mask == kMaskWindow) ? row - p.window : 0;
+      // Both bounds grow with the row, so the warp's smallest limit is its first row's and its
+      // largest first key its last row's: whether any row of the warp masks at either end of
+      // a key tile is known without a vote.
+      const int wr0 = w.q0 + t * kBQ + quarter * 32;
+      const int lim_min = (p.mask == 1)             ? wr0
+                          : (p.mask == kMaskWindow) ? min(wr0 + p.window, p.Nk - 1)
+                                                    : w.L - 1;
+      const int first_max = (p.mask == kMaskWindow) ? wr0 + 31 - p.window : 0;
       float m_used = -INFINITY;
       float l = 0.f;
 
@@ -475,7 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const int col0 = (kt0 + j) * kBKV;
-        const bool masked = col0 + kBKV - 1 > limit || col0 < first;  // diagonal / edge tile
+        // diagonal / edge tile: keys q of the tile with q > hi or q < lo are excluded; some row
+        // of the warp has keys past its limit (mask_hi) or before its band (mask_lo)
+        const int hi = limit - col0;
+        const int lo = first - col0;
+        const bool mask_hi = lim_min - col0 < kBKV - 1;
+        const bool mask_lo = first_max - col0 > 0;
+        const bool masked = col0 + kBKV - 1 > limit || col0 < first;  // this row
         float sv[128];
         // the whole S row of this tile: 128 fp32 in registers, one TMEM round trip
         auto load_s = [&]() {
@@ -496,7 +516,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             sv[64 + q] = __uint_as_float(r2[q]);
             sv[96 + q] = __uint_as_float(r3[q]);
           }
-          if (masked) {  // exclude keys past limit
+          // Excluded keys get -inf (p = 0).  Band form: one compare against a per-row bound
+          // and one select per key; the warp takes the one-sided form when none of its rows
+          // has the other end inside the tile (causal and key-padding tiles, and the edge tiles
+          // of restricted attention whose radius spans whole tiles).  The per-key position
+          // test costs ~9 cycles per key there.
+          if constexpr (kBandMask) {
+            if (mask_hi || mask_lo) {
+              if (!mask_lo) {
+#pragma unroll
+                for (int q = 0; q < 128; ++q) sv[q] = q > hi ? -INFINITY : sv[q];
+              } else if (!mask_hi) {
+#pragma unroll
+                for (int q = 0; q < 128; ++q) sv[q] = q < lo ? -INFINITY : sv[q];
+              } else {
+#pragma unroll
+                for (int q = 0; q < 128; ++q) sv[q] = (q > hi || q < lo) ? -INFINITY : sv[q];
+              }
+            }
+          } else if (masked) {
 #pragma unroll
             for (int q = 0; q < 128; ++q)
               if (col0 + q > limit || col0 + q < first) sv[q] = -INFINITY;
@@ -740,16 +778,21 @@ cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
   p.so_n = a.so[2];
   p.status = ctx.status;
   p.timeout_ns = ctx.timeout_ns;
+  const bool band = a.mask != 0;
+  const void* fn = band ? reinterpret_cast<const void*>(sdpa_fwd_bf16_kernel<true>)
+                        : reinterpret_cast<const void*>(sdpa_fwd_bf16_kernel<false>);
   int regs = 0;
-  cudaError_t e =
-      prepare_kernel(reinterpret_cast<const void*>(sdpa_fwd_bf16_kernel), kSmemBytes, &regs);
+  cudaError_t e = prepare_kernel(fn, kSmemBytes, &regs);
   if (e != cudaSuccess) return e;
   // The setmaxnreg split must fit in what the block is launched with, or the increase would
   // wait forever: refuse to launch if the compiled register count is too small for it.
   if (regs * kThreads < 8 * 32 * kSoftmaxRegs + 4 * 32 * kControlRegs)
     return cudaErrorInvalidConfiguration;
   dim3 grid((a.Nq + 2 * kBQ - 1) / (2 * kBQ), a.H, a.B);
-  return launch_pdl(sdpa_fwd_bf16_kernel, grid, dim3(kThreads), kSmemBytes, s, tmQ, tmK, tmV,
+  if (band)
+    return launch_pdl(sdpa_fwd_bf16_kernel<true>, grid, dim3(kThreads), kSmemBytes, s, tmQ, tmK,
+                      tmV, tmO, p);
+  return launch_pdl(sdpa_fwd_bf16_kernel<false>, grid, dim3(kThreads), kSmemBytes, s, tmQ, tmK, tmV,
                     tmO, p);
 }
 
