@@ -235,9 +235,22 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
   MHA_NVTX_RANGE("linear");
   cudaError_t e;
   if (dtype == MHA_BF16) {
+    CUtensorMap tmX, tmW, tmY;
+    // at least four rounds of 256 x 256 tiles for the pairs of SMs: the two-CTA form (half of
+    // each operand per SM, a deeper ring of K slices).  Same-box A/B: 32768 x 3072 x 1024 137.9
+    // -> 127.6 us, 32768 x 4096 x 1024 (ReLU) 174.7 -> 162.4 us, 16384 x 2048 x 1024 53.9 ->
+    // 49.8 us; with 1-3 rounds (8192 or 4096 rows, K = 512) it was ~2 us slower, so those keep
+    // the single-CTA kernel.
+    const int64_t pair_tiles = ((M + 255) / 256) * static_cast<int64_t>((N + 255) / 256);
+    if (mha::gemm2_bf16_supported(M, N, K) && pair_tiles >= 4 * (ctx.num_sms / 2)) {
+      if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, 128) ||
+          !map_2d_bf16(&tmY, Y, N, M, ldy, 32))
+        return MHA_ERR_CUDA;
+      e = mha::launch_gemm2_bf16(tmX, tmW, tmY, relu, bias, M, N, K, ldy, ctx, s, residual);
+      return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+    }
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);
     const int bn = (tiles256 >= ctx.num_sms) ? 256 : 128;
-    CUtensorMap tmX, tmW, tmY;
     if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, bn) ||
         !map_2d_bf16(&tmY, Y, N, M, ldy, 32))
       return MHA_ERR_CUDA;

@@ -60,6 +60,14 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                              const void* residual = nullptr);
+// The same GEMM on pairs of SMs (gemm2_bf16.cu): a cluster of two CTAs per 256 x 256 output
+// tile, one pair-granularity MMA (M = 256) with half of each operand in each CTA.  tmX: box
+// {64, 128}; tmW: box {64, 128}; tmY: box {64, 32}.  Needs K % 64 == 0 and N % 64 == 0.
+bool gemm2_bf16_supported(int M, int N, int K);
+cudaError_t launch_gemm2_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
+                              const CUtensorMap& tmY, bool relu, const void* bias, int M, int N,
+                              int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
+                              const void* residual = nullptr);
 // Weight-gradient forms (no bias, no activation), both operands MN-major: X stored [K, M] and
 // W stored [K, N] (row-major activations, tokens = K), maps {M or N, K} with box {64, 64};
 // 128 x 128 tiles.  launch_gemm_bf16_mn writes Y directly.  The split-K form zeroes acc
