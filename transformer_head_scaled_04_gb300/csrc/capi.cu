@@ -325,7 +325,9 @@ int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t 
         !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.sv) ||
         !map_bhnd_bf16(&to, a.O, a.B, a.H, a.Nq, a.so, 32))
       return MHA_ERR_CUDA;
-    e = mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
+    // at most 128 queries per head: one query tile per CTA, two CTAs per SM
+    e = (a.Nq <= 128) ? mha::launch_sdpa_short_bf16(tq, tk, tv, to, a, ctx, s)
+                      : mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
   } else {
     mha::SdpaArgs af = a;
     af.status = ctx.status;
