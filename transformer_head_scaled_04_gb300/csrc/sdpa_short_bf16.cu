@@ -10,7 +10,8 @@
 // encoder self-attention and cross-attention, n = 128) its second tile has no rows and the
 // (b, h) units fill the 152 SMs in about two rounds.  Here a CTA owns one 128-row query tile
 // of one (b, h) with 192 threads, ~81 KB of shared memory and 256 TMEM columns, so two CTAs run
-// on each SM and the same heads finish in one round.
+// on each SM and the same heads finish in one round; the library uses it up to 512 queries
+// per head, where the persistent kernel's overlap of consecutive units buys little.
 //   warps 0-3  softmax, one query row per thread (its TMEM lane): the whole 128-key S row in
 //              registers, the mask, p = 2^(s c - m c) against the first key tile's row max (a
 //              tile whose row sum passes 2^64 is redone with its exact max after rescaling O
