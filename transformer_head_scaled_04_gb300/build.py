@@ -24,7 +24,7 @@ DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libmha_debug.so")
 
 SOURCES = ["capi.cu", "gemm_bf16.cu", "gemm_f32.cu", "sdpa_bf16.cu", "sdpa_f32.cu",
            "sdpa_decode.cu", "sdpa_bwd_f32.cu", "sdpa_bwd_bf16.cu", "bwd_util.cu", "layernorm.cu",
-           "gemm_ln_bf16.cu", "gemm2_bf16.cu", "sdpa_short_bf16.cu",
+           "gemm_ln_bf16.cu", "gemm2_bf16.cu",
            "layer_noalloc.cu", "layer_host.cu"]
 HEADERS = ["device_common.cuh", "launchers.h"]
 

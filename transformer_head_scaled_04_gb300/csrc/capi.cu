@@ -325,12 +325,7 @@ int run_sdpa(const mha::SdpaArgs& a, int dtype, const DevCtx& ctx, cudaStream_t 
         !map_bhnd_bf16(&tv, a.V, a.B, a.H, a.Nk, a.sv) ||
         !map_bhnd_bf16(&to, a.O, a.B, a.H, a.Nq, a.so, 32))
       return MHA_ERR_CUDA;
-    // up to 512 queries per head: one query tile per CTA, two CTAs per SM (same-box A/B
-    // against the two-tile persistent kernel: base config 2 17.0 -> 12.9 us, config 4 19.1 ->
-    // 15.0, config 3 21.1 -> 19.1, 16 x 8 heads of 512 rows 23.2 -> 21.2 causal and 25.2 ->
-    // 23.2 unmasked; 8 x 16 heads of 1024 rows the same either way)
-    e = (a.Nq <= 512) ? mha::launch_sdpa_short_bf16(tq, tk, tv, to, a, ctx, s)
-                      : mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
+    e = mha::launch_sdpa_bf16(tq, tk, tv, to, a, ctx, s);
   } else {
     mha::SdpaArgs af = a;
     af.status = ctx.status;

@@ -256,32 +256,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ------------------------------------------------------------------ persistent blocks
-// Ask the launch queue for a block of this grid that has not started yet; the 16-byte
-// response lands at `resp` and completes `bar` (armed for 16 bytes by the caller).
-__device__ __forceinline__ void launch_cancel_request(uint32_t resp, uint32_t bar) {
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
-      "[%0], [%1];" ::"r"(resp), "r"(bar)
-      : "memory");
-}
-// The linear index of the block a landed response took over, or -1 when there was none left.
-__device__ __forceinline__ int launch_cancel_result(uint32_t resp) {
-  uint32_t ok, cx, cy, cz;
-  asm volatile(
-      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
-      "ld.shared.b128 h, [%4];\n\t"
-      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t"
-      "clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, _}, h;\n\t"
-      "}"
-      : "=r"(ok), "=r"(cx), "=r"(cy), "=r"(cz)
-      : "r"(resp)
-      : "memory");
-  if (!ok) return -1;
-  return static_cast<int>(cx + gridDim.x * (cy + gridDim.y * cz));
-}
-
 // ------------------------------------------------------------------ thread-block clusters
 // This CTA's rank in its cluster, the cluster's index in the grid and the number of clusters
 // (x dimension; the kernels here use 1-D clusters and grids).

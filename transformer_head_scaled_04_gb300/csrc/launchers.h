@@ -124,11 +124,6 @@ struct SdpaArgs {
 cudaError_t launch_sdpa_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, const CUtensorMap& tmO, const SdpaArgs& a,
                              const DevCtx& ctx, cudaStream_t s);
-// The same for short query sequences (used up to 512 rows; sdpa_short_bf16.cu): one 128-row
-// query tile of one (b, h) per CTA, two CTAs per SM; same maps, masks and outputs.
-cudaError_t launch_sdpa_short_bf16(const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                                   const CUtensorMap& tmV, const CUtensorMap& tmO,
-                                   const SdpaArgs& a, const DevCtx& ctx, cudaStream_t s);
 cudaError_t launch_sdpa_f32(const SdpaArgs& a, cudaStream_t s);
 
 // ---- one generation step against a key/value cache (split-K over the cached keys)
