@@ -6,7 +6,7 @@
 //    attention, 训练样本 for the causal mask, Self-Attention的优势 for the restricted form).
 //
 // The n x n score matrix never leaves the SM.  A CTA owns one 128-row query tile of one (b, h)
-// and streams K/V in 128-row tiles; with 192 threads, ~81 KB of shared memory and 256 TMEM
+// and streams K/V in 128-row tiles; with 192 threads, ~97 KB of shared memory and 256 TMEM
 // columns two CTAs share each SM, so on each SMSP two softmax warps of different tiles take
 // turns with the exponentials while either CTA's tensor-core products run.  (An earlier design,
 // one persistent CTA per SM owning two query tiles on 384 threads and all 512 TMEM columns,
@@ -21,7 +21,7 @@
 //              TMEM once the previous P.V has read it; at the end O / l staged in the Q buffer
 //              (128-byte swizzle) and written by one bulk tensor store per warp, straight into
 //              any strided layout (the head-concat layout [B, Nq, H*64] in the sublayer)
-//   warp 4     TMA producer: Q, then K and V through separate two-slot rings
+//   warp 4     TMA producer: Q, then K and V through separate rings (two and three slots)
 //   warp 5     TMEM owner and MMA issuer: S = Q K_j^T (tcgen05.mma 128x128x16, fp32 in TMEM)
 //              as soon as the softmax warps have read S_{j-1}, O += P_j V_j (128x64x16, P from
 //              TMEM, V an MN-major shared-memory operand)
@@ -43,7 +43,8 @@ namespace {
 constexpr int kBQ = 128;   // query rows per CTA
 constexpr int kBKV = 128;  // keys per K/V tile
 constexpr int kHD = 64;    // head dim (d_k = d_v)
-constexpr int kRing = 2;   // K and V ring depth
+constexpr int kKRing = 2;  // K ring depth
+constexpr int kVRing = 3;  // V ring depth (a third slot: causal 277 -> 271 us in A/B)
 // 192 threads at <= 170 registers each (two CTAs per SM); the softmax warps' S row and P fit
 // without a register split (the producer and issuer warps are only half a warpgroup, so they
 // could not take part in one)
@@ -51,8 +52,8 @@ constexpr int kThreads = 192;
 constexpr int kTileBytes = kBQ * kHD * 2;  // 16 KB
 constexpr int kOffQ = 0;                   // also stages O at the end
 constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kRing * kTileBytes;
-constexpr int kOffBar = kOffV + kRing * kTileBytes;
+constexpr int kOffV = kOffK + kKRing * kTileBytes;
+constexpr int kOffBar = kOffV + kVRing * kTileBytes;
 constexpr int kSmemBytes = 1024 + kOffBar + 256;
 // TMEM columns: S [0,128) O [128,192) P [192,256) (P: 128 bf16 per row, two per column)
 constexpr uint32_t kTmemCols = 256;
@@ -72,11 +73,11 @@ enum : int {
 };
 
 constexpr int kBarQ = 0;
-constexpr int kBarKFull = 1;                    // [2]
-constexpr int kBarKEmpty = kBarKFull + kRing;   // [2]
-constexpr int kBarVFull = kBarKEmpty + kRing;   // [2]
-constexpr int kBarVEmpty = kBarVFull + kRing;   // [2]
-constexpr int kBarSFull = kBarVEmpty + kRing;
+constexpr int kBarKFull = 1;
+constexpr int kBarKEmpty = kBarKFull + kKRing;
+constexpr int kBarVFull = kBarKEmpty + kKRing;
+constexpr int kBarVEmpty = kBarVFull + kVRing;
+constexpr int kBarSFull = kBarVEmpty + kVRing;
 constexpr int kBarSFree = kBarSFull + 1;
 constexpr int kBarPFull = kBarSFree + 1;
 constexpr int kBarODone = kBarPFull + 1;
@@ -148,9 +149,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kKRing; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
       mbar_init(bar(kBarKEmpty + i), 1);
+    }
+    for (int i = 0; i < kVRing; ++i) {
       mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
     }
@@ -183,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_arrive_expect_tx(bar(kBarQ), kTileBytes);
       tma_load_4d(sQ, &tmQ, bar(kBarQ), 0, q0, h, b);
       for (int j = 0; ok && j < nt; ++j) {
-        const int sl = j % kRing;
-        const uint32_t par = ((j / kRing) & 1) ^ 1;
+        const int sl = j % kKRing, vs = j % kVRing;
+        const uint32_t par = ((j / kKRing) & 1) ^ 1, vpar = ((j / kVRing) & 1) ^ 1;
         if (!mbar_wait_backoff(bar(kBarKEmpty + sl), par, p.timeout_ns)) {
           ok = false;
           break;
@@ -192,21 +195,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_arrive_expect_tx(bar(kBarKFull + sl), kTileBytes);
         tma_load_4d(sK + sl * kTileBytes, &tmK, bar(kBarKFull + sl), 0, (kt0 + j) * kBKV, h, b);
         ++kn;
-        if (!mbar_wait_backoff(bar(kBarVEmpty + sl), par, p.timeout_ns)) {
+        if (!mbar_wait_backoff(bar(kBarVEmpty + vs), vpar, p.timeout_ns)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarVFull + sl), kTileBytes);
-        tma_load_4d(sV + sl * kTileBytes, &tmV, bar(kBarVFull + sl), 0, (kt0 + j) * kBKV, h, b);
+        mbar_arrive_expect_tx(bar(kBarVFull + vs), kTileBytes);
+        tma_load_4d(sV + vs * kTileBytes, &tmV, bar(kBarVFull + vs), 0, (kt0 + j) * kBKV, h, b);
         ++vn;
       }
       if (!ok) record_error(p.status, kErrTimeout, kSiteProducer);
       // every copy started here lands before the CTA can exit
       (void)mbar_wait(bar(kBarQ), 0, p.timeout_ns);
-      for (int j = (kn > kRing ? kn - kRing : 0); j < kn; ++j)
-        (void)mbar_wait(bar(kBarKFull + j % kRing), (j / kRing) & 1, p.timeout_ns);
-      for (int j = (vn > kRing ? vn - kRing : 0); j < vn; ++j)
-        (void)mbar_wait(bar(kBarVFull + j % kRing), (j / kRing) & 1, p.timeout_ns);
+      for (int j = (kn > kKRing ? kn - kKRing : 0); j < kn; ++j)
+        (void)mbar_wait(bar(kBarKFull + j % kKRing), (j / kKRing) & 1, p.timeout_ns);
+      for (int j = (vn > kVRing ? vn - kVRing : 0); j < vn; ++j)
+        (void)mbar_wait(bar(kBarVFull + j % kVRing), (j / kVRing) & 1, p.timeout_ns);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------------ MMA issuer
@@ -219,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       bool ok = mbar_wait(bar(kBarQ), 0, p.timeout_ns);
       // S(j) = Q K(j)^T once the softmax warps have read S(j-1) out of TMEM
       auto issue_s = [&](int j) -> bool {
-        const int sl = j % kRing;
-        if (!mbar_wait(bar(kBarKFull + sl), (j / kRing) & 1, p.timeout_ns)) return false;
+        const int sl = j % kKRing;
+        if (!mbar_wait(bar(kBarKFull + sl), (j / kKRing) & 1, p.timeout_ns)) return false;
         if (j > 0 && !mbar_wait(bar(kBarSFree), (j - 1) & 1, p.timeout_ns)) return false;
         tc_fence_after();
         const uint64_t bk = dK0 + static_cast<uint64_t>((sl * kTileBytes) >> 4);
@@ -235,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 1; ok && j <= nt; ++j) {
         if (j < nt && !(ok = issue_s(j))) break;
         // O += P(j-1) V(j-1) once the softmax warps have written P(j-1)
-        const int pj = j - 1, sl = pj % kRing;
+        const int pj = j - 1, sl = pj % kVRing;
         if (!mbar_wait(bar(kBarPFull), pj & 1, p.timeout_ns) ||
-            !mbar_wait(bar(kBarVFull + sl), (pj / kRing) & 1, p.timeout_ns)) {
+            !mbar_wait(bar(kBarVFull + sl), (pj / kVRing) & 1, p.timeout_ns)) {
           ok = false;
           break;
         }
