@@ -315,6 +315,28 @@ def test_linear_bf16(M, N, K, bias):
     assert_bf16_close(host(Y), oracle.linear_ref(X, W, b), f"linear bf16 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K,bias,relu", [
+    (9800, 2048, 512, True, False),   # last row band: the odd CTA of the pair has no rows
+    (9900, 2112, 448, True, True),    # ragged N: the odd CTA's W rows of the last band past N
+    (16384, 2048, 1024, False, False),
+])
+def test_linear_bf16_pair_tiles(M, N, K, bias, relu):
+    """Shapes with at least four rounds of 256 x 256 tiles run on pairs of SMs.  Weights in
+    [-0.04, 0.04] keep every |y| below 8, where half a bf16 ulp of the rounded output stays
+    under the 2e-2 bound (tens of millions of outputs with the wider weights of the other cases
+    reach |y| > 8, whose half-ulp is 0.031)."""
+    g = np.random.Generator(np.random.PCG64(M * 7 + N + K))
+    X = si.round_bf16(g.standard_normal((M, K)))
+    W = si.round_bf16(g.uniform(-0.04, 0.04, (N, K)))
+    b = si.round_bf16(0.1 * g.standard_normal(N)) if bias else None
+    Y = mha.linear(to_dev(X, torch.bfloat16), to_dev(W, torch.bfloat16),
+                   to_dev(b, torch.bfloat16), relu=relu)
+    ref = oracle.linear_ref(X, W, b)
+    if relu:
+        ref = np.maximum(ref, 0.0)
+    assert_bf16_close(host(Y), ref, f"linear bf16 pair tiles {M}x{N}x{K}")
+
+
 def test_linear_bf16_row_pitch():
     g = np.random.Generator(np.random.PCG64(3))
     X = si.round_bf16(g.standard_normal((257, 320)))

@@ -242,11 +242,12 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
     // 49.8 us; with 1-3 rounds (8192 or 4096 rows, K = 512) it was ~2 us slower, so those keep
     // the single-CTA kernel.
     const int64_t pair_tiles = ((M + 255) / 256) * static_cast<int64_t>((N + 255) / 256);
-    if (mha::gemm2_bf16_supported(M, N, K) && pair_tiles >= 4 * (ctx.num_sms / 2)) {
+    if (mha::gemm2_bf16_supported(M, N, K) && pair_tiles >= 4 * (ctx.num_sms / 2) &&
+        residual == nullptr) {
       if (!map_2d_bf16(&tmX, X, K, M, ldx, 128) || !map_2d_bf16(&tmW, W, K, N, K, 128) ||
           !map_2d_bf16(&tmY, Y, N, M, ldy, 32))
         return MHA_ERR_CUDA;
-      e = mha::launch_gemm2_bf16(tmX, tmW, tmY, relu, bias, M, N, K, ldy, ctx, s, residual);
+      e = mha::launch_gemm2_bf16(tmX, tmW, tmY, relu, bias, M, N, K, ctx, s);
       return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
     }
     const int64_t tiles256 = ((M + 127) / 128) * static_cast<int64_t>((N + 255) / 256);

@@ -1,5 +1,5 @@
-// gemm2_bf16.cu -- Y[M,N] = act(X[M,K] W[N,K]^T + bias[N] (+ R)) on pairs of SMs, act =
-// identity or ReLU.
+// gemm2_bf16.cu -- Y[M,N] = act(X[M,K] W[N,K]^T + bias[N]) on pairs of SMs, act = identity
+// or ReLU.
 //
 // The same projection steps as gemm_bf16.cu: the fused Q|K|V projection of every head and the
 // output projection W^O ("Attention Is All You Need", lettle.cn translation, 3.2.2 多头注意力;
@@ -19,7 +19,7 @@
 //   warp 1     TMEM owner in both CTAs (512 columns allocated as a pair: two accumulators of
 //              256 columns); MMA issuer in the even CTA, which also releases ring slots and
 //              hands accumulators to the epilogues of both CTAs by multicast commits
-//   warps 2-5  epilogue (both CTAs, its own 128 rows): tcgen05.ld, bias (+ R), ReLU if asked,
+//   warps 2-5  epilogue (both CTAs, its own 128 rows): tcgen05.ld, bias, ReLU if asked,
 //              bf16 round to nearest even, hand the accumulator back to the even CTA, store
 //              through swizzled staging boxes with bulk tensor stores
 // Every wait is bounded; on a timeout the kernel records MHA_ERR_DEVICE_TIMEOUT, lets its
@@ -54,8 +54,7 @@ enum : int {
   kSitePairProducer = 61,
   kSitePairMma = 62,
   kSitePairEpilogue = 63,
-  kSitePairBias = 64,  // index checks (MHA_DEBUG_BOUNDS builds)
-  kSitePairResidual = 65
+  kSitePairBias = 64  // index checks (MHA_DEBUG_BOUNDS builds)
 };
 
 // ---- pair-granularity tcgen05 forms
@@ -107,8 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const __grid_constant__ CUtensorMap tmW,
                            const __grid_constant__ CUtensorMap tmY,
                            const __nv_bfloat16* __restrict__ bias, int M, int N, int K,
-                           int64_t ldy, int* status, uint64_t timeout_ns,
-                           const __nv_bfloat16* __restrict__ R) {
+                           int* status, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -156,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  pdl_wait();  // the previous kernel's output (X, the bias, R) is complete from here on
+  pdl_wait();  // the previous kernel's output (X, the bias) is complete from here on
 
   bool ok = true;
   if (warp == 0 && lane == 0) {
@@ -230,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = tcount & 1;
       const int m0 = (t / tiles_n) * (2 * kRows) + static_cast<int>(rank) * kRows;
       const int n0 = (t % tiles_n) * kCols;
-      const int row = m0 + quarter * 32 + lane;
       if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (tcount >> 1) & 1, timeout_ns))) {
         record_error(status, kErrTimeout, kSitePairEpilogue);
         break;
@@ -278,22 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < 64; ++i) bv[i] = 0.f;
-        }
-        if (R != nullptr && row < M && span_ok(col, 64, N, status, kSitePairResidual)) {
-          // a residual matrix with Y's layout joins the bias
-          const uint4* rp =
-              reinterpret_cast<const uint4*>(R + static_cast<int64_t>(row) * ldy + col);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            uint4 u = rp[v];
-            const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float2 f = __bfloat1622float2(hv[e]);
-              bv[v * 8 + e * 2] += f.x;
-              bv[v * 8 + e * 2 + 1] += f.y;
-            }
-          }
         }
         // the store issued from this staging box two boxes ago must have read it
         const uint32_t sb = sOut + (quarter * 2 + (box & 1)) * kOutBoxBytes;
@@ -370,8 +351,8 @@ int max_pairs(const DevCtx& ctx) {
 
 template <bool kRelu>
 cudaError_t launch_relu(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
-                        const void* bias, int M, int N, int K, int64_t ldy, const DevCtx& ctx,
-                        cudaStream_t s, const void* R) {
+                        const void* bias, int M, int N, int K, const DevCtx& ctx,
+                        cudaStream_t s) {
   auto kern = gemm2_bias_bf16_kernel<kRelu>;
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), kSmemBytes, nullptr);
   if (e != cudaSuccess) return e;
@@ -395,8 +376,7 @@ cudaError_t launch_relu(const CUtensorMap& tmX, const CUtensorMap& tmW, const CU
   cfg.attrs = at;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmY, static_cast<const __nv_bfloat16*>(bias),
-                            M, N, K, ldy, ctx.status, ctx.timeout_ns,
-                            static_cast<const __nv_bfloat16*>(R));
+                            M, N, K, ctx.status, ctx.timeout_ns);
 }
 
 }  // namespace
@@ -407,10 +387,9 @@ bool gemm2_bf16_supported(int M, int N, int K) {
 
 cudaError_t launch_gemm2_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                               const CUtensorMap& tmY, bool relu, const void* bias, int M, int N,
-                              int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
-                              const void* residual) {
-  if (relu) return launch_relu<true>(tmX, tmW, tmY, bias, M, N, K, ldy, ctx, s, residual);
-  return launch_relu<false>(tmX, tmW, tmY, bias, M, N, K, ldy, ctx, s, residual);
+                              int K, const DevCtx& ctx, cudaStream_t s) {
+  if (relu) return launch_relu<true>(tmX, tmW, tmY, bias, M, N, K, ctx, s);
+  return launch_relu<false>(tmX, tmW, tmY, bias, M, N, K, ctx, s);
 }
 
 }  // namespace mha

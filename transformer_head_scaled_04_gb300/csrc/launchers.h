@@ -66,8 +66,7 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
 bool gemm2_bf16_supported(int M, int N, int K);
 cudaError_t launch_gemm2_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                               const CUtensorMap& tmY, bool relu, const void* bias, int M, int N,
-                              int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
-                              const void* residual = nullptr);
+                              int K, const DevCtx& ctx, cudaStream_t s);
 // Weight-gradient forms (no bias, no activation), both operands MN-major: X stored [K, M] and
 // W stored [K, N] (row-major activations, tokens = K), maps {M or N, K} with box {64, 64};
 // 128 x 128 tiles.  launch_gemm_bf16_mn writes Y directly.  The split-K form zeroes acc
