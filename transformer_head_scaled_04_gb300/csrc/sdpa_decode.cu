@@ -31,6 +31,7 @@ namespace {
 constexpr int kChunk = 256;  // keys per CTA
 constexpr int kD = 64;       // head dim (d_k = d_v)
 constexpr int kThreads = 128;
+static_assert(kChunk == 2 * kThreads, "each thread scores two keys of the chunk");
 constexpr int kWarps = kThreads / 32;
 constexpr int kBox = 128;                // rows per TMA box
 constexpr int kBoxBytes = kBox * kD * 2;  // 16 KB
@@ -134,25 +135,35 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
 
-  // ---- scores: thread t takes keys t and t + 128 of the chunk
-  for (int kk = tid; kk < kChunk; kk += kThreads) {
-    const int key = k0 + kk;
-    float s[NQ];
-    if (kk < nk) {
-      const uint8_t* row = smem + kOffK + kk * 128;  // box rows are consecutive 128-byte rows
+  // ---- scores: thread t takes keys t and t + 128 of the chunk together, so each query value
+  // read from shared memory serves both keys (the sum over d runs in the same order as for one)
+  {
+    const int kk0 = tid, kk1 = tid + kThreads;
+    const bool in0 = kk0 < nk, in1 = kk1 < nk;
+    float s0[NQ], s1[NQ];
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) s[q] = 0.f;
+    for (int q = 0; q < NQ; ++q) s0[q] = s1[q] = 0.f;
+    const uint8_t* row0 = smem + kOffK + kk0 * 128;  // box rows are consecutive 128-byte rows
+    const uint8_t* row1 = smem + kOffK + kk1 * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of row kk sits at chunk c ^ (kk & 7)
-        const uint4 u = *reinterpret_cast<const uint4*>(row + ((c ^ (kk & 7)) << 4));
-        const float kv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+    for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of row kk sits at chunk c ^ (kk & 7)
+      const uint4 u0 = in0 ? *reinterpret_cast<const uint4*>(row0 + ((c ^ (kk0 & 7)) << 4))
+                           : make_uint4(0, 0, 0, 0);
+      const uint4 u1 = in1 ? *reinterpret_cast<const uint4*>(row1 + ((c ^ (kk1 & 7)) << 4))
+                           : make_uint4(0, 0, 0, 0);
+      const float k0v[8] = {bf16_lo(u0.x), bf16_hi(u0.x), bf16_lo(u0.y), bf16_hi(u0.y),
+                            bf16_lo(u0.z), bf16_hi(u0.z), bf16_lo(u0.w), bf16_hi(u0.w)};
+      const float k1v[8] = {bf16_lo(u1.x), bf16_hi(u1.x), bf16_lo(u1.y), bf16_hi(u1.y),
+                            bf16_lo(u1.z), bf16_hi(u1.z), bf16_lo(u1.w), bf16_hi(u1.w)};
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          if (q < Nq) {
-            const float* qr = sQ + q * kD + c * 8;
+      for (int q = 0; q < NQ; ++q) {
+        if (q < Nq) {
+          const float* qr = sQ + q * kD + c * 8;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s[q] = fmaf(qr[e], kv[e], s[q]);
+          for (int e = 0; e < 8; ++e) {
+            const float qe = qr[e];
+            s0[q] = fmaf(qe, k0v[e], s0[q]);
+            s1[q] = fmaf(qe, k1v[e], s1[q]);
           }
         }
       }
@@ -160,8 +171,10 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
       if (q < Nq) {
-        const bool ok = kk < nk && (!p.causal || key <= L - Nq + q);
-        sS[q * kChunk + kk] = ok ? s[q] : -INFINITY;
+        const bool ok0 = in0 && (!p.causal || k0 + kk0 <= L - Nq + q);
+        const bool ok1 = in1 && (!p.causal || k0 + kk1 <= L - Nq + q);
+        sS[q * kChunk + kk0] = ok0 ? s0[q] : -INFINITY;
+        sS[q * kChunk + kk1] = ok1 ? s1[q] : -INFINITY;
       }
     }
   }
