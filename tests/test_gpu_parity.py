@@ -69,6 +69,7 @@ SDPA_CASES = [
     (2, 2, 300, 300, "causal", None),
     (2, 1, 257, 257, "causal", None),
     (1, 2, 640, 640, "causal", None),
+    (3, 5, 1000, 1000, "causal", None),   # heaviest query tiles of all 15 heads launch first
     (3, 2, 200, 390, "key_padding", [0, 1, 390]),
     (4, 1, 129, 256, "key_padding", [64, 127, 128, 129]),
     # more key tiles than K/V ring slots while a block's second query tile is empty

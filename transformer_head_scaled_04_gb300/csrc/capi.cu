@@ -264,6 +264,35 @@ int run_linear(int M, int N, int K, int dtype, const void* X, int64_t ldx, const
   return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+// The two projections of cross-attention, Y1 = X1 W1^T + b1 and Y2 = X2 W2^T + b2 with the same
+// K.  bf16 problems too small for the pair form alone run as one launch (the CTAs take the
+// second problem's tiles after the first's), so the GPU fills once; everything else is two
+// run_linear calls.
+int run_linear_two(int M1, int N1, const void* X1, const void* W1, const void* b1, void* Y1,
+                   int M2, int N2, const void* X2, const void* W2, const void* b2, void* Y2,
+                   int K, int dtype, const DevCtx& ctx, cudaStream_t s) {
+  const int64_t pair_tiles = ((M1 + 255) / 256) * static_cast<int64_t>((N1 + 255) / 256) +
+                             ((M2 + 255) / 256) * static_cast<int64_t>((N2 + 255) / 256);
+  if (dtype == MHA_BF16 && pair_tiles < 4 * (ctx.num_sms / 2) && K % 64 == 0 &&
+      N1 % 64 == 0 && N2 % 64 == 0) {
+    MHA_NVTX_RANGE("linear_two");
+    const int64_t tiles256 = ((M1 + 127) / 128) * static_cast<int64_t>((N1 + 255) / 256) +
+                             ((M2 + 127) / 128) * static_cast<int64_t>((N2 + 255) / 256);
+    const int bn = (tiles256 >= ctx.num_sms) ? 256 : 128;
+    CUtensorMap tmX1, tmW1, tmY1, tmX2, tmW2, tmY2;
+    if (!map_2d_bf16(&tmX1, X1, K, M1, K, 128) || !map_2d_bf16(&tmW1, W1, K, N1, K, bn) ||
+        !map_2d_bf16(&tmY1, Y1, N1, M1, N1, 32) || !map_2d_bf16(&tmX2, X2, K, M2, K, 128) ||
+        !map_2d_bf16(&tmW2, W2, K, N2, K, bn) || !map_2d_bf16(&tmY2, Y2, N2, M2, N2, 32))
+      return MHA_ERR_CUDA;
+    const cudaError_t e = mha::launch_gemm_bf16_two(tmX1, tmW1, tmY1, b1, M1, N1, tmX2, tmW2,
+                                                    tmY2, b2, M2, N2, K, bn, ctx, s);
+    return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  }
+  const int st = run_linear(M1, N1, K, dtype, X1, K, W1, b1, Y1, N1, ctx, s);
+  if (st != MHA_OK) return st;
+  return run_linear(M2, N2, K, dtype, X2, K, W2, b2, Y2, N2, ctx, s);
+}
+
 // K slices for a weight-gradient GEMM whose 128 x 128 tiles alone would fill the SMs badly:
 // the smallest split whose work units fill >= 90% of their last round (else the best of
 // 1..8), with at least 8 K blocks of 64 per slice
@@ -816,11 +845,10 @@ int layer_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dtype,
   } else {
     uint8_t* qb = ws + plan.off_q;
     uint8_t* kvb = ws + plan.off_kv;
-    st = run_linear(Mq, nqk, D, dtype, x_q, D, W_qkv, b_qkv, qb, nqk, ctx, stream);
-    if (st != MHA_OK) return st;
     const int ldkv = nqk + nv;
-    st = run_linear(Mk, ldkv, D, dtype, x_kv, D, Wb + static_cast<size_t>(nqk) * D * es,
-                    bq ? bq + nqk * es : nullptr, kvb, ldkv, ctx, stream);
+    st = run_linear_two(Mq, nqk, x_q, W_qkv, b_qkv, qb, Mk, ldkv, x_kv,
+                        Wb + static_cast<size_t>(nqk) * D * es, bq ? bq + nqk * es : nullptr,
+                        kvb, D, dtype, ctx, stream);
     if (st != MHA_OK) return st;
     a.Q = qb;
     a.K = kvb;
@@ -1298,10 +1326,9 @@ int layer_bwd_impl(int B, int H, int Nq, int Nk, int D, int d_k, int d_v, int dt
     a.V = qbuf + 2 * nqk * es;
   } else {
     if (recompute) {
-      MHA_TRY(run_linear(Mq, nqk, D, dtype, x_q, D, W_qkv, b_qkv, qbuf, nqk, ctx, stream));
-      MHA_TRY(run_linear(Mk, pl.ld_kv, D, dtype, x_kv, D,
-                         Wb + static_cast<size_t>(nqk) * D * es, bq ? bq + nqk * es : nullptr,
-                         kvbuf, pl.ld_kv, ctx, stream));
+      MHA_TRY(run_linear_two(Mq, nqk, x_q, W_qkv, b_qkv, qbuf, Mk, pl.ld_kv, x_kv,
+                             Wb + static_cast<size_t>(nqk) * D * es,
+                             bq ? bq + nqk * es : nullptr, kvbuf, D, dtype, ctx, stream));
     }
     a.Q = qbuf;
     a.K = kvbuf;

@@ -63,14 +63,23 @@ struct GemmShape {
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators; a power of two
 };
 
-template <int BN, bool kRelu, bool kAcc, bool kMN>
+// A second problem with the same K that the same launch works through after the first one's
+// tiles (kTwo: the query and the key|value projections of cross-attention)
+struct GemmSecond {
+  CUtensorMap tmX, tmW, tmY;
+  const __nv_bfloat16* bias;
+  int M, N;
+};
+
+template <int BN, bool kRelu, bool kAcc, bool kMN, bool kTwo = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bias_bf16_kernel(const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmW,
                           const __grid_constant__ CUtensorMap tmY,
                           const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ Y,
                           int M, int N, int K, int64_t ldy, int* status, uint64_t timeout_ns,
-                          const __nv_bfloat16* __restrict__ R, int ksplit) {
+                          const __nv_bfloat16* __restrict__ R, int ksplit,
+                          const __grid_constant__ GemmSecond g2) {
   using S = GemmShape<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,7 +95,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_kb = kMN ? (K + kBK - 1) / kBK : K / kBK;
   const int tiles_n = (N + BN - 1) / BN;
-  const int tiles = tiles_n * ((M + kBM - 1) / kBM);
+  const int tiles1 = tiles_n * ((M + kBM - 1) / kBM);
+  int tiles_n2 = 0, tiles2 = 0;
+  if constexpr (kTwo) {  // the second problem's tiles follow the first's (ksplit is 1)
+    tiles_n2 = (g2.N + BN - 1) / BN;
+    tiles2 = tiles_n2 * ((g2.M + kBM - 1) / kBM);
+  }
+  const int tiles = tiles1 + tiles2;
+  // tile -> its problem (second), first row and column
+  auto tile_pos = [&](int tile, bool& second, int& m0, int& n0) {
+    second = kTwo && tile >= tiles1;
+    if (second) {
+      const int t2 = tile - tiles1;
+      m0 = (t2 / tiles_n2) * kBM;
+      n0 = (t2 % tiles_n2) * BN;
+    } else {
+      m0 = (tile / tiles_n) * kBM;
+      n0 = (tile % tiles_n) * BN;
+    }
+  };
   // work unit u: tile u % tiles, K slice u / tiles (units running together share K slices)
   const int units = tiles * ksplit;
   auto kb_begin = [&](int u) { return (u / tiles) * num_kb / ksplit; };
@@ -127,10 +154,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmW);
     int it = 0;
     bool ok = true;
+    if constexpr (kTwo) {
+      prefetch_tmap(&g2.tmX);
+      prefetch_tmap(&g2.tmW);
+    }
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-      const int tile = u % tiles;
-      const int m0 = (tile / tiles_n) * kBM;
-      const int n0 = (tile % tiles_n) * BN;
+      bool second;
+      int m0, n0;
+      tile_pos(u % tiles, second, m0, n0);
+      const CUtensorMap* mx = second ? &g2.tmX : &tmX;
+      const CUtensorMap* mw = second ? &g2.tmW : &tmW;
       for (int kb = kb_begin(u), kb1 = kb_end(u); kb < kb1; ++kb, ++it) {
         const int s = it % S::kStages;
         if (!mbar_wait_backoff(empty_bar(s), ((it / S::kStages) & 1) ^ 1, timeout_ns)) {
@@ -149,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(sB + s * S::kBBytes + c * 8192), &tmW, full_bar(s), n0 + c * 64,
                         kb * kBK);
         } else {
-          tma_load_2d(smem_u32(sA + s * S::kABytes), &tmX, full_bar(s), kb * kBK, m0);
-          tma_load_2d(smem_u32(sB + s * S::kBBytes), &tmW, full_bar(s), kb * kBK, n0);
+          tma_load_2d(smem_u32(sA + s * S::kABytes), mx, full_bar(s), kb * kBK, m0);
+          tma_load_2d(smem_u32(sB + s * S::kBBytes), mw, full_bar(s), kb * kBK, n0);
         }
       }
     }
@@ -203,10 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tcount = 0;
     int box = 0;  // staging boxes used so far (alternating)
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++tcount) {
-      const int tile = u % tiles;
       const int buf = tcount & 1;
-      const int m0 = (tile / tiles_n) * kBM;
-      const int n0 = (tile % tiles_n) * BN;
+      bool second;
+      int m0, n0;
+      tile_pos(u % tiles, second, m0, n0);
+      const int Mt = second ? g2.M : M;  // this tile's problem
+      const int Nt = second ? g2.N : N;
+      const CUtensorMap* my = second ? &g2.tmY : &tmY;
+      const __nv_bfloat16* bias_t = second ? g2.bias : bias;
       const int row = m0 + quarter * 32 + lane;
       if (!__all_sync(0xffffffffu, mbar_wait(acc_full(buf), (tcount >> 1) & 1, timeout_ns))) {
         record_error(status, kErrTimeout, kSiteGemmEpilogue);
@@ -237,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(acc_empty(buf));
         }
         const int col = n0 + c * 64;
-        if (wrow0 >= M || col >= N) continue;  // nothing of this box is inside Y
+        if (wrow0 >= Mt || col >= Nt) continue;  // nothing of this box is inside Y
         if constexpr (kAcc) {
           // two 32 x 32 fp32 boxes (128-byte rows, swizzled) added into the fp32 buffer
 #pragma unroll
@@ -261,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         float bv[64];
-        if (bias != nullptr && span_ok(col, 64, N, status, kSiteGemmBias)) {
-          const uint4* bp = reinterpret_cast<const uint4*>(bias + col);
+        if (bias_t != nullptr && span_ok(col, 64, Nt, status, kSiteGemmBias)) {
+          const uint4* bp = reinterpret_cast<const uint4*>(bias_t + col);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             uint4 u = __ldg(bp + v);
@@ -316,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {  // rows past M are not written
-          tma_store_2d(&tmY, sb, col, wrow0);
+          tma_store_2d(my, sb, col, wrow0);
           bulk_commit_group();
         }
       }
@@ -338,22 +375,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, bool kRelu, bool kAcc, bool kMN = false>
+template <int BN, bool kRelu, bool kAcc, bool kMN = false, bool kTwo = false>
 cudaError_t launch_bn(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY,
                       const void* bias, void* Y,
                       int M, int N, int K, int64_t ldy, const DevCtx& ctx, cudaStream_t s,
-                      const void* R, int ksplit) {
+                      const void* R, int ksplit, const GemmSecond& g2 = GemmSecond{}) {
   using S = GemmShape<BN>;
-  auto kern = gemm_bias_bf16_kernel<BN, kRelu, kAcc, kMN>;
+  auto kern = gemm_bias_bf16_kernel<BN, kRelu, kAcc, kMN, kTwo>;
   cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), S::kSmemBytes, nullptr);
   if (e != cudaSuccess) return e;
-  const int64_t units =
-      static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM) * ksplit;
+  int64_t units = static_cast<int64_t>((N + BN - 1) / BN) * ((M + kBM - 1) / kBM) * ksplit;
+  if (kTwo) units += static_cast<int64_t>((g2.N + BN - 1) / BN) * ((g2.M + kBM - 1) / kBM);
   const int grid = static_cast<int>(units < ctx.num_sms ? units : ctx.num_sms);
   return launch_pdl(kern, dim3(grid), dim3(kThreads), S::kSmemBytes, s, tmX, tmW, tmY,
                     static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(Y), M,
                     N, K, ldy, ctx.status, ctx.timeout_ns, static_cast<const __nv_bfloat16*>(R),
-                    ksplit);
+                    ksplit, g2);
 }
 
 // acc [M, N] fp32 -> Y bf16 (row pitch ldy), 8 values per thread
@@ -393,6 +430,25 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
   if (block_n == 256)
     return launch_bn<256, false, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
   return launch_bn<128, false, false>(tmX, tmW, tmY, bias, Y, M, N, K, ldy, ctx, s, R, 1);
+}
+
+cudaError_t launch_gemm_bf16_two(const CUtensorMap& tmX1, const CUtensorMap& tmW1,
+                                 const CUtensorMap& tmY1, const void* bias1, int M1, int N1,
+                                 const CUtensorMap& tmX2, const CUtensorMap& tmW2,
+                                 const CUtensorMap& tmY2, const void* bias2, int M2, int N2,
+                                 int K, int block_n, const DevCtx& ctx, cudaStream_t s) {
+  GemmSecond g2;
+  g2.tmX = tmX2;
+  g2.tmW = tmW2;
+  g2.tmY = tmY2;
+  g2.bias = static_cast<const __nv_bfloat16*>(bias2);
+  g2.M = M2;
+  g2.N = N2;
+  if (block_n == 256)
+    return launch_bn<256, false, false, false, true>(tmX1, tmW1, tmY1, bias1, nullptr, M1, N1, K,
+                                                     N1, ctx, s, nullptr, 1, g2);
+  return launch_bn<128, false, false, false, true>(tmX1, tmW1, tmY1, bias1, nullptr, M1, N1, K,
+                                                   N1, ctx, s, nullptr, 1, g2);
 }
 
 cudaError_t launch_gemm_bf16_mn(const CUtensorMap& tmX, const CUtensorMap& tmW,

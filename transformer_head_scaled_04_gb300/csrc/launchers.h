@@ -60,6 +60,14 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmX, const CUtensorMap& tmW,
                              bool relu, const void* bias, void* Y, int M, int N, int K,
                              int64_t ldy, const DevCtx& ctx, cudaStream_t s,
                              const void* residual = nullptr);
+// Two such GEMMs with the same K (no ReLU, no residual) in one launch: the persistent CTAs
+// work through the first problem's tiles and then the second's, so two small projections
+// share one fill of the GPU.  Both sets of maps as for launch_gemm_bf16 with this block_n.
+cudaError_t launch_gemm_bf16_two(const CUtensorMap& tmX1, const CUtensorMap& tmW1,
+                                 const CUtensorMap& tmY1, const void* bias1, int M1, int N1,
+                                 const CUtensorMap& tmX2, const CUtensorMap& tmW2,
+                                 const CUtensorMap& tmY2, const void* bias2, int M2, int N2,
+                                 int K, int block_n, const DevCtx& ctx, cudaStream_t s);
 // The same GEMM on pairs of SMs (gemm2_bf16.cu): a cluster of two CTAs per 256 x 256 output
 // tile, one pair-granularity MMA (M = 256) with half of each operand in each CTA.  tmX: box
 // {64, 128}; tmW: box {64, 128}; tmY: box {64, 32}.  Needs K % 64 == 0 and N % 64 == 0.
