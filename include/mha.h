@@ -388,6 +388,19 @@ int mha_linear_relu_fwd(int M, int N, int K, int dtype, const void* X, int64_t l
                         cudaStream_t stream);
 
 /*
+ * mha_linear2_fwd -- two projections with the same K in one launch:
+ *     Y1[M1,N1] = X1[M1,K] W1[N1,K]^T + b1[N1],   Y2[M2,N2] = X2[M2,K] W2[N2,K]^T + b2[N2]
+ * the query projection of the decoder states and the key|value projection of the encoder
+ * output in encoder-decoder attention ([LT] 3.2.3: queries from the previous decoder layer,
+ * keys and values from the encoder output).  All matrices dense (row pitch K for X1, X2, W1,
+ * W2; N1 and N2 for Y1 and Y2); b1, b2 may be NULL.  Y1 and Y2 equal what two mha_linear_fwd
+ * calls write, bit for bit.  Limits and errors as mha_linear_fwd for each problem.
+ */
+int mha_linear2_fwd(int M1, int N1, const void* X1, const void* W1, const void* b1, void* Y1,
+                    int M2, int N2, const void* X2, const void* W2, const void* b2, void* Y2,
+                    int K, int dtype, cudaStream_t stream);
+
+/*
  * mha_ffn_workspace_size -- bytes of device workspace mha_ffn_fwd needs: the hidden
  * activations [M, d_ff] and the second linear map's output [M, D].
  */

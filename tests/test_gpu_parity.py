@@ -338,6 +338,28 @@ def test_linear_bf16_pair_tiles(M, N, K, bias, relu):
     assert_bf16_close(host(Y), ref, f"linear bf16 pair tiles {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M1, N1, M2, N2, K", [(4096, 512, 8192, 1024, 512),
+                                               (300, 128, 1000, 192, 64),
+                                               (8192, 1024, 16384, 2048, 1024)])
+def test_linear2_bf16(M1, N1, M2, N2, K):
+    """The two projections of encoder-decoder attention in one launch: each output equals its
+    own mha_linear_fwd call bit for bit and the oracle within the bf16 bound (the last case
+    is large enough that each problem alone would take the pair-SM form: two launches)."""
+    g = np.random.Generator(np.random.PCG64(M1 + N2 * 3 + K))
+    X1 = si.round_bf16(g.standard_normal((M1, K)))
+    X2 = si.round_bf16(g.standard_normal((M2, K)))
+    W1 = si.round_bf16(g.uniform(-0.04, 0.04, (N1, K)))
+    W2 = si.round_bf16(g.uniform(-0.04, 0.04, (N2, K)))
+    b1 = si.round_bf16(0.1 * g.standard_normal(N1))
+    b2 = si.round_bf16(0.1 * g.standard_normal(N2))
+    d = [to_dev(a, torch.bfloat16) for a in (X1, W1, b1, X2, W2, b2)]
+    y1, y2 = mha.linear2(*d)
+    assert torch.equal(y1, mha.linear(d[0], d[1], d[2]))
+    assert torch.equal(y2, mha.linear(d[3], d[4], d[5]))
+    assert_bf16_close(host(y1), oracle.linear_ref(X1, W1, b1), f"linear2 first {M1}x{N1}x{K}")
+    assert_bf16_close(host(y2), oracle.linear_ref(X2, W2, b2), f"linear2 second {M2}x{N2}x{K}")
+
+
 def test_linear_bf16_row_pitch():
     g = np.random.Generator(np.random.PCG64(3))
     X = si.round_bf16(g.standard_normal((257, 320)))

@@ -22,6 +22,7 @@ from .api import (  # noqa: F401
     layer_bwd_workspace_size,
     layer_workspace_size,
     linear,
+    linear2,
     mha_layer,
     mha_layer_backward,
     mha_layer_forward_train,

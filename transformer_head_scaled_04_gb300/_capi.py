@@ -46,6 +46,8 @@ PROTOTYPES = {
     "mha_layer_fwd_host": (_c_int, [_c_int] * 8 + [_vp, _c_float] + [_vp] * 8 + [_c_int, _vp,
                                                                                   _size, _vp]),
     "mha_linear_fwd": (_c_int, [_c_int] * 4 + [_vp, _i64, _vp, _vp, _vp, _i64, _vp]),
+    "mha_linear2_fwd": (_c_int, [_c_int] * 2 + [_vp] * 4 + [_c_int] * 2 + [_vp] * 4
+                        + [_c_int] * 2 + [_vp]),
     "mha_linear_relu_fwd": (_c_int, [_c_int] * 4 + [_vp, _i64, _vp, _vp, _vp, _i64, _vp]),
     "mha_ffn_workspace_size": (_c_int, [_c_int] * 4 + [ctypes.POINTER(_size)]),
     "mha_ffn_fwd": (_c_int, [_c_int] * 4 + [_c_float] + [_vp] * 9 + [_size, _vp]),

@@ -291,6 +291,25 @@ def linear(x, W, bias=None, out=None, relu=False):
     return out
 
 
+def linear2(x1, W1, b1, x2, W2, b2):
+    """(x1 W1^T + b1, x2 W2^T + b2) in one launch via ``mha_linear2_fwd``; dense x1 [M1,K],
+    W1 [N1,K], x2 [M2,K], W2 [N2,K] (the two projections of encoder-decoder attention)."""
+    _cuda(x1, W1, b1, x2, W2, b2)
+    _contiguous("linear2", x1, W1, b1, x2, W2, b2)
+    (M1, K), (M2, K2) = x1.shape, x2.shape
+    N1, N2 = W1.shape[0], W2.shape[0]
+    if K2 != K or W1.shape[1] != K or W2.shape[1] != K:
+        raise ValueError("linear2: x1, W1, x2, W2 must share K")
+    y1 = torch.empty((M1, N1), dtype=x1.dtype, device=x1.device)
+    y2 = torch.empty((M2, N2), dtype=x1.dtype, device=x1.device)
+    with torch.cuda.device(x1.device):
+        code = C.load().mha_linear2_fwd(M1, N1, _ptr(x1), _ptr(W1), _ptr(b1), _ptr(y1), M2, N2,
+                                        _ptr(x2), _ptr(W2), _ptr(b2), _ptr(y2), K, _dt(x1),
+                                        _stream(x1.device))
+    C.check(code, "mha_linear2_fwd")
+    return y1, y2
+
+
 def ffn_workspace_size(M, D, d_ff, dtype) -> int:
     n = ctypes.c_size_t(0)
     dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)

@@ -992,6 +992,20 @@ int mha_linear_fwd(int M, int N, int K, int dtype, const void* X, int64_t ldx, c
   return run_linear(M, N, K, dtype, X, ldx, W, bias, Y, ldy, ctx, stream);
 }
 
+int mha_linear2_fwd(int M1, int N1, const void* X1, const void* W1, const void* b1, void* Y1,
+                    int M2, int N2, const void* X2, const void* W2, const void* b2, void* Y2,
+                    int K, int dtype, cudaStream_t stream) {
+  MHA_NVTX_RANGE("mha_linear2_fwd");
+  int st = check_linear(M1, N1, K, dtype, X1, K, W1, b1, Y1, N1);
+  if (st != MHA_OK) return st;
+  st = check_linear(M2, N2, K, dtype, X2, K, W2, b2, Y2, N2);
+  if (st != MHA_OK) return st;
+  DevCtx ctx;
+  const int sc = device_ctx(&ctx);
+  if (sc != MHA_OK) return sc;
+  return run_linear_two(M1, N1, X1, W1, b1, Y1, M2, N2, X2, W2, b2, Y2, K, dtype, ctx, stream);
+}
+
 }  // extern "C"
 
 namespace {
