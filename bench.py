@@ -1209,8 +1209,27 @@ def run_profile_case(args):
         return lambda: mha_pkg.mha_layer_backward(xs, None, Wl, zq, Wol, zo, ones, zo, H, dyl,
                                                   "none", workspace=wsl)
 
+    def decode_case():
+        # one generation step of the bench's decode leg (its own sizes, not --batch): Nq = 1
+        # new query per sequence against full caches of DECODE_L positions, 1.07 GB
+        g3 = torch.Generator(device=dev).manual_seed(20260013)
+        Bd, L = DECODE_B, DECODE_L
+        qd = torch.randn(Bd, H, 1, d, device=dev, generator=g3).to(bf)
+        kc = torch.randn(Bd, H, L, d, device=dev, generator=g3).to(bf)
+        vc = torch.randn(Bd, H, L, d, device=dev, generator=g3).to(bf)
+        cl = torch.full((Bd,), L, dtype=torch.int32, device=dev)
+        od = torch.empty_like(qd)
+        nd = ctypes.c_size_t(0)
+        C.check(lib.mha_decode_workspace_size(Bd, H, 1, L, C.MHA_BF16, ctypes.byref(nd)), "ws")
+        wsd = torch.empty(nd.value, dtype=torch.uint8, device=dev)
+        a = (Bd, H, 1, L, d, d, C.MHA_BF16, 1, vp(cl), 0.0, vp(qd), vp(kc), vp(vc), vp(od),
+             None, vp(wsd), nd.value, sp)
+        return lambda: C.check(lib.mha_sdpa_decode_fwd(*a), "mha_sdpa_decode_fwd")
+
     if args.profile_case == "layer_bwd":
         fn = layer_bwd_case()
+    elif args.profile_case == "decode":
+        fn = decode_case()
     else:
         fwd()
         fn = {"sdpa_fwd": fwd, "sdpa_bwd": bwd, "gemm_qkv": qkv, "layernorm": layernorm,
@@ -1226,6 +1245,8 @@ def run_profile_case(args):
         e1.record()
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
+    if args.profile_case == "decode":
+        B, N = DECODE_B, DECODE_L  # the decode case's own sizes (N: cached positions)
     print(json.dumps({"profile_case": args.profile_case, "B": B, "H": H, "n": N, "d": d,
                       "ms": float(np.mean(ms)), "status": int(lib.mha_debug_last_device_status(None))}))
     return 0
@@ -1241,7 +1262,7 @@ def main():
                     help="skip the timed CPU oracle sample")
     ap.add_argument("--profile-case",
                     choices=["sdpa_fwd", "sdpa_bwd", "gemm_qkv", "layernorm", "layer_bwd",
-                             "out_proj_ln"],
+                             "out_proj_ln", "decode"],
                     default=None,
                     help="run only this kernel family (for ncu captures), no bench line")
     ap.add_argument("--batch", type=int, default=4, help="batch of --profile-case")
